@@ -1,0 +1,169 @@
+"""Plain CPU oracle for MLX grouped affine quantization (test infrastructure).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never loads it, and the two share no code: the oracle is
+the C file ``qmm_oracle.c`` next to this module, compiled with gcc and loaded
+through ctypes.  The arithmetic it follows is described, with the passages of
+the pages it restates, at the top of that file.
+
+All arrays are numpy arrays on the host:
+  packed  uint32 [rows, cols*bits/32]   scales/biases uint16 (bf16 bits) [rows, cols/G]
+  x       uint16 (bf16 bits) [M, K]     idx uint32 [n]
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "qmm_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force=False):
+    """Compile the oracle with gcc (plain C99, no fast-math, no contraction)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + ".%d.tmp" % os.getpid()
+    cmd = ["gcc", "-std=gnu99", "-O2", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-pthread", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        I = ctypes.c_int
+        lib.oracle_code.argtypes = [P, I64, I]
+        lib.oracle_code.restype = ctypes.c_uint32
+        lib.oracle_unpack.argtypes = [P, I64, I64, I, P]
+        lib.oracle_pack.argtypes = [P, I64, I64, I, P]
+        lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_f32.restype = ctypes.c_float
+        lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+        lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_dequantize.argtypes = [P, P, P, I64, I64, I, I, I, P, I]
+        lib.oracle_rows.argtypes = [P, P, P, I64, I64, P, I64, I, I, I, P, I]
+        lib.oracle_rows.restype = I64
+        lib.oracle_qmm.argtypes = [P, I64, P, P, P, I64, I64, I, I, I, P, P, I]
+        lib.oracle_qmm_sampled.argtypes = [P, I64, P, P, P, I64, I64, I, I, I,
+                                           P, P, I64, P, P, I]
+        _lib = lib
+    return _lib
+
+
+def default_threads():
+    return os.cpu_count() or 1
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+def code(row_words, j, bits):
+    w, p = _c(row_words, np.uint32)
+    return int(_load().oracle_code(p, j, bits))
+
+
+def unpack(packed, cols, bits):
+    """codes uint8 [rows, cols] from packed uint32 [rows, cols*bits/32]."""
+    packed, p = _c(packed, np.uint32)
+    rows = packed.shape[0] if packed.ndim == 2 else 1
+    out = np.empty((rows, cols), dtype=np.uint8)
+    _load().oracle_unpack(p, rows, cols, bits, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def pack(codes, bits):
+    """packed uint32 [rows, cols*bits/32] from codes [rows, cols]."""
+    codes, p = _c(np.atleast_2d(codes), np.uint8)
+    rows, cols = codes.shape
+    out = np.empty((rows, cols * bits // 32), dtype=np.uint32)
+    _load().oracle_pack(p, rows, cols, bits, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def bf16_to_f32(h):
+    return float(_load().oracle_bf16_to_f32(int(h)))
+
+
+def f32_to_bf16(f):
+    return int(_load().oracle_f32_to_bf16(float(f)))
+
+
+def f32_to_bf16_array(a):
+    lib = _load()
+    flat = np.asarray(a, dtype=np.float32).ravel()
+    return np.array([lib.oracle_f32_to_bf16(float(v)) for v in flat],
+                    dtype=np.uint16).reshape(np.shape(a))
+
+
+def dequantize(packed, scales, biases, rows, cols, group_size, bits,
+               out_dtype="f32", nthreads=None):
+    """dequant(W) as float32 [rows, cols], or bf16 bits (uint16) if out_dtype='bf16'."""
+    packed, pp = _c(packed, np.uint32)
+    scales, ps = _c(scales, np.uint16)
+    biases, pb = _c(biases, np.uint16)
+    bf16 = out_dtype == "bf16"
+    out = np.empty((rows, cols), dtype=np.uint16 if bf16 else np.float32)
+    _load().oracle_dequantize(pp, ps, pb, rows, cols, group_size, bits, int(bf16),
+                              out.ctypes.data_as(ctypes.c_void_p),
+                              nthreads or default_threads())
+    return out
+
+
+def rows(packed, scales, biases, table_rows, cols, idx, group_size, bits,
+         out_dtype="bf16", nthreads=None):
+    """(out [n, cols], number of out-of-table indices)."""
+    packed, pp = _c(packed, np.uint32)
+    scales, ps = _c(scales, np.uint16)
+    biases, pb = _c(biases, np.uint16)
+    idx, pi = _c(idx, np.uint32)
+    bf16 = out_dtype == "bf16"
+    out = np.empty((idx.size, cols), dtype=np.uint16 if bf16 else np.float32)
+    bad = _load().oracle_rows(pp, ps, pb, table_rows, cols, pi, idx.size, group_size,
+                              bits, int(bf16), out.ctypes.data_as(ctypes.c_void_p),
+                              nthreads or default_threads())
+    return out, int(bad)
+
+
+def qmm(x, M, packed, scales, biases, N, K, transpose, group_size, bits, nthreads=None):
+    """(y, absy): fp64 [M, N] each; absy = sum_k |x*w|, the tolerance scale."""
+    x, px = _c(x, np.uint16)
+    packed, pp = _c(packed, np.uint32)
+    scales, ps = _c(scales, np.uint16)
+    biases, pb = _c(biases, np.uint16)
+    y = np.empty((M, N), dtype=np.float64)
+    a = np.empty((M, N), dtype=np.float64)
+    _load().oracle_qmm(px, M, pp, ps, pb, N, K, int(bool(transpose)), group_size, bits,
+                       y.ctypes.data_as(ctypes.c_void_p), a.ctypes.data_as(ctypes.c_void_p),
+                       nthreads or default_threads())
+    return y, a
+
+
+def qmm_sampled(x, M, packed, scales, biases, N, K, transpose, group_size, bits,
+                ms, ns, nthreads=None):
+    """(y, absy) at the sampled positions (ms[i], ns[i])."""
+    x, px = _c(x, np.uint16)
+    packed, pp = _c(packed, np.uint32)
+    scales, ps = _c(scales, np.uint16)
+    biases, pb = _c(biases, np.uint16)
+    ms, pm = _c(ms, np.int64)
+    ns, pn = _c(ns, np.int64)
+    y = np.empty(ms.size, dtype=np.float64)
+    a = np.empty(ms.size, dtype=np.float64)
+    _load().oracle_qmm_sampled(px, M, pp, ps, pb, N, K, int(bool(transpose)), group_size,
+                               bits, pm, pn, ms.size, y.ctypes.data_as(ctypes.c_void_p),
+                               a.ctypes.data_as(ctypes.c_void_p),
+                               nthreads or default_threads())
+    return y, a

@@ -1,0 +1,270 @@
+"""Pins for the CPU oracle: each test checks the oracle against something
+other than itself -- values printed on the pages (tests/golden), a library
+routine (numpy's bit unpacker, torch's bf16 rounding, numpy matmul), closed
+forms and brute force on tiny shapes.  A plausible mistake in the oracle (MSB
+first, bias subtracted, bias dropped, a wrong group index, a transposed
+operand, truncation instead of round-to-nearest-even) fails at least one."""
+import numpy as np
+import pytest
+
+import oracle
+from mlx_grouped_affine_gb300 import synth
+from conftest import ints, load_golden
+
+ALL_BITS = (1, 2, 3, 4, 5, 6, 8)
+
+
+# -- independent helpers (numpy / torch library routines) -------------------
+
+def np_codes(packed, cols, bits):
+    """Codes via numpy's unpackbits on the little-endian bytes of the words."""
+    packed = np.atleast_2d(np.asarray(packed, dtype="<u4"))
+    stream = np.unpackbits(packed.view(np.uint8), axis=1, bitorder="little")
+    stream = stream[:, : cols * bits].reshape(packed.shape[0], cols, bits).astype(np.uint32)
+    return (stream << np.arange(bits, dtype=np.uint32)).sum(axis=2).astype(np.uint32)
+
+
+def bf16_f64(u16):
+    return (np.asarray(u16, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def np_dense_f64(w):
+    """dequant(W) in fp64 with numpy's unpacker and np.repeat for the groups."""
+    c = np_codes(w.packed, w.cols, w.bits).astype(np.float64)
+    s = np.repeat(bf16_f64(w.scales), w.group_size, axis=1)
+    b = np.repeat(bf16_f64(w.biases), w.group_size, axis=1)
+    return s * c + b
+
+
+def torch_bf16_bits(f32):
+    torch = pytest.importorskip("torch")
+    t = torch.from_numpy(np.ascontiguousarray(f32, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().astype(np.uint16)
+
+
+# -- values printed on the pages ---------------------------------------------
+
+def _golden_weight(g):
+    words = np.array(ints(g["words"]), dtype=np.uint32)[None, :]
+    bits, cols, gs = int(g["bits"][0]), int(g["cols"][0]), int(g["group_size"][0])
+    groups = cols // gs
+    s = np.full((1, groups), int(g["scale_bf16"][0], 0), dtype=np.uint16)
+    b = np.full((1, groups), int(g["bias_bf16"][0], 0), dtype=np.uint16)
+    return words, s, b, cols, gs, bits
+
+
+def test_lsb_first_plus_bias():
+    g = load_golden("lsb_first_plus_bias.txt")
+    words, s, b, cols, gs, bits = _golden_weight(g)
+    out = oracle.dequantize(words, s, b, 1, cols, gs, bits, "f32")
+    assert out.ravel().tolist() == [float(v) for v in g["expect_f32"]]
+    assert oracle.unpack(words, cols, bits).ravel().tolist() == ints(g["codes"])
+
+
+def test_identity_shape():
+    g = load_golden("identity_shape.txt")
+    words, s, b, cols, gs, bits = _golden_weight(g)
+    out = oracle.dequantize(words, s, b, 1, cols, gs, bits, "f32")
+    assert out.size == int(g["expect_len"][0])
+    assert out.ravel().tolist() == [float(v) for v in g["expect_f32"]]
+
+
+def test_int8_byte_layout():
+    g = load_golden("int8_byte_layout.txt")
+    words = np.array(ints(g["words"]), dtype=np.uint32)
+    codes = oracle.unpack(words, int(g["cols"][0]), int(g["bits"][0]))
+    assert codes.ravel().tolist() == ints(g["codes"])
+
+
+def test_pack_shape():
+    g = load_golden("pack_shape.txt")
+    rows, cols = ints(g["weight_shape"])
+    bits = int(g["bits"][0])
+    codes = np.arange(rows * cols, dtype=np.uint8).reshape(rows, cols) % (1 << bits)
+    packed = oracle.pack(codes, bits)
+    assert list(packed.shape) == ints(g["packed_shape"])
+    assert oracle.unpack(packed, cols, bits).shape == (rows, cols)
+
+
+def test_three_bit_stream_by_hand():
+    g = load_golden("three_bit_stream.txt")
+    codes = np.array(ints(g["codes"]), dtype=np.uint8)[None, :]
+    packed = oracle.pack(codes, int(g["bits"][0]))
+    assert packed.ravel().tolist() == ints(g["words"])
+    assert oracle.unpack(packed, codes.shape[1], 3).ravel().tolist() == ints(g["codes"])
+
+
+def test_constant_weight_matmul():
+    g = load_golden("constant_weight_matmul.txt")
+    N, K, bits, gs = (int(g[k][0]) for k in ("N", "K", "bits", "group_size"))
+    packed = np.zeros((N, K * bits // 32), dtype=np.uint32)
+    x = np.full((1, K), 0x3F80, dtype=np.uint16)            # ones
+    s = np.full((N, K // gs), 0x3F80, dtype=np.uint16)      # 1.0
+    for bias, want in zip(g["bias_values"], g["expect_y"]):
+        bias_bits = int(np.float32(float(bias)).view(np.uint32) >> 16)
+        b = np.full((N, K // gs), bias_bits, dtype=np.uint16)
+        y, a = oracle.qmm(x, 1, packed, s, b, N, K, True, gs, bits)
+        assert (y == float(want)).all() and (a == float(want)).all()
+
+
+# -- library routines and closed forms --------------------------------------
+
+@pytest.mark.parametrize("bits", ALL_BITS)
+def test_unpack_matches_numpy_unpackbits(bits):
+    g = synth.rng(100 + bits)
+    cols = 256
+    packed = synth.random_words(g, 5, cols, bits)
+    assert (oracle.unpack(packed, cols, bits) == np_codes(packed, cols, bits)).all()
+
+
+@pytest.mark.parametrize("bits", ALL_BITS)
+def test_pack_unpack_round_trip(bits):
+    g = synth.rng(200 + bits)
+    packed = synth.random_words(g, 3, 128, bits)
+    codes = oracle.unpack(packed, 128, bits)
+    assert codes.max() <= (1 << bits) - 1
+    assert (oracle.pack(codes, bits) == packed).all()
+
+
+@pytest.mark.parametrize("bits", ALL_BITS)
+def test_zero_codes_give_bias(bits):
+    w = synth.quant_weight(7, 6, 128, bits, 32)
+    w.packed[:] = 0
+    out = oracle.dequantize(w.packed, w.scales, w.biases, 6, 128, 32, bits, "f32")
+    assert (out.astype(np.float64) == np.repeat(bf16_f64(w.biases), 32, axis=1)).all()
+
+
+@pytest.mark.parametrize("bits", ALL_BITS)
+@pytest.mark.parametrize("gs", (32, 64, 128))
+def test_dequant_f32_is_exact_value_rounded_once(bits, gs):
+    """fp32 dequant = the exact fp64 s*c+b rounded once to fp32 (the product is
+    exact, so only the add rounds); group index from np.repeat."""
+    w = synth.quant_weight(1000 + 10 * bits + gs, 7, 256, bits, gs)
+    out = oracle.dequantize(w.packed, w.scales, w.biases, 7, 256, gs, bits, "f32")
+    assert (out == np_dense_f64(w).astype(np.float32)).all()
+
+
+def test_bf16_rounding_matches_torch():
+    g = synth.rng(5)
+    vals = np.concatenate([
+        g.standard_normal(4000).astype(np.float32) * 10.0,
+        # exact ties between two bf16 values, both parities
+        ((np.arange(64, dtype=np.uint32) << 16) | 0x8000 | 0x3F800000).view(np.float32),
+        np.array([0.0, -0.0, 1e-40, -3e-39, 3.3895314e38, np.inf, -np.inf], np.float32),
+    ])
+    mine = oracle.f32_to_bf16_array(vals)
+    assert (mine == torch_bf16_bits(vals)).all()
+    nan = oracle.f32_to_bf16(float("nan"))
+    assert (nan & 0x7F80) == 0x7F80 and (nan & 0x7F) != 0
+
+
+@pytest.mark.parametrize("bits", (3, 4, 8))
+def test_dequant_bf16_is_rne_of_f32(bits):
+    w = synth.quant_weight(11, 9, 512, bits, 64)
+    f = oracle.dequantize(w.packed, w.scales, w.biases, 9, 512, 64, bits, "f32")
+    h = oracle.dequantize(w.packed, w.scales, w.biases, 9, 512, 64, bits, "bf16")
+    assert (h == torch_bf16_bits(f)).all()
+
+
+def test_thread_count_does_not_change_results():
+    w = synth.quant_weight(12, 33, 256, 5, 32)
+    a = oracle.dequantize(w.packed, w.scales, w.biases, 33, 256, 32, 5, "f32", nthreads=1)
+    b = oracle.dequantize(w.packed, w.scales, w.biases, 33, 256, 32, 5, "f32", nthreads=7)
+    assert (a == b).all()
+
+
+# -- matmul -------------------------------------------------------------------
+
+def _brute_force(x_u16, dense_kn):
+    """A naive triple loop over (m, n, k) in Python floats (fp64)."""
+    x = bf16_f64(x_u16)
+    M, K = x.shape
+    N = dense_kn.shape[1]
+    y = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):
+                acc += x[m, k] * dense_kn[k, n]
+            y[m, n] = acc
+    return y
+
+
+@pytest.mark.parametrize("bits", ALL_BITS)
+@pytest.mark.parametrize("K", (32, 64, 128))
+@pytest.mark.parametrize("transpose", (True, False))
+def test_qmm_brute_force_tiny(bits, K, transpose):
+    M, N = 3, 8 if transpose else 32        # transpose=False packs along N
+    gs = 32
+    x = synth.x_bf16(300 + bits, M, K)
+    if transpose:
+        w = synth.quant_weight(400 + bits + K, N, K, bits, gs)   # stored [N, K]
+        dense_kn = np_dense_f64(w).T
+    else:
+        w = synth.quant_weight(500 + bits + K, K, N, bits, gs)   # stored [K, N]
+        dense_kn = np_dense_f64(w)
+    y, a = oracle.qmm(x, M, w.packed, w.scales, w.biases, N, K, transpose, gs, bits)
+    want = _brute_force(x, dense_kn)
+    assert np.allclose(y, want, rtol=1e-12, atol=1e-12)
+    want_abs = np.abs(bf16_f64(x))[:, :, None] * np.abs(dense_kn)[None, :, :]
+    assert np.allclose(a, want_abs.sum(axis=1), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("transpose", (True, False))
+def test_qmm_matches_numpy_matmul(transpose):
+    M, K, bits, gs = 5, 256, 4, 64
+    N = 96 if transpose else 128            # packed along N when not transposed
+    x = synth.x_bf16(21, M, K)
+    if transpose:
+        w = synth.quant_weight(22, N, K, bits, gs)
+        dense_kn = np_dense_f64(w).T
+    else:
+        w = synth.quant_weight(23, K, N, bits, gs)
+        dense_kn = np_dense_f64(w)
+    y, _ = oracle.qmm(x, M, w.packed, w.scales, w.biases, N, K, transpose, gs, bits)
+    assert np.allclose(y, bf16_f64(x) @ dense_kn, rtol=1e-12, atol=1e-12)
+
+
+def test_transpose_flag_is_not_a_no_op():
+    """With a square weight the two layouts give different products."""
+    K = N = 64
+    x = synth.x_bf16(31, 2, K)
+    w = synth.quant_weight(32, N, K, 4, 32)
+    y_t, _ = oracle.qmm(x, 2, w.packed, w.scales, w.biases, N, K, True, 32, 4)
+    y_n, _ = oracle.qmm(x, 2, w.packed, w.scales, w.biases, N, K, False, 32, 4)
+    dense = np_dense_f64(w)
+    assert np.allclose(y_t, bf16_f64(x) @ dense.T, rtol=1e-12)
+    assert np.allclose(y_n, bf16_f64(x) @ dense, rtol=1e-12)
+    assert not np.allclose(y_t, y_n)
+
+
+def test_qmm_sampled_matches_full():
+    M, N, K = 4, 64, 128
+    x = synth.x_bf16(41, M, K)
+    w = synth.quant_weight(42, N, K, 6, 64)
+    y, a = oracle.qmm(x, M, w.packed, w.scales, w.biases, N, K, True, 64, 6)
+    g = synth.rng(43)
+    ms = g.integers(0, M, 50)
+    ns = g.integers(0, N, 50)
+    ys, as_ = oracle.qmm_sampled(x, M, w.packed, w.scales, w.biases, N, K, True, 64, 6, ms, ns)
+    assert (ys == y[ms, ns]).all() and (as_ == a[ms, ns]).all()
+
+
+# -- rows -------------------------------------------------------------------
+
+def test_rows_is_a_gather_of_dequantize():
+    w = synth.quant_weight(51, 40, 256, 3, 64)
+    idx = np.array([5, 0, 39, 5, 17], dtype=np.uint32)
+    out, bad = oracle.rows(w.packed, w.scales, w.biases, 40, 256, idx, 64, 3, "f32")
+    dense = np_dense_f64(w).astype(np.float32)
+    assert bad == 0 and (out == dense[idx]).all()
+
+
+def test_rows_out_of_table_gives_zero_row():
+    w = synth.quant_weight(52, 10, 64, 4, 32)
+    idx = np.array([3, 10, 4000000000, 9], dtype=np.uint32)
+    out, bad = oracle.rows(w.packed, w.scales, w.biases, 10, 64, idx, 32, 4, "bf16")
+    assert bad == 2
+    assert (out[1] == 0).all() and (out[2] == 0).all()
+    full = oracle.dequantize(w.packed, w.scales, w.biases, 10, 64, 32, 4, "bf16")
+    assert (out[0] == full[3]).all() and (out[3] == full[9]).all()
