@@ -1,0 +1,342 @@
+"""Benchmark of the quantized_matmul hot path on GB300.
+
+One step = one pass of the decode workload over a batch of R independent
+4-bit weights W_r [4096, 4096] (group 64), y_r = x . dequant(W_r)^T with
+x [1, 4096] -- like R layers of a decode step.  R is chosen so the weights
+span more than 3x the L2 cache, so every launch streams its weight from HBM.
+The R launches are captured once in a CUDA graph and replayed; time is taken
+with CUDA events on the launching stream.
+
+`value` is the step's algorithmic bytes (packed codes + scales + biases + x +
+y, per launch) over the step time, in GB/s.  `detail` carries the other
+decode shapes (M in 1, 4, 8, 16 at 4 and 8 bits), the prefill GEMM in TFLOP/s
+and the dequantize / rows throughputs, each measured the same way.
+
+`--impl reference` times the CPU oracle (plain C, all host cores) on a bounded
+sample of the same workload: this is the only reference there is, since the
+pages publish no implementation that runs here.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantized_matmul GB/s (M=1) and TFLOP/s (M=2048), % of HBM / bf16 TC roofline"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["source"] = "fallback"
+    return d
+
+
+def gemv_bytes(M, N, K, bits, group):
+    """Algorithmic bytes of one launch: codes + scales + biases + x + y (bf16)."""
+    return N * K * bits // 8 + 4 * N * (K // group) + 2 * M * K + 2 * M * N
+
+
+# ------------------------------------------------------------------ clocks ---
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.device = device
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append(parts)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(p[0]) for p in self.samples if p[0].replace(".", "").isdigit()]
+        mx = [float(p[1]) for p in self.samples if p[1].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for p in self.samples for n, v in zip(names, p[4:8]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------- GPU ----
+
+class Case:
+    """R rotating weights and one CUDA graph of R quantized_matmul launches."""
+
+    def __init__(self, torch, qmm, synth, M, N, K, bits, group, transpose=True, seed=1,
+                 min_bytes=3 * L2_BYTES, max_copies=64):
+        self.torch, self.qmm = torch, qmm
+        self.M, self.N, self.K, self.bits, self.group, self.transpose = M, N, K, bits, group, transpose
+        rows, cols = (N, K) if transpose else (K, N)
+        base = synth.quant_weight(seed, rows, cols, bits, group)
+        per = base.nbytes
+        self.R = int(max(1, min(max_copies, -(-min_bytes // per))))
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(
+            {np.dtype(np.uint32): np.int32, np.dtype(np.uint16): np.int16}[a.dtype])).cuda()
+        # Copies differ by a rotation of the random words, so no two are equal.
+        self.w = []
+        for r in range(self.R):
+            self.w.append((dev(np.roll(base.packed, r, axis=0)), dev(np.roll(base.scales, r, axis=0)),
+                           dev(np.roll(base.biases, r, axis=0))))
+        self.x_host = synth.x_bf16(seed + 1000, M, K)
+        self.x = torch.from_numpy(self.x_host.view(np.int16)).cuda()
+        self.y = torch.empty((self.R, M, N), dtype=torch.int16, device="cuda")
+        self.graph = None
+
+    def launch_all(self):
+        for r in range(self.R):
+            pw, ps, pb = self.w[r]
+            self.qmm.qmm_quantized_matmul(self.x, self.M, pw, ps, pb, self.N, self.K,
+                                          int(self.transpose), self.group, self.bits, self.y[r],
+                                          self.qmm.QMM_BF16)
+
+    def capture(self):
+        torch = self.torch
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.launch_all()                 # eager once (and warms the library)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.launch_all()
+        torch.cuda.synchronize()
+
+    def bytes_per_launch(self):
+        return gemv_bytes(self.M, self.N, self.K, self.bits, self.group)
+
+    def flops_per_launch(self):
+        return 2 * self.M * self.N * self.K
+
+
+def time_graph(torch, graph, steps, warmup, barrier=None):
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        graph.replay()
+    end.record()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return start.elapsed_time(end) / steps  # ms per step
+
+
+def run_gpu(args):
+    import torch
+    from mlx_grouped_affine_gb300 import qmm, synth
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    barrier = (lambda: dist.barrier()) if dist else None
+    peaks = load_peaks()
+    qmm.lib()
+
+    N, K = synth.DECODE_SHAPE
+    head = Case(torch, qmm, synth, 1, N, K, 4, 64, seed=1 + rank)
+    head.capture()
+    with ClockSampler(local) as clk:
+        ms = time_graph(torch, head.graph, args.steps, args.warmup, barrier)
+    clocks = clk.summary()
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    launch_ms = ms / head.R
+    per_launch = head.bytes_per_launch()
+    value = world * head.R * per_launch / (ms * 1e-3) / 1e9
+    achieved = per_launch / (launch_ms * 1e-3) / 1e9
+
+    # End to end through the public API with host buffers: per step, x for the
+    # R launches comes from pinned host memory and y goes back to it.
+    x_pin = torch.from_numpy(np.repeat(head.x_host.view(np.int16)[None], head.R, 0)).pin_memory()
+    y_pin = torch.empty((head.R, 1, N), dtype=torch.int16).pin_memory()
+    x_dev = torch.empty_like(x_pin, device="cuda")
+    def e2e_step():
+        x_dev.copy_(x_pin, non_blocking=True)
+        for r in range(head.R):
+            pw, ps, pb = head.w[r]
+            qmm.qmm_quantized_matmul(x_dev[r], 1, pw, ps, pb, N, K, 1, 64, 4, head.y[r], qmm.QMM_BF16)
+        y_pin.copy_(head.y, non_blocking=True)
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(10, min(args.steps, 200))
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / e_steps
+    e2e = {"value": world * head.R * per_launch / e2e_s / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": int(x_pin.numel() * 2), "d2h_bytes_per_step": int(y_pin.numel() * 2)}
+
+    detail = {}
+    if rank == 0 and not args.quick:
+        for bits in (4, 8):
+            for M in synth.DECODE_M:
+                c = Case(torch, qmm, synth, M, N, K, bits, 64, seed=10 + bits + M)
+                c.capture()
+                t = time_graph(torch, c.graph, max(20, args.steps // 4), args.warmup) / c.R
+                detail["decode_b%d_M%d" % (bits, M)] = {
+                    "us": round(t * 1e3, 3), "GB/s": round(c.bytes_per_launch() / (t * 1e-3) / 1e9, 1),
+                    "frac_hbm": round(c.bytes_per_launch() / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
+                del c
+                torch.cuda.empty_cache()
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u4->bf16",
+        "data": "synthetic (seeded uniform codes, bf16 scales/biases, N(0,1) x)",
+        "config": {"workload": "decode GEMV x[1,4096] . W[4096,4096]^T, 4-bit, group 64, bf16 out",
+                   "launches_per_step": head.R, "weight_copies_bytes": head.R * per_launch,
+                   "l2": "inputs larger than L2: %d rotating weight copies (> 3x L2)" % head.R,
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": None, "peak_source": peaks["source"]},
+        "clocks": clocks, "e2e": e2e, "gpu_launches": args.steps * head.R,
+        "detail": detail,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return out if rank == 0 else None
+
+
+# ------------------------------------------------------------------- CPU ----
+
+def cpu_baseline(budget_s=15.0, steps=None):
+    """The oracle, as it stands, on all host cores: whole problems of the
+    headline workload (x [1, 4096] . W[4096, 4096]^T at 4 bits), repeated
+    until about `budget_s` seconds have passed."""
+    import oracle
+    from mlx_grouped_affine_gb300 import synth
+    N, K = synth.DECODE_SHAPE
+    w = synth.quant_weight(1, N, K, 4, 64)
+    x = synth.x_bf16(1001, 1, K)
+    threads = oracle.default_threads()
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle.qmm(x, 1, w.packed, w.scales, w.biases, N, K, True, 64, 4, nthreads=threads)
+        done += 1
+        el = time.perf_counter() - t0
+        if (steps and done >= steps) or (not steps and el >= budget_s):
+            break
+    gbs = done * gemv_bytes(1, N, K, 4, 64) / el / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "%d full problems x[1,4096].W[4096,4096]^T 4-bit g64 in %.1f s" % (done, el)}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, timed per step on a bounded sample."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import oracle
+    from mlx_grouped_affine_gb300 import synth
+    N, K = synth.DECODE_SHAPE
+    w = synth.quant_weight(1, N, K, 4, 64)
+    x = synth.x_bf16(1001, 1, K)
+    threads = oracle.default_threads()
+    # Size a step (a slice of output columns) so that warmup + steps take
+    # about two minutes in all.
+    probe_rows = 256
+    t0 = time.perf_counter()
+    oracle.qmm(x, 1, w.packed[:probe_rows], w.scales[:probe_rows], w.biases[:probe_rows],
+               probe_rows, K, True, 64, 4, nthreads=threads)
+    per_row = (time.perf_counter() - t0) / probe_rows
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(max(16, min(N, budget / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        oracle.qmm(x, 1, w.packed[:rows], w.scales[:rows], w.biases[:rows], rows, K, True, 64, 4,
+                   nthreads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.qmm(x, 1, w.packed[:rows], w.scales[:rows], w.biases[:rows], rows, K, True, 64, 4,
+                   nthreads=threads)
+    el = time.perf_counter() - t0
+    step_bytes = gemv_bytes(1, rows, K, 4, 64)
+    value = args.steps * step_bytes / el / 1e9
+    sample = "first %d of 4096 weight rows per step (x[1,4096], 4-bit, group 64)" % rows
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": "decode GEMV x[1,4096] . W[4096,4096]^T, "
+                                            "4-bit, group 64 (CPU oracle sample)"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    p.add_argument("--quick", action="store_true", help="headline case only")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = p.parse_args()
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    out = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,142 @@
+/*
+ * qmm.h -- C ABI of the GB300 (sm_103a) library for MLX grouped affine
+ * quantization: dequantize, quantized_matmul and the rows gather-dequant.
+ *
+ * Packed format (nuvec_core quantized.rs, module doc; rlx-moshi
+ * src/mlx_dequant.rs, `dequantize_affine` doc; spark_runtime
+ * weights/mlx_int8.rs, module doc):
+ *   - A weight [rows, cols] stores `bits`-bit codes (bits in 1..6 or 8), each
+ *     row a little-endian bit stream packed into uint32 words: code j of a row
+ *     sits at stream bits [j*bits, (j+1)*bits), least significant bit first,
+ *     and stream bit i is bit (i mod 32) of word floor(i/32).  A row takes
+ *     cols*bits/32 words; rows are contiguous (row pitch cols*bits/8 bytes).
+ *     At 8 bits the low byte of a word is the first column.
+ *   - One bf16 scale and one bf16 bias per group of `group_size` (32, 64 or
+ *     128) consecutive codes of a row: scales and biases are bf16
+ *     [rows, cols/group_size], row-major.
+ *   - w = scale * code + bias.
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer is a DEVICE pointer owned by the caller (the library
+ *     allocates nothing on these paths and never frees caller memory, as
+ *     spark_runtime's `MlxInt8Weight` leaves buffers to their owner).  Every
+ *     pointer must be 16-byte aligned.  bf16 values are passed as their
+ *     16-bit patterns (uint16_t).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and run on the current CUDA device.  Results follow
+ *     stream order.
+ *   - Arguments are checked on the host before anything is launched.  A bad
+ *     argument returns QMM_ERR_INVALID_ARG, an unsupported dtype
+ *     QMM_ERR_UNSUPPORTED, and nothing runs.  A failed launch returns
+ *     QMM_ERR_CUDA.  qmm_last_error() then describes the failure.
+ *   - An empty output (zero rows, M == 0, N == 0 or n == 0) is a valid no-op.
+ *   - Outputs: QMM_F32 or QMM_BF16 (round to nearest even).
+ *
+ * Thread safety: calls may come from several host threads; the last-error
+ * message is per host thread.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *qmm_stream_t;
+
+typedef enum {
+    QMM_OK = 0,
+    QMM_ERR_INVALID_ARG = 1, /* shape, parameter, pointer or alignment rule broken */
+    QMM_ERR_UNSUPPORTED = 2, /* output dtype not supported */
+    QMM_ERR_CUDA = 3,        /* a CUDA call or launch failed */
+    QMM_ERR_INDEX = 4,       /* qmm_rows met an index outside the table */
+    QMM_ERR_TIMEOUT = 5      /* a bounded wait inside a kernel ran out */
+} qmm_status;
+
+typedef enum { QMM_F32 = 0, QMM_BF16 = 1 } qmm_dtype;
+
+/*
+ * qmm_dequantize -- out = dequant(W), contiguous [rows, cols].
+ * (nuvec_core quantized.rs, `dequantize`: code * scale + bias; rlx-moshi
+ *  src/mlx_dequant.rs, `dequantize_affine`; spark_runtime
+ *  weights/mlx_int8.rs, `dequantize_to`.)
+ *
+ *   w       uint32 [rows, cols*bits/32]
+ *   scales  bf16   [rows, cols/group_size]
+ *   biases  bf16   [rows, cols/group_size]
+ *   out     [rows, cols] of out_dtype
+ *
+ * Each element is fp32 scale*code + bias (the product is exact, one rounding
+ * at the add); QMM_F32 stores it as is, QMM_BF16 rounds it to nearest even.
+ * Rules: bits in {1,2,3,4,5,6,8}; group_size in {32,64,128}; cols > 0 and a
+ * multiple of group_size; rows >= 0.
+ */
+qmm_status qmm_dequantize(const uint32_t *w, const uint16_t *scales,
+                          const uint16_t *biases, int64_t rows, int64_t cols,
+                          int group_size, int bits, void *out,
+                          qmm_dtype out_dtype, qmm_stream_t stream);
+
+/*
+ * qmm_quantized_matmul -- y = x . dequant(W)^T (transpose = 1) or
+ * y = x . dequant(W) (transpose = 0), without materialising dequant(W).
+ * (nuvec_core quantized.rs, `quantized_matmul`; maya2_mlx quant.py, `mm`,
+ *  which always passes transpose=True for an [out, in] weight; spark_runtime
+ *  weights/mlx_int8.rs, `gemv` and `gemm`.)
+ *
+ *   x       bf16 [M, K]   (a 1-D x is M = 1; flatten batch dims into M)
+ *   transpose = 1: w uint32 [N, K*bits/32], scales/biases bf16 [N, K/group_size]
+ *   transpose = 0: w uint32 [K, N*bits/32], scales/biases bf16 [K, N/group_size]
+ *   y       [M, N] of y_dtype
+ *
+ * Accumulation is fp32 over weights rounded once to bf16; every output is
+ * within 8e-3 * sum_k |x[m,k] * w[k,n]| + 1e-6 of the exact product.
+ * Rules: bits and group_size as above; K > 0; the packed (last) axis of W a
+ * multiple of group_size (K when transpose, N otherwise); M, N >= 0;
+ * transpose in {0, 1}.  M <= 16 runs the decode kernel, larger M the
+ * tensor-core (tcgen05) kernel.
+ */
+qmm_status qmm_quantized_matmul(const uint16_t *x, int64_t M, const uint32_t *w,
+                                const uint16_t *scales, const uint16_t *biases,
+                                int64_t N, int64_t K, int transpose,
+                                int group_size, int bits, void *y,
+                                qmm_dtype y_dtype, qmm_stream_t stream);
+
+/*
+ * qmm_rows -- out[i, :] = dequant(W[idx[i], :]) for i < n: an embedding
+ * lookup that dequantizes only the gathered rows in one pass.
+ * (maya2_mlx quant.py, `rows`: dequantize(q[idx], scales[idx], biases[idx]).)
+ *
+ *   w, scales, biases  the table [table_rows, cols], laid out as for
+ *                      qmm_dequantize
+ *   idx     uint32 [n] device array of row indices (duplicates allowed)
+ *   out     [n, cols] of out_dtype
+ *
+ * An index >= table_rows gives a zero output row and records QMM_ERR_INDEX in
+ * the device error word (read by qmm_get_device_error); nothing faults.
+ */
+qmm_status qmm_rows(const uint32_t *w, const uint16_t *scales,
+                    const uint16_t *biases, int64_t table_rows, int64_t cols,
+                    const uint32_t *idx, int64_t n, int group_size, int bits,
+                    void *out, qmm_dtype out_dtype, qmm_stream_t stream);
+
+/* The message for the last non-OK status returned on this host thread
+ * (empty string if none).  The pointer stays valid until the next call. */
+const char *qmm_last_error(void);
+
+/*
+ * Synchronizes `stream`, then reads and clears the current device's error
+ * word: QMM_ERR_INDEX if a qmm_rows index was outside its table,
+ * QMM_ERR_TIMEOUT if a bounded wait in a kernel ran out (the kernel then
+ * stops early and its output is incomplete), QMM_ERR_CUDA if the
+ * synchronization itself failed, else QMM_OK.
+ */
+qmm_status qmm_get_device_error(qmm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */

@@ -1,0 +1,73 @@
+"""Builds the CUDA library libqmm.so in-tree with nvcc for sm_103a (GB300).
+
+Each source compiles to its own object in parallel under ``_build/``; the
+objects link into ``libqmm.so`` next to this file with the CUDA runtime linked
+statically, so the library loads (and its symbols can be inspected) on a
+machine without a GPU driver.
+"""
+import os
+import shutil
+import subprocess
+from concurrent.futures import ThreadPoolExecutor
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(HERE, "csrc")
+INCLUDE = os.path.join(os.path.dirname(HERE), "include")
+BUILD_DIR = os.path.join(HERE, "_build")
+LIBRARY = os.path.join(HERE, "libqmm.so")
+SOURCES = ("api.cpp", "dequant.cu", "gemv.cu", "gemm_sm103.cu")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def nvcc():
+    path = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(path):
+        raise RuntimeError("nvcc not found: the CUDA toolkit is needed to build libqmm.so")
+    return path
+
+
+def _inputs():
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    files.append(os.path.join(INCLUDE, "qmm.h"))
+    return files
+
+
+def up_to_date():
+    if not os.path.exists(LIBRARY):
+        return False
+    t = os.path.getmtime(LIBRARY)
+    return all(os.path.getmtime(f) <= t for f in _inputs())
+
+
+def _compile(src, extra):
+    obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+    cmd = [nvcc()] + ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+                             "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj] + extra
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("nvcc failed on %s:\n%s%s" % (src, r.stdout, r.stderr))
+    return obj, r.stderr
+
+
+def build(force=False, extra_flags=(), verbose=False):
+    """Compile and link libqmm.so; returns its path."""
+    if not force and up_to_date():
+        return LIBRARY
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    with ThreadPoolExecutor(max_workers=len(SOURCES)) as pool:
+        results = list(pool.map(lambda s: _compile(s, list(extra_flags)), SOURCES))
+    if verbose:
+        for _, log in results:
+            if log:
+                print(log)
+    tmp = LIBRARY + ".%d.tmp" % os.getpid()
+    cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + [o for o, _ in results]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("link failed:\n%s%s" % (r.stdout, r.stderr))
+    os.replace(tmp, LIBRARY)
+    return LIBRARY
+
+
+if __name__ == "__main__":
+    print(build(force=True, verbose=True))

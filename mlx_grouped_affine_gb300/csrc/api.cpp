@@ -1,0 +1,159 @@
+// The C ABI: argument checks, dispatch to the kernels, status codes and the
+// per-thread last-error message.
+//
+// The checks mirror the pages' rules: group size 32, 64 or 128 and bit width
+// 1-6 or 8 (nuvec_core quantized.rs, `check_params`); the grouped axis a
+// multiple of the group size and the packed axis equal to cols*bits/32
+// (rlx-moshi src/mlx_dequant.rs, `dequantize_affine`; spark_runtime
+// weights/mlx_int8.rs, `load`).  The library owns no buffer: every pointer is
+// the caller's (spark_runtime `MlxInt8Weight`, `release`).
+#include "../../include/qmm.h"
+#include "internal.h"
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+qmm_status fail(qmm_status st, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+qmm_status cuda_status(cudaError_t e, const char *what) {
+  if (e == cudaSuccess) return QMM_OK;
+  return fail(QMM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+qmm_status check_params(const char *op, int group_size, int bits) {
+  if (group_size != 32 && group_size != 64 && group_size != 128)
+    return fail(QMM_ERR_INVALID_ARG, "%s: group size %d is not supported (32, 64 or 128)", op,
+                group_size);
+  if (bits < 1 || bits > 8 || bits == 7)
+    return fail(QMM_ERR_INVALID_ARG, "%s: %d bits are not supported (1, 2, 3, 4, 5, 6 or 8)",
+                op, bits);
+  return QMM_OK;
+}
+
+qmm_status check_dtype(const char *op, qmm_dtype d) {
+  if (d != QMM_F32 && d != QMM_BF16)
+    return fail(QMM_ERR_UNSUPPORTED, "%s: output dtype %d is not supported (QMM_F32, QMM_BF16)",
+                op, static_cast<int>(d));
+  return QMM_OK;
+}
+
+// The packed weight [rows, cols]: grouped axis, pointers, alignment.
+qmm_status check_weight(const char *op, const uint32_t *w, const uint16_t *scales,
+                        const uint16_t *biases, int64_t rows, int64_t cols, int group_size) {
+  if (rows < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative row count %lld", op, (long long)rows);
+  if (cols <= 0 || cols % group_size != 0)
+    return fail(QMM_ERR_INVALID_ARG,
+                "%s: the grouped axis (%lld) must be positive and a multiple of group size %d", op,
+                (long long)cols, group_size);
+  if (cols > (int64_t(1) << 40) || rows > (int64_t(1) << 40))
+    return fail(QMM_ERR_INVALID_ARG, "%s: weight [%lld, %lld] is too large", op, (long long)rows,
+                (long long)cols);
+  if (!w || !scales || !biases)
+    return fail(QMM_ERR_INVALID_ARG, "%s: null weight, scales or biases pointer", op);
+  if (!aligned16(w) || !aligned16(scales) || !aligned16(biases))
+    return fail(QMM_ERR_INVALID_ARG, "%s: weight, scales and biases must be 16-byte aligned", op);
+  return QMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *qmm_last_error(void) { return g_last_error; }
+
+qmm_status qmm_dequantize(const uint32_t *w, const uint16_t *scales, const uint16_t *biases,
+                          int64_t rows, int64_t cols, int group_size, int bits, void *out,
+                          qmm_dtype out_dtype, qmm_stream_t stream) {
+  const char *op = "qmm_dequantize";
+  qmm_status st;
+  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
+  if ((st = check_dtype(op, out_dtype)) != QMM_OK) return st;
+  if ((st = check_weight(op, w, scales, biases, rows, cols, group_size)) != QMM_OK) return st;
+  if (rows == 0) return QMM_OK;
+  if (!out || !aligned16(out))
+    return fail(QMM_ERR_INVALID_ARG, "%s: output must be a non-null 16-byte aligned pointer", op);
+  qmm::PackedWeight pw{w, scales, biases, rows, cols, group_size, bits};
+  return cuda_status(qmm::launch_dequantize(pw, nullptr, rows, out, out_dtype == QMM_BF16,
+                                            reinterpret_cast<cudaStream_t>(stream)),
+                     op);
+}
+
+qmm_status qmm_rows(const uint32_t *w, const uint16_t *scales, const uint16_t *biases,
+                    int64_t table_rows, int64_t cols, const uint32_t *idx, int64_t n,
+                    int group_size, int bits, void *out, qmm_dtype out_dtype,
+                    qmm_stream_t stream) {
+  const char *op = "qmm_rows";
+  qmm_status st;
+  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
+  if ((st = check_dtype(op, out_dtype)) != QMM_OK) return st;
+  if ((st = check_weight(op, w, scales, biases, table_rows, cols, group_size)) != QMM_OK) return st;
+  if (n < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative index count %lld", op, (long long)n);
+  if (n == 0) return QMM_OK;
+  if (!idx || !aligned16(idx))
+    return fail(QMM_ERR_INVALID_ARG, "%s: indices must be a non-null 16-byte aligned pointer", op);
+  if (!out || !aligned16(out))
+    return fail(QMM_ERR_INVALID_ARG, "%s: output must be a non-null 16-byte aligned pointer", op);
+  qmm::PackedWeight pw{w, scales, biases, table_rows, cols, group_size, bits};
+  return cuda_status(qmm::launch_dequantize(pw, idx, n, out, out_dtype == QMM_BF16,
+                                            reinterpret_cast<cudaStream_t>(stream)),
+                     op);
+}
+
+qmm_status qmm_quantized_matmul(const uint16_t *x, int64_t M, const uint32_t *w,
+                                const uint16_t *scales, const uint16_t *biases, int64_t N,
+                                int64_t K, int transpose, int group_size, int bits, void *y,
+                                qmm_dtype y_dtype, qmm_stream_t stream) {
+  const char *op = "qmm_quantized_matmul";
+  qmm_status st;
+  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
+  if ((st = check_dtype(op, y_dtype)) != QMM_OK) return st;
+  if (transpose != 0 && transpose != 1)
+    return fail(QMM_ERR_INVALID_ARG, "%s: transpose must be 0 or 1, got %d", op, transpose);
+  if (M < 0 || N < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative M or N", op);
+  if (K <= 0) return fail(QMM_ERR_INVALID_ARG, "%s: K must be positive, got %lld", op, (long long)K);
+  // Stored weight: [N, K] when transposed, [K, N] otherwise; the packed,
+  // grouped axis is the stored last one.
+  const int64_t rows = transpose ? N : K, cols = transpose ? K : N;
+  if (transpose || N > 0) {
+    if ((st = check_weight(op, w, scales, biases, rows, cols, group_size)) != QMM_OK) return st;
+  }
+  if (M == 0 || N == 0) return QMM_OK;
+  if (!x || !aligned16(x))
+    return fail(QMM_ERR_INVALID_ARG, "%s: x must be a non-null 16-byte aligned pointer", op);
+  if (!y || !aligned16(y))
+    return fail(QMM_ERR_INVALID_ARG, "%s: y must be a non-null 16-byte aligned pointer", op);
+  if (M > (int64_t(1) << 31) || K > (int64_t(1) << 31) || N > (int64_t(1) << 31))
+    return fail(QMM_ERR_INVALID_ARG, "%s: M, N and K must each be below 2^31", op);
+  qmm::PackedWeight pw{w, scales, biases, rows, cols, group_size, bits};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool bf16 = y_dtype == QMM_BF16;
+  cudaError_t e = M <= 16 ? qmm::launch_gemv(x, M, pw, transpose != 0, y, bf16, s)
+                          : qmm::launch_gemm(x, M, pw, transpose != 0, y, bf16, s);
+  return cuda_status(e, op);
+}
+
+qmm_status qmm_get_device_error(qmm_stream_t stream) {
+  unsigned bits = 0;
+  cudaError_t e = qmm::take_device_error(reinterpret_cast<cudaStream_t>(stream), &bits);
+  if (e != cudaSuccess) return cuda_status(e, "qmm_get_device_error");
+  if (bits & qmm::kErrTimeoutBit)
+    return fail(QMM_ERR_TIMEOUT, "qmm_get_device_error: a bounded wait inside a kernel ran out");
+  if (bits & qmm::kErrIndexBit)
+    return fail(QMM_ERR_INDEX, "qmm_get_device_error: a qmm_rows index was outside its table");
+  return QMM_OK;
+}
+
+}  // extern "C"

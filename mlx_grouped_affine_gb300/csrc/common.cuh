@@ -1,0 +1,142 @@
+// Device helpers shared by the kernels: bf16 bit patterns, the packed-code
+// window reader and small PTX wrappers.  Format (nuvec_core quantized.rs,
+// module doc): a row is a little-endian bit stream of `bits`-bit codes in
+// uint32 words, code j at stream bits [j*bits, (j+1)*bits).
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace qmm {
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) {
+  return __uint_as_float(h << 16);  // exact widening
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));  // round to nearest even
+}
+
+// Two fp32 -> one bf16x2 register (lo in bits 0..15), each rounded to
+// nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// ---------------------------------------------------------------- PTX ----
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// (a & b) | c in one instruction.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// bf16x2 a - b and a*b + c, each lane rounded once to nearest even.
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ----------------------------------------------------- register dequant ----
+
+constexpr uint32_t kMagic = 0x43004300u;  // bf16x2 (128.0, 128.0)
+
+// Code j (0 <= j < n) of a little-endian bit stream held in words v[].
+template <int BITS>
+__device__ __forceinline__ uint32_t code_at(const uint32_t *v, int j) {
+  const int bit = j * BITS, word = bit >> 5, sh = bit & 31;
+  constexpr uint32_t mask = (1u << BITS) - 1u;
+  if (sh + BITS <= 32) return (v[word] >> sh) & mask;
+  return __funnelshift_r(v[word], v[word + 1], sh) & mask;
+}
+
+// Dequantize the 2*NP codes held in v[] (bit stream, LSB first) to NP bf16x2
+// natural pairs (code 2i in the low half, 2i+1 in the high half), each
+// RN(s*c + b).  s2, b2 are (s, s) and (b, b) in bf16x2; sf, bf the same in
+// fp32 (for 8-bit codes).
+template <int BITS, int NP>
+__device__ __forceinline__ void dequant_pairs(const uint32_t *v, uint32_t s2, uint32_t b2,
+                                              float sf, float bf, uint32_t *out) {
+  if constexpr (BITS == 4) {
+#pragma unroll
+    for (int q = 0; q < NP / 4; ++q) {
+      const uint32_t w = v[q], w4 = w >> 4;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        // byte i of w holds codes 8q+2i (low nibble) and 8q+2i+1 (high nibble)
+        const uint32_t t = prmt(w, w4, 0x0400u | (i << 8) | i);
+        const uint32_t c = bf16x2_sub(and_or(t, 0x000F000Fu, kMagic), kMagic);
+        out[4 * q + i] = bf16x2_fma(c, s2, b2);
+      }
+    }
+  } else if constexpr (BITS == 8) {
+#pragma unroll
+    for (int q = 0; q < NP / 2; ++q) {
+      const uint32_t w = v[q];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        // fp32 2^23 + byte, exact; minus 2^23 gives the code exactly.
+        const float c0 = __uint_as_float(prmt(w, 0x4B000000u, 0x7650u | (2 * i))) - 8388608.0f;
+        const float c1 = __uint_as_float(prmt(w, 0x4B000000u, 0x7650u | (2 * i + 1))) - 8388608.0f;
+        out[2 * q + i] = pack_bf16x2(__fmaf_rn(sf, c0, bf), __fmaf_rn(sf, c1, bf));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      const uint32_t p = code_at<BITS>(v, 2 * i) | (code_at<BITS>(v, 2 * i + 1) << 16) | kMagic;
+      out[i] = bf16x2_fma(bf16x2_sub(p, kMagic), s2, b2);
+    }
+  }
+}
+
+// Load n words from p (4-byte aligned, and 8/16-byte aligned when the width
+// allows it) as wide as the alignment lets us.
+template <int BITS>
+__device__ __forceinline__ void load_words(const uint32_t *__restrict__ p, uint32_t *v) {
+  if constexpr (BITS % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < BITS / 4; ++i) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p) + i);
+      v[4 * i] = u.x; v[4 * i + 1] = u.y; v[4 * i + 2] = u.z; v[4 * i + 3] = u.w;
+    }
+  } else if constexpr (BITS % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < BITS / 2; ++i) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p) + i);
+      v[2 * i] = u.x; v[2 * i + 1] = u.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < BITS; ++i) v[i] = __ldg(p + i);
+  }
+}
+
+__device__ __forceinline__ uint32_t bcast_bf16x2(uint16_t h) {
+  return static_cast<uint32_t>(h) * 0x00010001u;
+}
+
+}  // namespace qmm

@@ -1,0 +1,538 @@
+// Prefill path of quantized_matmul (M > 16) on the sm_103a tensor cores.
+//
+// y = x . dequant(W)^T (nuvec_core quantized.rs, `quantized_matmul`;
+// spark_runtime weights/mlx_int8.rs, `gemm`, whose naive kernel this
+// replaces).  The dequantized weight is never written to global memory: each
+// 256-row x 64-code tile of W is dequantized straight into shared memory,
+// where the tensor cores read it.
+//
+// One persistent block per SM walks output tiles of 128 x-rows by 256
+// weight-rows.  Its warps specialise:
+//   warp 0      TMA: x tiles [128 x 64] bf16 into a 128-byte-swizzled ring
+//   warp 1      allocates tensor memory and issues tcgen05.mma (one lane):
+//               D[128 x 256] fp32 in TMEM, two accumulators so the epilogue
+//               of one tile overlaps the main loop of the next
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator, convert, store y
+//   warps 6-13  dequantize: packed W -> bf16 (one rounding per weight,
+//               RN(scale * code + bias)) written in the same 128-byte swizzle
+//               the MMA descriptor expects, then fence.proxy.async and arrive
+// Stage hand-off uses mbarriers; every wait is bounded, and a wait that runs
+// out sets the device error word, makes every role stop, and the block still
+// waits for its own copies and MMAs and frees its tensor memory.
+//
+// Shared-memory tiles are K-major with the 128-byte swizzle: row r of a tile
+// is 128 bytes (64 bf16) at r*128, and its 16-byte chunk c sits at chunk
+// position c ^ (r % 8).  The UMMA descriptor gives stride 1024 bytes between
+// 8-row groups; a 16-wide K step inside the 64-wide atom advances the start
+// address by 32 bytes.
+#include "common.cuh"
+#include "internal.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace qmm {
+namespace {
+
+constexpr int BM = 128;   // x rows per tile (MMA M)
+constexpr int BN = 256;   // weight rows per tile (MMA N)
+constexpr int BK = 64;    // codes per stage: one 128-byte swizzle atom of bf16
+constexpr int STAGES = 4;
+constexpr int kEpiWarps = 4;
+constexpr int kDeqWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps + kDeqWarps);
+constexpr uint32_t A_BYTES = BM * BK * 2;
+constexpr uint32_t B_BYTES = BN * BK * 2;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr uint32_t kSpinLimit = 1u << 24;
+
+struct Barriers {
+  uint64_t full_a[STAGES], full_b[STAGES], empty[STAGES];
+  uint64_t tmem_full[2], tmem_empty[2], mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr size_t kSmemBytes = STAGES * (A_BYTES + B_BYTES) + sizeof(Barriers) + 1024;
+
+struct GemmArgs {
+  const uint32_t *w;
+  const uint16_t *scales, *biases;
+  void *y;
+  int M, N, K;
+  int group_shift;
+  int m_tiles, n_tiles;
+  unsigned *err;
+};
+
+// ------------------------------------------------------------- PTX glue ----
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count));
+}
+
+// One bounded poll: the thread may be suspended for at most kSuspendNs while
+// the phase is incomplete, so kSpinLimit polls take at most a few seconds.
+constexpr uint32_t kSuspendNs = 256;
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity), "n"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Whole-warp bounded wait for the phase of parity `parity` to complete.
+// Warp-uniform result: false if this wait ran out (the error word is set) or
+// another role already gave up.
+__device__ __noinline__ bool wait_warp(uint64_t *b, uint32_t parity, volatile int *abort,
+                                       unsigned *err) {
+  uint32_t spins = 0;
+  while (true) {
+    const bool done = mbar_try_wait(b, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+    if ((++spins & 255u) == 0) {
+      int stop = *abort;
+      if (!stop && spins > kSpinLimit) {
+        stop = 1;
+        *abort = 1;
+        atomicOr(err, kErrTimeoutBit);
+      }
+      if (__any_sync(0xffffffffu, stop)) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+// K-major, 128-byte swizzle, 8-row groups 1024 bytes apart (tcgen05 smem
+// matrix descriptor: start>>4 [0,14), LBO>>4 [16,30), SBO>>4 [32,46),
+// version 1 [46,48), swizzle mode [61,64) with 2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N = BN, M = BM.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                            (static_cast<uint32_t>(BN >> 3) << 17) |
+                            (static_cast<uint32_t>(BM >> 4) << 24);
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(kIdesc), "r"(acc));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint32_t (&v)[4]) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+
+// ---------------------------------------------------------------- roles ----
+
+// Dequant side: the 8-code chunk (k .. k+7) of weight row n.
+template <int BITS>
+struct ChunkLoad {
+  uint32_t win[2];
+  uint16_t s, b;
+};
+
+template <int BITS>
+__device__ __forceinline__ void load_chunk(const GemmArgs &a, int n, int k, ChunkLoad<BITS> &c) {
+  c.win[0] = c.win[1] = 0u;
+  c.s = c.b = 0;
+  if (n < a.N && k < a.K) {
+    const int64_t wpr = (static_cast<int64_t>(a.K) * BITS) >> 5;
+    const int cbit = k * BITS, cword = cbit >> 5, csh = cbit & 31;
+    const uint32_t *rp = a.w + static_cast<int64_t>(n) * wpr + cword;
+    const uint32_t lo = __ldg(rp);
+    const uint32_t hi = (csh + 8 * BITS > 32) ? __ldg(rp + 1) : 0u;
+    c.win[0] = csh ? __funnelshift_r(lo, hi, csh) : lo;
+    c.win[1] = csh ? (hi >> csh) : hi;
+    const int64_t g = static_cast<int64_t>(n) * (a.K >> a.group_shift) + (k >> a.group_shift);
+    c.s = __ldg(a.scales + g);
+    c.b = __ldg(a.biases + g);
+  }
+}
+
+template <int BITS>
+__device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int nk) {
+  const int dt = threadIdx.x - 32 * (2 + kEpiWarps);  // 0 .. 255
+  const int c = dt & 7, rbase = dt >> 3;               // chunk in the row, first row
+  const int num_tiles = a.m_tiles * a.n_tiles;
+  volatile int *abort = &bars->abort;
+  int tile = blockIdx.x, kb = 0;
+  if (tile >= num_tiles) return;
+  ChunkLoad<BITS> next[BN / 32];
+  auto prefetch = [&](int t, int kbi) {
+    const int n0 = (t / a.m_tiles) * BN;
+#pragma unroll
+    for (int i = 0; i < BN / 32; ++i) load_chunk<BITS>(a, n0 + rbase + 32 * i, kbi * BK + 8 * c, next[i]);
+  };
+  prefetch(tile, kb);
+  int s = 0;
+  uint32_t ph = 0;
+  while (tile < num_tiles) {
+    ChunkLoad<BITS> cur[BN / 32];
+#pragma unroll
+    for (int i = 0; i < BN / 32; ++i) cur[i] = next[i];
+    int nt = tile, nkb = kb + 1;
+    if (nkb == nk) { nkb = 0; nt += gridDim.x; }
+    if (nt < num_tiles) prefetch(nt, nkb);
+    if (!wait_warp(&bars->empty[s], ph ^ 1u, abort, a.err)) return;
+    const uint32_t base = smem_u32(sB + s * B_BYTES);
+#pragma unroll
+    for (int i = 0; i < BN / 32; ++i) {
+      const int r = rbase + 32 * i;
+      uint32_t v[4];
+      dequant_pairs<BITS, 4>(cur[i].win, bcast_bf16x2(cur[i].s), bcast_bf16x2(cur[i].b),
+                             bf16_bits_to_f32(cur[i].s), bf16_bits_to_f32(cur[i].b), v);
+      st_shared_v4(base + r * 128 + ((c ^ (r & 7)) << 4), v);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive(&bars->full_b[s]);
+    if (++s == STAGES) { s = 0; ph ^= 1u; }
+    tile = nt;
+    kb = nkb;
+  }
+}
+
+__device__ void tma_role(const CUtensorMap *tmap, const GemmArgs &a, uint8_t *sA, Barriers *bars,
+                         int nk) {
+  const int lane = threadIdx.x & 31;
+  const int num_tiles = a.m_tiles * a.n_tiles;
+  volatile int *abort = &bars->abort;
+  int s = 0;
+  uint32_t ph = 0;
+  // Parity of the last load issued into each stage that has not been seen to
+  // land, so that a role that stops early can wait for its copies.
+  int pending[STAGES];
+  for (int i = 0; i < STAGES; ++i) pending[i] = -1;
+  bool ok = true;
+  for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+    const int m0 = (tile % a.m_tiles) * BM;
+    for (int kb = 0; kb < nk; ++kb) {
+      if (!wait_warp(&bars->empty[s], ph ^ 1u, abort, a.err)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_expect_tx(&bars->full_a[s], A_BYTES);
+        tma_load_2d(smem_u32(sA + s * A_BYTES), tmap, kb * BK, m0, &bars->full_a[s]);
+      }
+      __syncwarp();
+      pending[s] = static_cast<int>(ph);
+      if (++s == STAGES) { s = 0; ph ^= 1u; }
+    }
+  }
+  if (!ok) {
+    // Stopped early: wait (bounded) for the copies still in flight.
+    for (int i = 0; i < STAGES; ++i) {
+      if (pending[i] < 0) continue;
+      for (uint32_t spin = 0; spin < kSpinLimit; ++spin)
+        if (__all_sync(0xffffffffu, mbar_try_wait(&bars->full_a[i], pending[i]))) break;
+    }
+  }
+}
+
+__device__ void mma_role(const GemmArgs &a, uint8_t *sA, uint8_t *sB, Barriers *bars, int nk,
+                         uint32_t tmem) {
+  const int lane = threadIdx.x & 31;
+  const int num_tiles = a.m_tiles * a.n_tiles;
+  volatile int *abort = &bars->abort;
+  int s = 0, it = 0;
+  uint32_t ph = 0;
+  bool ok = true;
+  for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++it) {
+    const int acc = it & 1;
+    const uint32_t aph = (it >> 1) & 1;
+    if (!wait_warp(&bars->tmem_empty[acc], aph ^ 1u, abort, a.err)) break;
+    tc_fence_after();
+    const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
+    for (int kb = 0; kb < nk; ++kb) {
+      if (!wait_warp(&bars->full_a[s], ph, abort, a.err) ||
+          !wait_warp(&bars->full_b[s], ph, abort, a.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint64_t da = sw128_kmajor_desc(smem_u32(sA + s * A_BYTES));
+        const uint64_t db = sw128_kmajor_desc(smem_u32(sB + s * B_BYTES));
+#pragma unroll
+        for (int j = 0; j < BK / 16; ++j)
+          umma(d_tmem, da + 2 * j, db + 2 * j, (kb | j) != 0 ? 1u : 0u);
+        umma_commit(&bars->empty[s]);
+      }
+      __syncwarp();
+      if (++s == STAGES) { s = 0; ph ^= 1u; }
+    }
+    if (!ok) break;
+    if (lane == 0) umma_commit(&bars->tmem_full[acc]);
+    __syncwarp();
+  }
+  // Retire every MMA this thread issued before the block frees TMEM.
+  if (lane == 0) umma_commit(&bars->mma_done);
+  __syncwarp();
+  for (uint32_t spin = 0; spin < kSpinLimit; ++spin)
+    if (__all_sync(0xffffffffu, mbar_try_wait(&bars->mma_done, 0))) break;
+}
+
+template <bool OUT_BF16>
+__device__ void epilogue_role(const GemmArgs &a, Barriers *bars, uint32_t tmem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3;  // TMEM lane quarter this warp may access
+  const int num_tiles = a.m_tiles * a.n_tiles;
+  volatile int *abort = &bars->abort;
+  const bool vec = OUT_BF16 ? (a.N % 8 == 0) : (a.N % 4 == 0);
+  int it = 0;
+  for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+    const int acc = it & 1;
+    const uint32_t aph = (it >> 1) & 1;
+    if (!wait_warp(&bars->tmem_full[acc], aph, abort, a.err)) return;
+    tc_fence_after();
+    const int m = (tile % a.m_tiles) * BM + 32 * q + lane;
+    const int n0 = (tile / a.m_tiles) * BN;
+#pragma unroll 1
+    for (int cc = 0; cc < BN / 32; ++cc) {
+      uint32_t r[32];
+      tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * BN + 32 * cc), r);
+      const int n = n0 + 32 * cc;
+      if (m >= a.M || n >= a.N) continue;
+      const int64_t o = static_cast<int64_t>(m) * a.N + n;
+      if (OUT_BF16) {
+        uint16_t *yp = static_cast<uint16_t *>(a.y) + o;
+        if (vec && n + 32 <= a.N) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 p;
+            p.x = pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
+            p.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
+            p.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
+            p.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
+            reinterpret_cast<uint4 *>(yp)[j] = p;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (n + j < a.N) yp[j] = f32_to_bf16_bits(__uint_as_float(r[j]));
+        }
+      } else {
+        float *yp = static_cast<float *>(a.y) + o;
+        if (vec && n + 32 <= a.N) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            reinterpret_cast<float4 *>(yp)[j] =
+                make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                            __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (n + j < a.N) yp[j] = __uint_as_float(r[j]);
+        }
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(&bars->tmem_empty[acc]);
+  }
+}
+
+template <int BITS, bool OUT_BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + STAGES * A_BYTES;
+  Barriers *bars = reinterpret_cast<Barriers *>(sB + STAGES * B_BYTES);
+  const int warp = threadIdx.x >> 5;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&bars->full_a[i], 1);
+      mbar_init(&bars->full_b[i], 32 * kDeqWarps);
+      mbar_init(&bars->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->tmem_full[i], 1);
+      mbar_init(&bars->tmem_empty[i], 32 * kEpiWarps);
+    }
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_x) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&bars->tmem_base)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const int nk = (a.K + BK - 1) / BK;
+
+  if (warp == 0) tma_role(&tmap_x, a, sA, bars, nk);
+  else if (warp == 1) mma_role(a, sA, sB, bars, nk, tmem);
+  else if (warp < 2 + kEpiWarps) epilogue_role<OUT_BF16>(a, bars, tmem);
+  else dequant_role<BITS>(a, sB, bars, nk);
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TMEM_COLS));
+  }
+}
+
+// ----------------------------------------------------------------- host ----
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  return n;
+}
+
+template <int BITS, bool OUT_BF16>
+cudaError_t launch_t(const uint16_t *x, const GemmArgs &a, cudaStream_t stream) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K) * 2};
+  const cuuint32_t box[2] = {BK, BM};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  auto kern = gemm_kernel<BITS, OUT_BF16>;
+  static bool attr_set = false;  // per instantiation
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int tiles = a.m_tiles * a.n_tiles;
+  const int grid = tiles < sm_count() ? tiles : sm_count();
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(map, a);
+  return cudaGetLastError();
+}
+
+template <int BITS>
+cudaError_t launch_bits(const uint16_t *x, const GemmArgs &a, bool y_bf16, cudaStream_t stream) {
+  return y_bf16 ? launch_t<BITS, true>(x, a, stream) : launch_t<BITS, false>(x, a, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const uint16_t *x, int64_t M, const PackedWeight &w, bool transpose,
+                        void *y, bool y_bf16, cudaStream_t stream) {
+  if (!transpose) return cudaErrorNotSupported;
+  GemmArgs a;
+  a.w = w.w;
+  a.scales = w.scales;
+  a.biases = w.biases;
+  a.y = y;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(w.rows);
+  a.K = static_cast<int>(w.cols);
+  a.group_shift = w.group == 32 ? 5 : w.group == 64 ? 6 : 7;
+  a.m_tiles = (a.M + BM - 1) / BM;
+  a.n_tiles = (a.N + BN - 1) / BN;
+  a.err = device_error_word();
+  if (!a.err) return cudaErrorInvalidSymbol;
+  switch (w.bits) {
+    case 1: return launch_bits<1>(x, a, y_bf16, stream);
+    case 2: return launch_bits<2>(x, a, y_bf16, stream);
+    case 3: return launch_bits<3>(x, a, y_bf16, stream);
+    case 4: return launch_bits<4>(x, a, y_bf16, stream);
+    case 5: return launch_bits<5>(x, a, y_bf16, stream);
+    case 6: return launch_bits<6>(x, a, y_bf16, stream);
+    case 8: return launch_bits<8>(x, a, y_bf16, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace qmm

@@ -1,0 +1,412 @@
+// Decode path of quantized_matmul: M <= 16 rows of x.
+//
+// y = x . dequant(W)^T (transpose) or x . dequant(W) (nuvec_core
+// quantized.rs, `quantized_matmul`; spark_runtime weights/mlx_int8.rs,
+// `gemv`).  The kernel streams the packed weight once from HBM; everything
+// else serves that stream:
+//
+//  * Each weight is dequantized in registers to bf16 with one rounding,
+//    w = RN(scale * code + bias), from exact bf16 codes.  For widths below 8
+//    a code c becomes the bf16 (128 + c) by OR-ing it into the mantissa of
+//    128.0, and 128 is then subtracted exactly.  8-bit codes go through fp32.
+//  * The products x * w and their fp32 sums run on the tensor pipe
+//    (mma.sync m16n8k16, bf16 in, fp32 accumulate) with the dequantized
+//    weights as the A operand straight from registers: at M <= 16 the FMA
+//    pipe would otherwise be the bottleneck, and no shared-memory round trip
+//    is needed.  x rows beyond M are zero.
+//  * K is split across the warps of a block (partials reduced through shared
+//    memory) and, when the weight has few rows, across the blocks of a thread
+//    block cluster (partials reduced through distributed shared memory).  No
+//    global scratch memory is used.
+//
+// Fragment layout of m16n8k16 (g = lane / 4, t = lane % 4):
+//   A 16x16: {a0a1} row g, k 2t..2t+1; {a2a3} row g+8, same k;
+//            {a4a5} row g, k 2t+8..; {a6a7} row g+8, k 2t+8..
+//   B 16x8:  {b0b1} k 2t..2t+1, col g; {b2b3} k 2t+8.., col g
+//   D 16x8:  d0,d1 row g, cols 2t, 2t+1; d2,d3 row g+8, cols 2t, 2t+1
+// The contraction index may be permuted freely as long as A and B agree.
+#include "common.cuh"
+#include "internal.h"
+
+namespace qmm {
+namespace {
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+struct GemvArgs {
+  const uint16_t *x;
+  const uint32_t *w;
+  const uint16_t *scales, *biases;
+  void *y;
+  int M, N, K;
+  int group_shift;
+  int parts;  // K parts = cluster size * warps per block
+};
+
+// ------------------------------------------------------------------------
+// Cross-warp and cross-block reduction of ACC fp32 values per lane, then the
+// store.  Every warp of every block in the cluster holds a partial of the
+// same output tile with the same lane -> (m, n) mapping.
+template <int ACC, typename MapFn>
+__device__ __forceinline__ void reduce_and_store(float (&acc)[ACC], float *red, int warps,
+                                                 int cluster, const GemvArgs &a, bool out_bf16,
+                                                 MapFn map) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int i = 0; i < ACC; ++i) red[(warp * ACC + i) * 32 + lane] = acc[i];
+  __syncthreads();
+  float sum[ACC];
+  if (warp == 0) {
+#pragma unroll
+    for (int i = 0; i < ACC; ++i) {
+      float s = 0.0f;
+      for (int w = 0; w < warps; ++w) s += red[(w * ACC + i) * 32 + lane];
+      sum[i] = s;
+    }
+  }
+  if (cluster > 1) {
+    // Block partials go to the first warp-slot of `red`; the leader block adds
+    // its peers' through distributed shared memory.
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+      for (int i = 0; i < ACC; ++i) red[i * 32 + lane] = sum[i];
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    uint32_t rank;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    if (rank == 0 && warp == 0) {
+      const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(red));
+      for (int r = 1; r < cluster; ++r) {
+        uint32_t remote;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(base), "r"(r));
+#pragma unroll
+        for (int i = 0; i < ACC; ++i) {
+          float v;
+          asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                       : "=f"(v) : "r"(remote + static_cast<uint32_t>((i * 32 + lane) * 4)));
+          sum[i] += v;
+        }
+      }
+    }
+    // Peers keep their shared memory alive until the leader has read it.
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (rank != 0) return;
+  }
+  if (warp != 0) return;
+#pragma unroll
+  for (int i = 0; i < ACC; ++i) {
+    int m, n;
+    map(lane, i, m, n);
+    if (m < a.M && n < a.N) {
+      const int64_t o = static_cast<int64_t>(m) * a.N + n;
+      if (out_bf16) static_cast<uint16_t *>(a.y)[o] = f32_to_bf16_bits(sum[i]);
+      else static_cast<float *>(a.y)[o] = sum[i];
+    }
+  }
+}
+
+// ------------------------------------------------------------------------
+// transpose = true: W stored [N, K].  A warp owns a 16-row tile and a range of
+// 128-code chunks of K.  In a chunk, lane (g, t) holds codes [32t, 32t+32) of
+// rows g and g+8: `BITS` words per row, loaded with the widest aligned loads.
+// Its 16 natural pairs per row feed 8 MMAs; MMA r contracts logical k
+// (2t, 2t+1) with physical codes 32t+4r, +1 and logical (2t+8, 2t+9) with
+// 32t+4r+2, +3, so the matching x values are the two words of x at
+// k = 32t + 4r: lane (g, t) reads x[m][32t .. 32t+32) with four 16-byte loads.
+template <int BITS, int NT, bool OUT_BF16>
+__global__ void __launch_bounds__(512)
+gemv_t_kernel(GemvArgs a) {
+  extern __shared__ float red[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, warps = blockDim.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  uint32_t crank = 0, csize = 1;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
+  const int n0 = blockIdx.x * 16;
+  const int part = static_cast<int>(crank) * warps + warp;
+  const int nchunks = (a.K + 127) >> 7;
+  const int c_begin = static_cast<int>(static_cast<int64_t>(nchunks) * part / a.parts);
+  const int c_end = static_cast<int>(static_cast<int64_t>(nchunks) * (part + 1) / a.parts);
+
+  const int64_t wpr = (static_cast<int64_t>(a.K) * BITS) >> 5;
+  const int groups = a.K >> a.group_shift;
+  const int row0 = n0 + g, row1 = n0 + g + 8;
+  const bool ok0 = row0 < a.N, ok1 = row1 < a.N;
+  const uint32_t *w0 = a.w + static_cast<int64_t>(ok0 ? row0 : 0) * wpr;
+  const uint32_t *w1 = a.w + static_cast<int64_t>(ok1 ? row1 : 0) * wpr;
+
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+
+  for (int c = c_begin; c < c_end; ++c) {
+    const int k = (c << 7) + 32 * t;  // first code of this lane's 32
+    const bool kin = k < a.K;
+    uint32_t v0[BITS], v1[BITS];
+#pragma unroll
+    for (int i = 0; i < BITS; ++i) { v0[i] = 0u; v1[i] = 0u; }
+    uint16_t s0 = 0, b0 = 0, s1 = 0, b1 = 0;
+    if (kin && ok0) {
+      load_words<BITS>(w0 + (k >> 5) * BITS, v0);
+      s0 = __ldg(a.scales + static_cast<int64_t>(row0) * groups + (k >> a.group_shift));
+      b0 = __ldg(a.biases + static_cast<int64_t>(row0) * groups + (k >> a.group_shift));
+    }
+    if (kin && ok1) {
+      load_words<BITS>(w1 + (k >> 5) * BITS, v1);
+      s1 = __ldg(a.scales + static_cast<int64_t>(row1) * groups + (k >> a.group_shift));
+      b1 = __ldg(a.biases + static_cast<int64_t>(row1) * groups + (k >> a.group_shift));
+    }
+    uint32_t xv[NT][16];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int m = g + 8 * nt;
+      if (kin && m < a.M) {
+        const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + static_cast<int64_t>(m) * a.K + k);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 u = __ldg(xp + i);
+          xv[nt][4 * i] = u.x; xv[nt][4 * i + 1] = u.y; xv[nt][4 * i + 2] = u.z; xv[nt][4 * i + 3] = u.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) xv[nt][i] = 0u;
+      }
+    }
+    uint32_t p0[16], p1[16];
+    dequant_pairs<BITS, 16>(v0, bcast_bf16x2(s0), bcast_bf16x2(b0), bf16_bits_to_f32(s0),
+                            bf16_bits_to_f32(b0), p0);
+    dequant_pairs<BITS, 16>(v1, bcast_bf16x2(s1), bcast_bf16x2(b1), bf16_bits_to_f32(s1),
+                            bf16_bits_to_f32(b1), p1);
+    if (!kin) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) { p0[i] = 0u; p1[i] = 0u; }
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        mma_bf16_16816(acc[nt], p0[2 * r], p1[2 * r], p0[2 * r + 1], p1[2 * r + 1],
+                       xv[nt][2 * r], xv[nt][2 * r + 1]);
+  }
+
+  float flat[NT * 4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) flat[nt * 4 + i] = acc[nt][i];
+  reduce_and_store<NT * 4>(flat, red, warps, static_cast<int>(csize), a, OUT_BF16,
+                           [&](int ln, int i, int &m, int &n) {
+                             const int gg = ln >> 2, tt = ln & 3, nt = i >> 2, e = i & 3;
+                             n = n0 + gg + 8 * (e >> 1);
+                             m = 8 * nt + 2 * tt + (e & 1);
+                           });
+}
+
+// ------------------------------------------------------------------------
+// transpose = false: W stored [K, N], packed and grouped along N.  A warp owns
+// a 32-column tile of y and a range of 16-row steps of K.  In a step, lane
+// (g, t) reads the 8 codes [8t, 8t+8) of the tile from stored rows k0+g and
+// k0+8+g (one 8-code chunk each) and dequantizes them to 4 natural pairs
+// along N.  Pair j of lane (g, t) is element (g, t) of an 8x8 bf16 block Q_j
+// whose rows are k and whose column 2t+e is n = 8t + 2j + e; movmatrix.trans
+// turns Q_j into the B fragment of n8-tile j, whose column c is
+// n = 8(c/2) + 2j + (c%2).  x is the A operand (natural pairs along K).
+template <int BITS, bool OUT_BF16>
+__global__ void __launch_bounds__(512)
+gemv_n_kernel(GemvArgs a) {
+  extern __shared__ float red[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, warps = blockDim.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  uint32_t crank = 0, csize = 1;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
+  const int n0 = blockIdx.x * 32;
+  const int part = static_cast<int>(crank) * warps + warp;
+  const int nsteps = (a.K + 15) >> 4;  // K (the stored row count) may be any size
+  const int s_begin = static_cast<int>(static_cast<int64_t>(nsteps) * part / a.parts);
+  const int s_end = static_cast<int>(static_cast<int64_t>(nsteps) * (part + 1) / a.parts);
+
+  const int64_t wpr = (static_cast<int64_t>(a.N) * BITS) >> 5;
+  const int groups = a.N >> a.group_shift;
+  const int nc = n0 + 8 * t;          // first column of this lane's chunk
+  const bool nok = nc < a.N;
+  const int gcol = nc >> a.group_shift;
+  // The chunk's codes start at bit 8*BITS*(nc/8) of a stored row.
+  const int cbit = BITS * nc, cword = cbit >> 5, csh = cbit & 31;
+  constexpr bool kTwoWords = (BITS == 8) || (BITS == 3) || (BITS == 5) || (BITS == 6);
+
+  float acc[4][4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[j][i] = 0.0f;
+
+  for (int s = s_begin; s < s_end; ++s) {
+    const int k0 = s << 4;
+    uint32_t bfrag[4][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int krow = k0 + 8 * h + g;
+      uint32_t win[2] = {0u, 0u};
+      uint16_t sv = 0, bv = 0;
+      if (nok && krow < a.K) {
+        const uint32_t *rp = a.w + static_cast<int64_t>(krow) * wpr + cword;
+        const uint32_t lo = __ldg(rp);
+        uint32_t hi = 0u;
+        if (kTwoWords && (csh + 8 * BITS > 32)) hi = __ldg(rp + 1);
+        win[0] = csh ? __funnelshift_r(lo, hi, csh) : lo;
+        win[1] = csh ? (hi >> csh) : hi;
+        sv = __ldg(a.scales + static_cast<int64_t>(krow) * groups + gcol);
+        bv = __ldg(a.biases + static_cast<int64_t>(krow) * groups + gcol);
+      }
+      uint32_t pr[4];
+      dequant_pairs<BITS, 4>(win, bcast_bf16x2(sv), bcast_bf16x2(bv), bf16_bits_to_f32(sv),
+                             bf16_bits_to_f32(bv), pr);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t tr;
+        asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(tr) : "r"(pr[j]));
+        bfrag[j][h] = tr;
+      }
+    }
+    // A = x rows g and g+8 (zero beyond M and K), natural pairs along K.  x
+    // rows need not be 4-byte aligned here (K may be odd): 16-bit loads.
+    uint32_t xa[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int m = g + 8 * (q & 1), kk = k0 + 2 * t + 8 * (q >> 1);
+      uint32_t lo = 0u, hi = 0u;
+      if (m < a.M) {
+        const uint16_t *xr = a.x + static_cast<int64_t>(m) * a.K;
+        if (kk < a.K) lo = __ldg(xr + kk);
+        if (kk + 1 < a.K) hi = __ldg(xr + kk + 1);
+      }
+      xa[q] = lo | (hi << 16);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      mma_bf16_16816(acc[j], xa[0], xa[1], xa[2], xa[3], bfrag[j][0], bfrag[j][1]);
+  }
+
+  float flat[16];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) flat[j * 4 + i] = acc[j][i];
+  reduce_and_store<16>(flat, red, warps, static_cast<int>(csize), a, OUT_BF16,
+                       [&](int ln, int i, int &m, int &n) {
+                         const int gg = ln >> 2, tt = ln & 3, j = i >> 2, e = i & 3;
+                         m = gg + 8 * (e >> 1);
+                         n = n0 + 8 * tt + 2 * j + (e & 1);
+                       });
+}
+
+// ------------------------------------------------------------------------
+
+struct Shape {
+  int warps, cluster;
+};
+
+// Split K over `warps` warps per block and `cluster` blocks so that about
+// 4096 warps stream the weight (enough loads in flight to cover HBM latency
+// on 152 SMs), without giving a warp less than one K step.
+Shape pick_shape(int64_t tiles, int64_t ksteps) {
+  int64_t split = (4096 + tiles - 1) / tiles;
+  if (split > ksteps) split = ksteps;
+  int p = 1;
+  while (p * 2 <= split && p < 128) p *= 2;
+  Shape s;
+  s.warps = p < 16 ? (p < 4 ? 4 : p) : 16;
+  s.cluster = p > 16 ? p / 16 : 1;
+  if (s.cluster > 8) s.cluster = 8;
+  return s;
+}
+
+template <typename Kern>
+cudaError_t launch_clustered(Kern kern, dim3 grid, Shape s, size_t smem, cudaStream_t stream,
+                             const GemvArgs &a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(32 * s.warps);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = s.cluster;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <int BITS, int NT, bool OUT_BF16>
+cudaError_t launch_t(const GemvArgs &a0, cudaStream_t stream) {
+  GemvArgs a = a0;
+  const int64_t tiles = (a.N + 15) / 16;
+  Shape s = pick_shape(tiles, (a.K + 127) / 128);
+  a.parts = s.warps * s.cluster;
+  const size_t smem = sizeof(float) * s.warps * NT * 4 * 32;
+  return launch_clustered(gemv_t_kernel<BITS, NT, OUT_BF16>, dim3(tiles, s.cluster), s, smem,
+                          stream, a);
+}
+
+template <int BITS, bool OUT_BF16>
+cudaError_t launch_n(const GemvArgs &a0, cudaStream_t stream) {
+  GemvArgs a = a0;
+  const int64_t tiles = (a.N + 31) / 32;
+  Shape s = pick_shape(tiles, (a.K + 15) / 16);
+  a.parts = s.warps * s.cluster;
+  const size_t smem = sizeof(float) * s.warps * 16 * 32;
+  return launch_clustered(gemv_n_kernel<BITS, OUT_BF16>, dim3(tiles, s.cluster), s, smem,
+                          stream, a);
+}
+
+template <int BITS>
+cudaError_t launch_bits(const GemvArgs &a, bool transpose, bool y_bf16, cudaStream_t stream) {
+  if (transpose) {
+    if (a.M <= 8) return y_bf16 ? launch_t<BITS, 1, true>(a, stream) : launch_t<BITS, 1, false>(a, stream);
+    return y_bf16 ? launch_t<BITS, 2, true>(a, stream) : launch_t<BITS, 2, false>(a, stream);
+  }
+  return y_bf16 ? launch_n<BITS, true>(a, stream) : launch_n<BITS, false>(a, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_gemv(const uint16_t *x, int64_t M, const PackedWeight &w, bool transpose,
+                        void *y, bool y_bf16, cudaStream_t stream) {
+  GemvArgs a;
+  a.x = x;
+  a.w = w.w;
+  a.scales = w.scales;
+  a.biases = w.biases;
+  a.y = y;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(transpose ? w.rows : w.cols);
+  a.K = static_cast<int>(transpose ? w.cols : w.rows);
+  a.group_shift = w.group == 32 ? 5 : w.group == 64 ? 6 : 7;
+  a.parts = 1;
+  switch (w.bits) {
+    case 1: return launch_bits<1>(a, transpose, y_bf16, stream);
+    case 2: return launch_bits<2>(a, transpose, y_bf16, stream);
+    case 3: return launch_bits<3>(a, transpose, y_bf16, stream);
+    case 4: return launch_bits<4>(a, transpose, y_bf16, stream);
+    case 5: return launch_bits<5>(a, transpose, y_bf16, stream);
+    case 6: return launch_bits<6>(a, transpose, y_bf16, stream);
+    case 8: return launch_bits<8>(a, transpose, y_bf16, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace qmm

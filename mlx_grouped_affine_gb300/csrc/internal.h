@@ -1,0 +1,43 @@
+// Host-side interface between the C ABI (api.cpp) and the kernel files.
+// Arguments reaching these launchers have already been validated.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qmm {
+
+// Bits of the device error word (read back by qmm_get_device_error).
+constexpr unsigned kErrIndexBit = 1u;    // a qmm_rows index outside the table
+constexpr unsigned kErrTimeoutBit = 2u;  // a bounded wait inside a kernel ran out
+
+struct PackedWeight {
+  const uint32_t *w;       // [rows, cols*bits/32]
+  const uint16_t *scales;  // bf16 [rows, cols/group]
+  const uint16_t *biases;  // bf16 [rows, cols/group]
+  int64_t rows, cols;
+  int group, bits;
+};
+
+// The current device's error word (a static __device__ variable); its device
+// address, looked up once per device.  nullptr if the lookup failed.
+unsigned *device_error_word();
+// Synchronize `stream`, read the word and clear it.
+cudaError_t take_device_error(cudaStream_t stream, unsigned *bits);
+
+// dequant.cu: out[r, :] = dequant(W[src(r), :]) for r < out_rows, where
+// src(r) = idx[r] if idx is given (a rows gather) else r.
+cudaError_t launch_dequantize(const PackedWeight &w, const uint32_t *idx,
+                              int64_t out_rows, void *out, bool out_bf16,
+                              cudaStream_t stream);
+
+// gemv.cu: decode path, M <= 16.
+cudaError_t launch_gemv(const uint16_t *x, int64_t M, const PackedWeight &w,
+                        bool transpose, void *y, bool y_bf16,
+                        cudaStream_t stream);
+
+// gemm_sm103.cu: tensor-core path for larger M.
+cudaError_t launch_gemm(const uint16_t *x, int64_t M, const PackedWeight &w,
+                        bool transpose, void *y, bool y_bf16,
+                        cudaStream_t stream);
+
+}  // namespace qmm

@@ -1,0 +1,95 @@
+"""Thin Python binding of the C ABI in include/qmm.h (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and passes the
+device pointers of torch tensors straight through; all computation happens in
+the CUDA kernels of libqmm.so.  There is no fallback: if the library cannot be
+built or loaded, or a call returns an error status, a QmmError is raised.
+"""
+import ctypes
+
+from . import build as _build
+
+QMM_OK, QMM_ERR_INVALID_ARG, QMM_ERR_UNSUPPORTED, QMM_ERR_CUDA, QMM_ERR_INDEX, QMM_ERR_TIMEOUT = range(6)
+QMM_F32, QMM_BF16 = 0, 1
+STATUS_NAMES = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED",
+                3: "QMM_ERR_CUDA", 4: "QMM_ERR_INDEX", 5: "QMM_ERR_TIMEOUT"}
+EXPORTS = ("qmm_dequantize", "qmm_quantized_matmul", "qmm_rows", "qmm_last_error",
+           "qmm_get_device_error")
+
+_lib = None
+
+
+class QmmError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__("%s: %s" % (STATUS_NAMES.get(status, status), message))
+        self.status = status
+
+
+def lib():
+    """The loaded libqmm.so (built first if it is missing or stale)."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.qmm_dequantize.argtypes = [P, P, P, I64, I64, I, I, P, I, P]
+        L.qmm_quantized_matmul.argtypes = [P, I64, P, P, P, I64, I64, I, I, I, P, I, P]
+        L.qmm_rows.argtypes = [P, P, P, I64, I64, P, I64, I, I, P, I, P]
+        L.qmm_get_device_error.argtypes = [P]
+        for f in ("qmm_dequantize", "qmm_quantized_matmul", "qmm_rows", "qmm_get_device_error"):
+            getattr(L, f).restype = I
+        L.qmm_last_error.argtypes = []
+        L.qmm_last_error.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    """Device address of a tensor (or an int address, or None -> NULL)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status):
+    if status != QMM_OK:
+        raise QmmError(status, qmm_last_error())
+
+
+def qmm_last_error():
+    return lib().qmm_last_error().decode()
+
+
+def qmm_dequantize(w, scales, biases, rows, cols, group_size, bits, out, out_dtype,
+                   stream=None):
+    _check(lib().qmm_dequantize(_ptr(w), _ptr(scales), _ptr(biases), rows, cols, group_size,
+                                bits, _ptr(out), out_dtype, _stream(stream)))
+
+
+def qmm_quantized_matmul(x, M, w, scales, biases, N, K, transpose, group_size, bits, y,
+                         y_dtype, stream=None):
+    _check(lib().qmm_quantized_matmul(_ptr(x), M, _ptr(w), _ptr(scales), _ptr(biases), N, K,
+                                      int(transpose), group_size, bits, _ptr(y), y_dtype,
+                                      _stream(stream)))
+
+
+def qmm_rows(w, scales, biases, table_rows, cols, idx, n, group_size, bits, out, out_dtype,
+             stream=None):
+    _check(lib().qmm_rows(_ptr(w), _ptr(scales), _ptr(biases), table_rows, cols, _ptr(idx), n,
+                          group_size, bits, _ptr(out), out_dtype, _stream(stream)))
+
+
+def qmm_get_device_error(stream=None):
+    """The status qmm_get_device_error returns (does not raise)."""
+    return lib().qmm_get_device_error(_stream(stream))

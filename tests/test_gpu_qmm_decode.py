@@ -1,0 +1,133 @@
+"""GPU parity of qmm_quantized_matmul on the decode path (M <= 16) against the
+fp64 oracle: every output within 8e-3 * sum_k |x w| + 1e-6."""
+import numpy as np
+import pytest
+
+import oracle
+from mlx_grouped_affine_gb300 import qmm, synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+from gpu_util import assert_within_tolerance, dev, empty_out, weight  # noqa: E402
+
+ALL_BITS = (1, 2, 3, 4, 5, 6, 8)
+
+
+def run_qmm(x, M, w, N, K, transpose, y_dtype=qmm.QMM_BF16):
+    pw, ps, pb = weight(w)
+    dx = dev(x)
+    y = empty_out((M, N), y_dtype)
+    qmm.qmm_quantized_matmul(dx, M, pw, ps, pb, N, K, transpose, w.group_size, w.bits, y, y_dtype)
+    torch.cuda.synchronize()
+    return y
+
+
+def check(x, M, w, N, K, transpose, y_dtype=qmm.QMM_BF16, what=""):
+    y = run_qmm(x, M, w, N, K, transpose, y_dtype)
+    ref, absy = oracle.qmm(x, M, w.packed, w.scales, w.biases, N, K, transpose, w.group_size, w.bits)
+    return assert_within_tolerance(y, ref, absy, what)
+
+
+def test_small_reference_case():
+    """x [1, 512] . W[256, 512]^T at 4 bits, group 64, fp32 output."""
+    w = synth.pr1_weight(0)
+    x = synth.x_bf16(0, 1, 512)
+    check(x, 1, w, 256, 512, True, qmm.QMM_F32, "pr1")
+
+
+@pytest.mark.parametrize("bits", ALL_BITS)
+@pytest.mark.parametrize("gs", (32, 128))
+@pytest.mark.parametrize("M", (1, 3, 8, 9, 16))
+def test_transposed_all_widths(bits, gs, M):
+    # N = 200: a ragged last 16-row tile; K = 640 = five 128-code chunks.
+    N, K = 200, 640
+    w = synth.quant_weight(10 * bits + gs + M, N, K, bits, gs)
+    x = synth.x_bf16(M + bits, M, K)
+    check(x, M, w, N, K, True, what="bits=%d gs=%d M=%d" % (bits, gs, M))
+
+
+@pytest.mark.parametrize("bits", (3, 4, 8))
+def test_transposed_partial_chunk(bits):
+    # K = 608 = 4 full 128-code chunks and 96 codes.
+    N, K = 48, 608
+    w = synth.quant_weight(71 + bits, N, K, bits, 32)
+    x = synth.x_bf16(72, 2, K)
+    check(x, 2, w, N, K, True, qmm.QMM_F32, "partial chunk")
+
+
+@pytest.mark.parametrize("bits", ALL_BITS)
+@pytest.mark.parametrize("M", (1, 5, 16))
+def test_not_transposed_all_widths(bits, M):
+    # W stored [K, N], packed and grouped along N; K = 77 is odd.
+    K, N = 77, 192
+    w = synth.quant_weight(500 + bits + M, K, N, bits, 64)
+    x = synth.x_bf16(600 + M, M, K)
+    check(x, M, w, N, K, False, what="transpose=0 bits=%d M=%d" % (bits, M))
+
+
+@pytest.mark.parametrize("bits", (4, 8))
+@pytest.mark.parametrize("M", synth.DECODE_M)
+def test_decode_full_size(bits, M):
+    """x [M, 4096] . W[4096, 4096]^T at group 64: every output checked."""
+    N, K = synth.DECODE_SHAPE
+    w = synth.quant_weight(bits, N, K, bits, 64)
+    x = synth.x_bf16(100 + M, M, K)
+    check(x, M, w, N, K, True, what="decode b%d M%d" % (bits, M))
+
+
+@pytest.mark.parametrize("bits", synth.ODD_BITS)
+@pytest.mark.parametrize("gs", synth.ODD_GROUPS)
+def test_odd_widths_full_size(bits, gs):
+    """x [1, 4096] . W[11008, 4096]^T: every output checked."""
+    N, K = synth.ODD_SHAPE
+    w = synth.quant_weight(200 + bits + gs, N, K, bits, gs)
+    x = synth.x_bf16(201, 1, K)
+    check(x, 1, w, N, K, True, what="odd b%d g%d" % (bits, gs))
+
+
+@pytest.mark.parametrize("shape", synth.SWEEP_SHAPES)
+@pytest.mark.parametrize("transpose", (True, False))
+def test_sweep_shapes_m16(shape, transpose):
+    N, K = shape
+    rows, cols = (N, K) if transpose else (K, N)
+    w = synth.quant_weight(N + K + int(transpose), rows, cols, 4, 64)
+    x = synth.x_bf16(7, 16, K)
+    check(x, 16, w, N, K, transpose, what="sweep %s t=%d" % (shape, transpose))
+
+
+@pytest.mark.parametrize("bits", (1, 4, 6, 8))
+def test_weights_that_are_exactly_zero(bits):
+    """Codes 2^(bits-1) with bias -scale * 2^(bits-1): every weight is exactly 0,
+    so y must be 0 within the absolute 1e-6."""
+    N, K = 64, 256
+    w = synth.quant_weight(9, N, K, bits, 64)
+    c = 1 << (bits - 1)
+    codes = np.full((N, K), c, dtype=np.uint8)
+    w.packed = oracle.pack(codes, bits)
+    s = (w.scales.astype(np.uint32) << 16).view(np.float32)
+    b = -(s * np.float32(c))                          # exact: times a power of two
+    w.biases = (b.view(np.uint32) >> 16).astype(np.uint16)
+    x = synth.x_bf16(10, 4, K)
+    y = run_qmm(x, 4, w, N, K, True, qmm.QMM_F32)
+    assert np.abs(y.cpu().numpy()).max() <= 1e-6
+
+
+def test_zero_x_gives_zero():
+    N, K = 32, 128
+    w = synth.quant_weight(12, N, K, 5, 32)
+    x = np.zeros((3, K), dtype=np.uint16)
+    y = run_qmm(x, 3, w, N, K, True, qmm.QMM_F32)
+    assert (y.cpu().numpy() == 0).all()
+
+
+def test_constant_weight_matmul_exact():
+    """Every code 0, scale 1, bias 1 or 2, x = ones(64): y = 64 or 128 (the
+    construction of nuvec_core's gather_qmm doctest)."""
+    N, K = 4, 64
+    for bias_bits, want in ((0x3F80, 64.0), (0x4000, 128.0)):
+        w = synth.QuantWeight(np.zeros((N, K // 8), np.uint32), np.full((N, 1), 0x3F80, np.uint16),
+                              np.full((N, 1), bias_bits, np.uint16), N, K, 4, 64)
+        x = np.full((1, K), 0x3F80, dtype=np.uint16)
+        y = run_qmm(x, 1, w, N, K, True, qmm.QMM_F32)
+        assert (y.cpu().numpy() == want).all()
