@@ -219,6 +219,18 @@ def run_gpu(args):
            "h2d_bytes_per_step": int(x_pin.numel() * 2), "d2h_bytes_per_step": int(y_pin.numel() * 2)}
 
     detail = {}
+    if rank == 0:
+        p = synth.PREFILL
+        c = Case(torch, qmm, synth, p["M"], p["N"], p["K"], 4, 64, seed=30)
+        c.capture()
+        t = time_graph(torch, c.graph, max(5, args.steps // 200), args.warmup) / c.R
+        tf = c.flops_per_launch() / (t * 1e-3) / 1e12
+        detail["prefill_b4_M2048"] = {
+            "us": round(t * 1e3, 2), "TFLOP/s": round(tf, 1),
+            "frac_bf16": round(tf / peaks["bf16_tflops"], 4),
+            "launches_timed": c.R * max(5, args.steps // 200)}
+        del c
+        torch.cuda.empty_cache()
     if rank == 0 and not args.quick:
         for bits in (4, 8):
             for M in synth.DECODE_M:

@@ -69,39 +69,6 @@ struct GemmArgs {
 
 // ------------------------------------------------------------- PTX glue ----
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count));
-}
-
-// One bounded poll: the thread may be suspended for at most kSuspendNs while
-// the phase is incomplete, so kSpinLimit polls take at most a few seconds.
-constexpr uint32_t kSuspendNs = 256;
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(b)), "r"(parity), "n"(kSuspendNs)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)),
-               "r"(bytes)
-               : "memory");
-}
-
 // Whole-warp bounded wait for the phase of parity `parity` to complete.
 // Warp-uniform result: false if this wait ran out (the error word is set) or
 // another role already gave up.

@@ -313,6 +313,214 @@ gemv_n_kernel(GemvArgs a) {
 }
 
 // ------------------------------------------------------------------------
+// transpose = true, streamed through bulk copies.  Used when K is a multiple
+// of 128 (so every row segment below is 16-byte aligned and sized).
+//
+// A block owns a 16-row tile and a K range [k0, k1) of at most a few
+// thousand codes; the blocks of a cluster split K.  At kernel start one warp
+// issues the whole working set as cp.async.bulk copies: each row's packed
+// segment and each x row's segment (contiguous in global memory) into shared
+// memory.  Every block of the grid does this at once, so the packed weight is
+// in flight almost entirely within the first few hundred nanoseconds -- the
+// kernel is a single HBM stream with no per-warp load latency to hide.
+// Scales and biases (a few bytes per 32 codes) are read with ordinary loads
+// while the copies land.  Rows are padded in shared memory so that the 8 rows
+// a quarter-warp reads fall in different banks.
+//
+// The 4 warps then take 128-code chunks in turn; lane (g, t) reads its 32
+// codes of rows g and g+8 and 64 bytes of x, and runs the same 8 MMAs per
+// chunk as the kernel above.  Partials meet through shared memory and, across
+// the cluster, distributed shared memory.
+
+constexpr int kBulkWarps = 4;
+constexpr int kBulkMaxChunksPerWarp = 4;  // K range per block <= 4 * 4 * 128 codes
+
+// The two natural pairs 2r and 2r+1 (codes 4r .. 4r+3) of a lane's 32 codes.
+template <int BITS>
+__device__ __forceinline__ void dequant_step(const uint32_t *v, int r, uint32_t s2, uint32_t b2,
+                                             float sf, float bf, uint32_t &p0, uint32_t &p1) {
+  if constexpr (BITS == 4) {
+    const uint32_t w = v[r >> 1], w4 = w >> 4;
+    const uint32_t i0 = 2u * (r & 1), i1 = i0 + 1;
+    p0 = bf16x2_fma(bf16x2_sub(and_or(prmt(w, w4, 0x0400u | (i0 << 8) | i0), 0x000F000Fu, kMagic), kMagic), s2, b2);
+    p1 = bf16x2_fma(bf16x2_sub(and_or(prmt(w, w4, 0x0400u | (i1 << 8) | i1), 0x000F000Fu, kMagic), kMagic), s2, b2);
+  } else if constexpr (BITS == 8) {
+    const uint32_t w = v[r];
+    float c[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      c[j] = __uint_as_float(prmt(w, 0x4B000000u, 0x7650u | j)) - 8388608.0f;
+    p0 = pack_bf16x2(__fmaf_rn(sf, c[0], bf), __fmaf_rn(sf, c[1], bf));
+    p1 = pack_bf16x2(__fmaf_rn(sf, c[2], bf), __fmaf_rn(sf, c[3], bf));
+  } else {
+    const uint32_t q0 = code_at<BITS>(v, 4 * r) | (code_at<BITS>(v, 4 * r + 1) << 16) | kMagic;
+    const uint32_t q1 = code_at<BITS>(v, 4 * r + 2) | (code_at<BITS>(v, 4 * r + 3) << 16) | kMagic;
+    p0 = bf16x2_fma(bf16x2_sub(q0, kMagic), s2, b2);
+    p1 = bf16x2_fma(bf16x2_sub(q1, kMagic), s2, b2);
+  }
+}
+
+template <int BITS>
+__device__ __forceinline__ void lds_words(const uint8_t *p, uint32_t *v) {
+  if constexpr (BITS % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < BITS / 4; ++i) {
+      const uint4 u = reinterpret_cast<const uint4 *>(p)[i];
+      v[4 * i] = u.x; v[4 * i + 1] = u.y; v[4 * i + 2] = u.z; v[4 * i + 3] = u.w;
+    }
+  } else if constexpr (BITS % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < BITS / 2; ++i) {
+      const uint2 u = reinterpret_cast<const uint2 *>(p)[i];
+      v[2 * i] = u.x; v[2 * i + 1] = u.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < BITS; ++i) v[i] = reinterpret_cast<const uint32_t *>(p)[i];
+  }
+}
+
+struct BulkLayout {
+  int kr;      // codes per block (multiple of 128)
+  int pitch;   // shared-memory row pitch of the packed segments, bytes
+  int xpitch;  // shared-memory row pitch of the x segments, bytes
+  int x_off;   // offset of the x rows
+  int red_off; // offset of the reduction buffer
+  int bar_off; // offset of the mbarrier
+};
+
+template <int BITS, int NT, bool OUT_BF16>
+__global__ void __launch_bounds__(32 * kBulkWarps)
+gemv_t_bulk_kernel(GemvArgs a, BulkLayout L, unsigned *err) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L.bar_off);
+  float *red = reinterpret_cast<float *>(smem + L.red_off);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  uint32_t crank = 0, csize = 1;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
+  const int n0 = blockIdx.x * 16;
+  const int k0 = static_cast<int>(crank) * L.kr;
+  const int k1 = min(a.K, k0 + L.kr);
+  const int ncodes = k1 > k0 ? k1 - k0 : 0;
+  const int rows = min(16, a.N - n0);
+  const int64_t row_bytes = (static_cast<int64_t>(a.K) * BITS) >> 3;
+  const uint32_t seg = static_cast<uint32_t>(ncodes) * BITS / 8;
+  const uint32_t xseg = static_cast<uint32_t>(ncodes) * 2;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (warp == 0 && ncodes > 0) {
+    if (lane == 0) mbar_expect_tx(bar, rows * seg + a.M * xseg);
+    __syncwarp();
+    if (lane < rows)
+      bulk_g2s(smem + lane * L.pitch,
+               reinterpret_cast<const uint8_t *>(a.w) + (n0 + lane) * row_bytes + (static_cast<int64_t>(k0) * BITS >> 3),
+               seg, bar);
+    if (lane >= 16 && lane - 16 < a.M)
+      bulk_g2s(smem + L.x_off + (lane - 16) * L.xpitch,
+               a.x + static_cast<int64_t>(lane - 16) * a.K + k0, xseg, bar);
+  }
+
+  // Scales and biases of this warp's chunks, while the copies land.
+  const int groups = a.K >> a.group_shift;
+  const int nchunks = ncodes >> 7;
+  const int row0 = n0 + g, row1 = n0 + g + 8;
+  uint16_t sv[kBulkMaxChunksPerWarp][4];
+#pragma unroll
+  for (int j = 0; j < kBulkMaxChunksPerWarp; ++j) {
+    const int c = warp + kBulkWarps * j;
+    const int kk = k0 + (c << 7) + 32 * t;
+    sv[j][0] = sv[j][1] = sv[j][2] = sv[j][3] = 0;
+    if (c < nchunks) {
+      const int gi = kk >> a.group_shift;
+      if (row0 < a.N) {
+        sv[j][0] = __ldg(a.scales + static_cast<int64_t>(row0) * groups + gi);
+        sv[j][1] = __ldg(a.biases + static_cast<int64_t>(row0) * groups + gi);
+      }
+      if (row1 < a.N) {
+        sv[j][2] = __ldg(a.scales + static_cast<int64_t>(row1) * groups + gi);
+        sv[j][3] = __ldg(a.biases + static_cast<int64_t>(row1) * groups + gi);
+      }
+    }
+  }
+
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+
+  bool ready = ncodes > 0;
+  if (ready) {
+    uint32_t spins = 0;
+    while (!mbar_try_wait(bar, 0)) {
+      if (++spins > (1u << 24)) {
+        if (threadIdx.x == 0) atomicOr(err, kErrTimeoutBit);
+        ready = false;
+        break;
+      }
+    }
+  }
+  if (ready) {
+#pragma unroll
+    for (int j = 0; j < kBulkMaxChunksPerWarp; ++j) {
+      const int c = warp + kBulkWarps * j;
+      if (c >= nchunks) break;
+      const int cc = (c << 7) + 32 * t;  // this lane's first code within the block's range
+      uint32_t v0[BITS], v1[BITS];
+      lds_words<BITS>(smem + g * L.pitch + (cc * BITS >> 3), v0);
+      lds_words<BITS>(smem + (g + 8) * L.pitch + (cc * BITS >> 3), v1);
+      uint32_t xv[NT][16];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int m = g + 8 * nt;
+        if (m < a.M) {
+          const uint4 *xp = reinterpret_cast<const uint4 *>(smem + L.x_off + m * L.xpitch + 2 * cc);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 u = xp[i];
+            xv[nt][4 * i] = u.x; xv[nt][4 * i + 1] = u.y; xv[nt][4 * i + 2] = u.z; xv[nt][4 * i + 3] = u.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) xv[nt][i] = 0u;
+        }
+      }
+      const uint32_t s0 = bcast_bf16x2(sv[j][0]), b0 = bcast_bf16x2(sv[j][1]);
+      const uint32_t s1 = bcast_bf16x2(sv[j][2]), b1 = bcast_bf16x2(sv[j][3]);
+      const float fs0 = bf16_bits_to_f32(sv[j][0]), fb0 = bf16_bits_to_f32(sv[j][1]);
+      const float fs1 = bf16_bits_to_f32(sv[j][2]), fb1 = bf16_bits_to_f32(sv[j][3]);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        uint32_t a0, a2, a1, a3;
+        dequant_step<BITS>(v0, r, s0, b0, fs0, fb0, a0, a2);
+        dequant_step<BITS>(v1, r, s1, b1, fs1, fb1, a1, a3);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          mma_bf16_16816(acc[nt], a0, a1, a2, a3, xv[nt][2 * r], xv[nt][2 * r + 1]);
+      }
+    }
+  }
+
+  float flat[NT * 4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) flat[nt * 4 + i] = acc[nt][i];
+  reduce_and_store<NT * 4>(flat, red, kBulkWarps, static_cast<int>(csize), a, OUT_BF16,
+                           [&](int ln, int i, int &m, int &n) {
+                             const int gg = ln >> 2, tt = ln & 3, nt = i >> 2, e = i & 3;
+                             n = n0 + gg + 8 * (e >> 1);
+                             m = 8 * nt + 2 * tt + (e & 1);
+                           });
+}
+
+// ------------------------------------------------------------------------
 
 struct Shape {
   int warps, cluster;
@@ -362,6 +570,61 @@ cudaError_t launch_t(const GemvArgs &a0, cudaStream_t stream) {
                           stream, a);
 }
 
+// Bytes that put consecutive shared-memory rows of packed codes in different
+// banks for the reads of a quarter (or half) warp: a row pitch congruent to
+// 16 * BITS modulo 128 (16 for 8-bit codes).
+constexpr int row_pad_target(int bits) { return bits == 8 ? 16 : (16 * bits) % 128; }
+
+template <int BITS, int NT, bool OUT_BF16>
+cudaError_t launch_t_bulk(const GemvArgs &a0, cudaStream_t stream) {
+  GemvArgs a = a0;
+  const int64_t tiles = (a.N + 15) / 16;
+  // Split K over a cluster: enough blocks to fill the GPU several times over
+  // with everything resident, and no more than 2048 codes (and a modest
+  // amount of shared memory) per block.
+  int C = 1;
+  auto kr_of = [&](int c) { return ((a.K / c + 127) / 128) * 128; };
+  auto smem_of = [&](int c) {
+    const int kr = kr_of(c);
+    return 16 * (kr * BITS / 8 + 128) + a.M * (2 * kr + 16) + kBulkWarps * NT * 4 * 32 * 4 + 64;
+  };
+  while (C < 8 && kr_of(2 * C) >= 128 &&
+         (tiles * C < 912 || kr_of(C) > kBulkWarps * kBulkMaxChunksPerWarp * 128 ||
+          smem_of(C) > 48 * 1024))
+    C *= 2;
+  if (kr_of(C) > kBulkWarps * kBulkMaxChunksPerWarp * 128) return cudaErrorNotSupported;
+  BulkLayout L;
+  L.kr = kr_of(C);
+  const int seg = L.kr * BITS / 8;
+  L.pitch = seg + ((row_pad_target(BITS) - seg % 128) + 128) % 128;
+  L.xpitch = 2 * L.kr + 16;
+  L.x_off = 16 * L.pitch;
+  L.red_off = L.x_off + ((a.M * L.xpitch + 15) / 16) * 16;
+  L.bar_off = L.red_off + kBulkWarps * NT * 4 * 32 * 4;
+  const size_t smem = L.bar_off + 16;
+  unsigned *err = device_error_word();
+  if (!err) return cudaErrorInvalidSymbol;
+  auto kern = gemv_t_bulk_kernel<BITS, NT, OUT_BF16>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles), C);
+  cfg.blockDim = dim3(32 * kBulkWarps);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = C;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, L, err);
+}
+
 template <int BITS, bool OUT_BF16>
 cudaError_t launch_n(const GemvArgs &a0, cudaStream_t stream) {
   GemvArgs a = a0;
@@ -375,6 +638,14 @@ cudaError_t launch_n(const GemvArgs &a0, cudaStream_t stream) {
 
 template <int BITS>
 cudaError_t launch_bits(const GemvArgs &a, bool transpose, bool y_bf16, cudaStream_t stream) {
+  if (transpose && a.K % 128 == 0) {
+    cudaError_t e;
+    if (a.M <= 8)
+      e = y_bf16 ? launch_t_bulk<BITS, 1, true>(a, stream) : launch_t_bulk<BITS, 1, false>(a, stream);
+    else
+      e = y_bf16 ? launch_t_bulk<BITS, 2, true>(a, stream) : launch_t_bulk<BITS, 2, false>(a, stream);
+    if (e != cudaErrorNotSupported) return e;
+  }
   if (transpose) {
     if (a.M <= 8) return y_bf16 ? launch_t<BITS, 1, true>(a, stream) : launch_t<BITS, 1, false>(a, stream);
     return y_bf16 ? launch_t<BITS, 2, true>(a, stream) : launch_t<BITS, 2, false>(a, stream);
