@@ -181,6 +181,10 @@ def run_gpu(args):
     qmm.lib()
 
     N, K = synth.DECODE_SHAPE
+    # Decode launches go out with programmatic dependent launch (each GEMV
+    # starts streaming its weights while the previous kernel finishes), the
+    # way a serving loop would run them.
+    qmm.qmm_set_launch_flags(0 if args.no_pdl else qmm.QMM_LAUNCH_PDL)
     head = Case(torch, qmm, synth, 1, N, K, 4, 64, seed=1 + rank)
     head.capture()
     with ClockSampler(local) as clk:
@@ -220,6 +224,14 @@ def run_gpu(args):
 
     detail = {}
     if rank == 0:
+        flags = qmm.qmm_set_launch_flags(0)
+        c = Case(torch, qmm, synth, 1, N, K, 4, 64, seed=2)
+        c.capture()
+        t = time_graph(torch, c.graph, max(20, args.steps // 4), args.warmup) / c.R
+        detail["decode_b4_M1_without_pdl"] = {
+            "us": round(t * 1e3, 3), "GB/s": round(c.bytes_per_launch() / (t * 1e-3) / 1e9, 1)}
+        del c
+        qmm.qmm_set_launch_flags(flags)
         p = synth.PREFILL
         c = Case(torch, qmm, synth, p["M"], p["N"], p["K"], 4, 64, seed=30)
         c.capture()
@@ -251,7 +263,10 @@ def run_gpu(args):
         "config": {"workload": "decode GEMV x[1,4096] . W[4096,4096]^T, 4-bit, group 64, bf16 out",
                    "launches_per_step": head.R, "weight_copies_bytes": head.R * per_launch,
                    "l2": "inputs larger than L2: %d rotating weight copies (> 3x L2)" % head.R,
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "launch": "CUDA graph of the step's launches; decode kernels with "
+                             + ("stream-ordered launch" if args.no_pdl else
+                                "programmatic dependent launch")},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": None, "peak_source": peaks["source"]},
@@ -333,16 +348,49 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
+PROFILE_CASES = {
+    # name: (M, N, K, bits, group, transpose)
+    "decode": (1, 4096, 4096, 4, 64, True),
+    "decode_m16": (16, 4096, 4096, 4, 64, True),
+    "decode_b8": (1, 4096, 4096, 8, 64, True),
+    "prefill": (2048, 14336, 4096, 4, 64, True),
+}
+
+
+def run_profile(case, launches):
+    """A few eager launches of one case over rotating weights (inputs > L2),
+    for ncu: a small, fixed amount of device memory and no CUDA graph."""
+    import torch
+    from mlx_grouped_affine_gb300 import qmm, synth
+    M, N, K, bits, group, transpose = PROFILE_CASES[case]
+    c = Case(torch, qmm, synth, M, N, K, bits, group, transpose, seed=5,
+             min_bytes=int(1.5 * L2_BYTES), max_copies=16)
+    for i in range(launches):
+        r = i % c.R
+        pw, ps, pb = c.w[r]
+        qmm.qmm_quantized_matmul(c.x, M, pw, ps, pb, N, K, int(transpose), group, bits, c.y[r],
+                                 qmm.QMM_BF16)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": case, "launches": launches, "copies": c.R}))
+
+
 def main():
     p = argparse.ArgumentParser()
+    p.add_argument("--profile", choices=sorted(PROFILE_CASES),
+                   help="run a few eager launches of one case (for ncu) and exit")
+    p.add_argument("--launches", type=int, default=6)
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=10000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="ours", choices=("ours", "reference"))
     p.add_argument("--quick", action="store_true", help="headline case only")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-pdl", action="store_true", help="launch decode kernels without PDL")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     args = p.parse_args()
+    if args.profile:
+        run_profile(args.profile, args.launches)
+        return
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
     out = run_reference(args) if args.impl == "reference" else run_gpu(args)

@@ -122,6 +122,26 @@ qmm_status qmm_rows(const uint32_t *w, const uint16_t *scales,
                     const uint32_t *idx, int64_t n, int group_size, int bits,
                     void *out, qmm_dtype out_dtype, qmm_stream_t stream);
 
+/*
+ * Launch options for the calls this host thread makes from now on (the pages
+ * have no counterpart: this is a property of how kernels are launched on
+ * this GPU).  Returns the previous flags.
+ *
+ *   QMM_LAUNCH_PDL  Launch the decode kernels (qmm_quantized_matmul with
+ *                   M <= 16) with programmatic dependent launch: a kernel may
+ *                   start, and begin streaming its packed weight, scales and
+ *                   biases, before the previous kernel in the stream has
+ *                   finished; it reads x and writes y only after that kernel
+ *                   has completed.  Only use it when the weights are not
+ *                   written by the kernel immediately before the call in the
+ *                   same stream (model weights normally are not).  Default
+ *                   off.
+ * Unknown bits return QMM_ERR_INVALID_ARG through qmm_last_error and are
+ * ignored; the previous flags are still returned.
+ */
+#define QMM_LAUNCH_PDL 1u
+unsigned qmm_set_launch_flags(unsigned flags);
+
 /* The message for the last non-OK status returned on this host thread
  * (empty string if none).  The pointer stays valid until the next call. */
 const char *qmm_last_error(void);

@@ -7,7 +7,7 @@
 // (rlx-moshi src/mlx_dequant.rs, `dequantize_affine`; spark_runtime
 // weights/mlx_int8.rs, `load`).  The library owns no buffer: every pointer is
 // the caller's (spark_runtime `MlxInt8Weight`, `release`).
-#include "../../include/qmm.h"
+#include "qmm.h"
 #include "internal.h"
 
 #include <cstdarg>
@@ -17,6 +17,7 @@
 namespace {
 
 thread_local char g_last_error[512] = "";
+thread_local unsigned g_launch_flags = 0;
 
 qmm_status fail(qmm_status st, const char *fmt, ...) {
   va_list ap;
@@ -70,9 +71,24 @@ qmm_status check_weight(const char *op, const uint32_t *w, const uint16_t *scale
 
 }  // namespace
 
+namespace qmm {
+unsigned launch_flags() { return g_launch_flags; }
+}  // namespace qmm
+
 extern "C" {
 
 const char *qmm_last_error(void) { return g_last_error; }
+
+unsigned qmm_set_launch_flags(unsigned flags) {
+  const unsigned prev = g_launch_flags;
+  if (flags & ~QMM_LAUNCH_PDL) {
+    fail(QMM_ERR_INVALID_ARG, "qmm_set_launch_flags: unknown flag bits 0x%x ignored",
+         flags & ~QMM_LAUNCH_PDL);
+    flags &= QMM_LAUNCH_PDL;
+  }
+  g_launch_flags = flags;
+  return prev;
+}
 
 qmm_status qmm_dequantize(const uint32_t *w, const uint16_t *scales, const uint16_t *biases,
                           int64_t rows, int64_t cols, int group_size, int bits, void *out,

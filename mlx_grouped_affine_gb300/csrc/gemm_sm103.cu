@@ -6,16 +6,18 @@
 // 256-row x 64-code tile of W is dequantized straight into shared memory,
 // where the tensor cores read it.
 //
-// One persistent block per SM walks output tiles of 128 x-rows by 256
-// weight-rows.  Its warps specialise:
-//   warp 0      TMA: x tiles [128 x 64] bf16 into a 128-byte-swizzled ring
+// One persistent block per SM walks output tiles of 256 x-rows by 256
+// weight-rows.  Each dequantized W tile feeds two 128-row MMAs (the two x
+// halves), which halves the dequantization work per tensor-core flop
+// compared with a 128-row tile.  Its warps specialise:
+//   warp 0      TMA: x tiles [256 x 64] bf16 into a 128-byte-swizzled ring
 //   warp 1      allocates tensor memory and issues tcgen05.mma (one lane):
-//               D[128 x 256] fp32 in TMEM, two accumulators so the epilogue
-//               of one tile overlaps the main loop of the next
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator, convert, store y
-//   warps 6-13  dequantize: packed W -> bf16 (one rounding per weight,
+//               D[2 x 128 x 256] fp32 in TMEM (all 512 columns)
+//   warps 2-5   epilogue: tcgen05.ld of the accumulators, convert, store y
+//   warps 6-21  dequantize: packed W -> bf16 (one rounding per weight,
 //               RN(scale * code + bias)) written in the same 128-byte swizzle
-//               the MMA descriptor expects, then fence.proxy.async and arrive
+//               the MMA descriptor expects, then fence.proxy.async and arrive;
+//               the packed codes of the next two stages are kept in flight
 // Stage hand-off uses mbarriers; every wait is bounded, and a wait that runs
 // out sets the device error word, makes every role stop, and the block still
 // waits for its own copies and MMAs and frees its tensor memory.
@@ -36,21 +38,25 @@
 namespace qmm {
 namespace {
 
-constexpr int BM = 128;   // x rows per tile (MMA M)
+constexpr int UM = 128;   // rows of one MMA (x rows)
+constexpr int BM = 2 * UM; // x rows per tile: two MMAs share each dequantized W tile
 constexpr int BN = 256;   // weight rows per tile (MMA N)
 constexpr int BK = 64;    // codes per stage: one 128-byte swizzle atom of bf16
-constexpr int STAGES = 4;
+constexpr int STAGES = 3;
 constexpr int kEpiWarps = 4;
-constexpr int kDeqWarps = 8;
+constexpr int kDeqWarps = 16;
+constexpr int kRowsPerPass = kDeqWarps * 4;     // 8 chunk-threads per 64-code row
+constexpr int kChunks = BN / kRowsPerPass;      // 8-code chunks per thread per stage
 constexpr int kThreads = 32 * (2 + kEpiWarps + kDeqWarps);
 constexpr uint32_t A_BYTES = BM * BK * 2;
+constexpr uint32_t A_HALF = UM * BK * 2;
 constexpr uint32_t B_BYTES = BN * BK * 2;
-constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr uint32_t TMEM_COLS = 2 * BN;  // accumulators of the two x halves
 constexpr uint32_t kSpinLimit = 1u << 24;
 
 struct Barriers {
   uint64_t full_a[STAGES], full_b[STAGES], empty[STAGES];
-  uint64_t tmem_full[2], tmem_empty[2], mma_done;
+  uint64_t tmem_full, tmem_empty, mma_done;
   uint32_t tmem_base;
   int abort;
 };
@@ -119,16 +125,31 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
 }
 
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, N = BN, M = BM.
+// K-major, N = BN, M = UM (each of the tile's two MMAs).
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                             (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(BM >> 4) << 24);
+                            (static_cast<uint32_t>(UM >> 4) << 24);
 
+// The same with B (the dequantized weight) MN-major: bit 16 = transpose B.
+constexpr uint32_t kIdescBmn = kIdesc | (1u << 16);
+
+// MN-major, 128-byte swizzle: atoms of 64 N-elements x 8 K-rows; LBO = 8192
+// bytes between atoms along N, SBO = 1024 bytes between atoms along K.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(8192 >> 4) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+template <uint32_t IDESC>
 __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(kIdesc), "r"(acc));
+      "l"(a), "l"(b), "r"(IDESC), "r"(acc));
 }
 
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
@@ -168,63 +189,106 @@ struct ChunkLoad {
   uint16_t s, b;
 };
 
-template <int BITS>
-__device__ __forceinline__ void load_chunk(const GemmArgs &a, int n, int k, ChunkLoad<BITS> &c) {
+// The 8 codes starting at column `col` of stored row `row` (stored [N, K] when
+// TRANS, else [K, N]; codes and groups run along the stored columns).
+template <int BITS, bool TRANS>
+__device__ __forceinline__ void load_chunk(const GemmArgs &a, int row, int col, ChunkLoad<BITS> &c) {
+  const int rows = TRANS ? a.N : a.K, cols = TRANS ? a.K : a.N;
   c.win[0] = c.win[1] = 0u;
   c.s = c.b = 0;
-  if (n < a.N && k < a.K) {
-    const int64_t wpr = (static_cast<int64_t>(a.K) * BITS) >> 5;
-    const int cbit = k * BITS, cword = cbit >> 5, csh = cbit & 31;
-    const uint32_t *rp = a.w + static_cast<int64_t>(n) * wpr + cword;
+  if (row < rows && col < cols) {
+    const int64_t wpr = (static_cast<int64_t>(cols) * BITS) >> 5;
+    const int cbit = col * BITS, cword = cbit >> 5, csh = cbit & 31;
+    const uint32_t *rp = a.w + static_cast<int64_t>(row) * wpr + cword;
     const uint32_t lo = __ldg(rp);
     const uint32_t hi = (csh + 8 * BITS > 32) ? __ldg(rp + 1) : 0u;
     c.win[0] = csh ? __funnelshift_r(lo, hi, csh) : lo;
     c.win[1] = csh ? (hi >> csh) : hi;
-    const int64_t g = static_cast<int64_t>(n) * (a.K >> a.group_shift) + (k >> a.group_shift);
+    const int64_t g = static_cast<int64_t>(row) * (cols >> a.group_shift) + (col >> a.group_shift);
     c.s = __ldg(a.scales + g);
     c.b = __ldg(a.biases + g);
   }
 }
 
-template <int BITS>
+// Shared-memory byte offset of the 16-byte chunk holding the 8 dequantized
+// weights a thread produces, and the (row, column) those 8 start at.
+//  TRANS: the W tile is K-major (as the x tile): 256 weight rows of 128 bytes;
+//    thread chunk c (of 8 per 64-code row) of row r.
+//  !TRANS: the W tile is MN-major: 8 consecutive n of one k row per chunk.
+//    Swizzle atoms of 64 n x 8 k (1024 bytes) sit at ((n/64) * 8 + k/8) * 1024:
+//    8192 bytes between atoms along N, 1024 along K.
+template <bool TRANS>
+__device__ __forceinline__ void chunk_place(int dt, int i, int tile_n0, int kb, int &row, int &col,
+                                            uint32_t &off) {
+  if (TRANS) {
+    const int c = dt & 7, r = (dt >> 3) + kRowsPerPass * i;
+    row = tile_n0 + r;
+    col = kb * BK + 8 * c;
+    off = r * 128 + ((c ^ (r & 7)) << 4);
+  } else {
+    const int j = dt & 31, kr = (dt >> 5) + (32 * kDeqWarps / 32) * i;  // k row in the stage
+    row = kb * BK + kr;
+    col = tile_n0 + 8 * j;
+    const int kw = kr & 7;
+    off = ((j >> 3) * 8 + (kr >> 3)) * 1024 + kw * 128 + (((j & 7) ^ kw) << 4);
+  }
+}
+
+template <int BITS, bool TRANS>
 __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int nk) {
-  const int dt = threadIdx.x - 32 * (2 + kEpiWarps);  // 0 .. 255
-  const int c = dt & 7, rbase = dt >> 3;               // chunk in the row, first row
+  const int dt = threadIdx.x - 32 * (2 + kEpiWarps);  // 0 .. 32 * kDeqWarps - 1
   const int num_tiles = a.m_tiles * a.n_tiles;
   volatile int *abort = &bars->abort;
-  int tile = blockIdx.x, kb = 0;
-  if (tile >= num_tiles) return;
-  ChunkLoad<BITS> next[BN / 32];
-  auto prefetch = [&](int t, int kbi) {
-    const int n0 = (t / a.m_tiles) * BN;
-#pragma unroll
-    for (int i = 0; i < BN / 32; ++i) load_chunk<BITS>(a, n0 + rbase + 32 * i, kbi * BK + 8 * c, next[i]);
+  // Stages are consumed in order (tile, kb); the codes of the next two stages
+  // are always in flight in two register buffers while one is dequantized.
+  int tile = blockIdx.x, kb = 0;    // next stage to dequantize
+  int ptile = tile, pkb = 0;        // next stage to load
+  auto advance = [&](int &t, int &k) {
+    if (++k == nk) { k = 0; t += gridDim.x; }
   };
-  prefetch(tile, kb);
+  auto prefetch = [&](ChunkLoad<BITS> (&buf)[kChunks]) {
+    if (ptile >= num_tiles) return;
+    const int n0 = (ptile / a.m_tiles) * BN;
+#pragma unroll
+    for (int i = 0; i < kChunks; ++i) {
+      int row, col;
+      uint32_t off;
+      chunk_place<TRANS>(dt, i, n0, pkb, row, col, off);
+      load_chunk<BITS, TRANS>(a, row, col, buf[i]);
+    }
+    advance(ptile, pkb);
+  };
+  ChunkLoad<BITS> buf0[kChunks], buf1[kChunks];
+  prefetch(buf0);
+  prefetch(buf1);
   int s = 0;
   uint32_t ph = 0;
-  while (tile < num_tiles) {
-    ChunkLoad<BITS> cur[BN / 32];
+  // One stage out of `buf`, which is then refilled; false when done or stopped.
+  auto step = [&](ChunkLoad<BITS> (&buf)[kChunks]) -> bool {
+    if (tile >= num_tiles) return false;
+    ChunkLoad<BITS> cur[kChunks];
 #pragma unroll
-    for (int i = 0; i < BN / 32; ++i) cur[i] = next[i];
-    int nt = tile, nkb = kb + 1;
-    if (nkb == nk) { nkb = 0; nt += gridDim.x; }
-    if (nt < num_tiles) prefetch(nt, nkb);
-    if (!wait_warp(&bars->empty[s], ph ^ 1u, abort, a.err)) return;
+    for (int i = 0; i < kChunks; ++i) cur[i] = buf[i];
+    prefetch(buf);
+    if (!wait_warp(&bars->empty[s], ph ^ 1u, abort, a.err)) return false;
     const uint32_t base = smem_u32(sB + s * B_BYTES);
 #pragma unroll
-    for (int i = 0; i < BN / 32; ++i) {
-      const int r = rbase + 32 * i;
+    for (int i = 0; i < kChunks; ++i) {
+      int row, col;
+      uint32_t off;
+      chunk_place<TRANS>(dt, i, 0, 0, row, col, off);
       uint32_t v[4];
       dequant_pairs<BITS, 4>(cur[i].win, bcast_bf16x2(cur[i].s), bcast_bf16x2(cur[i].b),
                              bf16_bits_to_f32(cur[i].s), bf16_bits_to_f32(cur[i].b), v);
-      st_shared_v4(base + r * 128 + ((c ^ (r & 7)) << 4), v);
+      st_shared_v4(base + off, v);
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_arrive(&bars->full_b[s]);
     if (++s == STAGES) { s = 0; ph ^= 1u; }
-    tile = nt;
-    kb = nkb;
+    advance(tile, kb);
+    return true;
+  };
+  while (step(buf0) && step(buf1)) {
   }
 }
 
@@ -263,8 +327,13 @@ __device__ void tma_role(const CUtensorMap *tmap, const GemmArgs &a, uint8_t *sA
   }
 }
 
+template <bool TRANS>
 __device__ void mma_role(const GemmArgs &a, uint8_t *sA, uint8_t *sB, Barriers *bars, int nk,
                          uint32_t tmem) {
+  constexpr uint32_t idesc = TRANS ? kIdesc : kIdescBmn;
+  // Start-address step of one 16-wide K slice: 32 bytes inside a K-major row,
+  // two 8-row K atoms (2048 bytes) in the MN-major tile; in units of 16 bytes.
+  constexpr uint64_t b_step = TRANS ? 2 : 128;
   const int lane = threadIdx.x & 31;
   const int num_tiles = a.m_tiles * a.n_tiles;
   volatile int *abort = &bars->abort;
@@ -272,11 +341,11 @@ __device__ void mma_role(const GemmArgs &a, uint8_t *sA, uint8_t *sB, Barriers *
   uint32_t ph = 0;
   bool ok = true;
   for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++it) {
-    const int acc = it & 1;
-    const uint32_t aph = (it >> 1) & 1;
-    if (!wait_warp(&bars->tmem_empty[acc], aph ^ 1u, abort, a.err)) break;
+    // The epilogue must have drained the accumulators of the previous tile.
+    if (!wait_warp(&bars->tmem_empty, (it & 1) ^ 1u, abort, a.err)) break;
     tc_fence_after();
-    const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
+    // The second 128-row half only when this tile has x rows there.
+    const bool two = (tile % a.m_tiles) * BM + UM < a.M;
     for (int kb = 0; kb < nk; ++kb) {
       if (!wait_warp(&bars->full_a[s], ph, abort, a.err) ||
           !wait_warp(&bars->full_b[s], ph, abort, a.err)) {
@@ -285,18 +354,23 @@ __device__ void mma_role(const GemmArgs &a, uint8_t *sA, uint8_t *sB, Barriers *
       }
       tc_fence_after();
       if (lane == 0) {
-        const uint64_t da = sw128_kmajor_desc(smem_u32(sA + s * A_BYTES));
-        const uint64_t db = sw128_kmajor_desc(smem_u32(sB + s * B_BYTES));
+        const uint64_t da0 = sw128_kmajor_desc(smem_u32(sA + s * A_BYTES));
+        const uint64_t da1 = sw128_kmajor_desc(smem_u32(sA + s * A_BYTES + A_HALF));
+        const uint32_t bs = smem_u32(sB + s * B_BYTES);
+        const uint64_t db = TRANS ? sw128_kmajor_desc(bs) : sw128_mnmajor_desc(bs);
 #pragma unroll
-        for (int j = 0; j < BK / 16; ++j)
-          umma(d_tmem, da + 2 * j, db + 2 * j, (kb | j) != 0 ? 1u : 0u);
+        for (int j = 0; j < BK / 16; ++j) {
+          const uint32_t accumulate = (kb | j) != 0 ? 1u : 0u;
+          umma<idesc>(tmem, da0 + 2 * j, db + b_step * j, accumulate);
+          if (two) umma<idesc>(tmem + BN, da1 + 2 * j, db + b_step * j, accumulate);
+        }
         umma_commit(&bars->empty[s]);
       }
       __syncwarp();
       if (++s == STAGES) { s = 0; ph ^= 1u; }
     }
     if (!ok) break;
-    if (lane == 0) umma_commit(&bars->tmem_full[acc]);
+    if (lane == 0) umma_commit(&bars->tmem_full);
     __syncwarp();
   }
   // Retire every MMA this thread issued before the block frees TMEM.
@@ -315,16 +389,16 @@ __device__ void epilogue_role(const GemmArgs &a, Barriers *bars, uint32_t tmem) 
   const bool vec = OUT_BF16 ? (a.N % 8 == 0) : (a.N % 4 == 0);
   int it = 0;
   for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
-    const int acc = it & 1;
-    const uint32_t aph = (it >> 1) & 1;
-    if (!wait_warp(&bars->tmem_full[acc], aph, abort, a.err)) return;
+    if (!wait_warp(&bars->tmem_full, it & 1, abort, a.err)) return;
     tc_fence_after();
-    const int m = (tile % a.m_tiles) * BM + 32 * q + lane;
     const int n0 = (tile / a.m_tiles) * BN;
 #pragma unroll 1
-    for (int cc = 0; cc < BN / 32; ++cc) {
+    for (int hc = 0; hc < 2 * (BN / 32); ++hc) {
+      const int half = hc / (BN / 32), cc = hc % (BN / 32);
+      const int m = (tile % a.m_tiles) * BM + UM * half + 32 * q + lane;
+      if (half == 1 && (tile % a.m_tiles) * BM + UM >= a.M) break;  // no second half
       uint32_t r[32];
-      tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * BN + 32 * cc), r);
+      tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(half * BN + 32 * cc), r);
       const int n = n0 + 32 * cc;
       if (m >= a.M || n >= a.N) continue;
       const int64_t o = static_cast<int64_t>(m) * a.N + n;
@@ -361,11 +435,11 @@ __device__ void epilogue_role(const GemmArgs &a, Barriers *bars, uint32_t tmem) 
       }
     }
     tc_fence_before();
-    mbar_arrive(&bars->tmem_empty[acc]);
+    mbar_arrive(&bars->tmem_empty);
   }
 }
 
-template <int BITS, bool OUT_BF16>
+template <int BITS, bool OUT_BF16, bool TRANS>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -382,10 +456,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, GemmArgs a) {
       mbar_init(&bars->full_b[i], 32 * kDeqWarps);
       mbar_init(&bars->empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->tmem_full[i], 1);
-      mbar_init(&bars->tmem_empty[i], 32 * kEpiWarps);
-    }
+    mbar_init(&bars->tmem_full, 1);
+    mbar_init(&bars->tmem_empty, 32 * kEpiWarps);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -404,9 +476,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, GemmArgs a) {
   const int nk = (a.K + BK - 1) / BK;
 
   if (warp == 0) tma_role(&tmap_x, a, sA, bars, nk);
-  else if (warp == 1) mma_role(a, sA, sB, bars, nk, tmem);
+  else if (warp == 1) mma_role<TRANS>(a, sA, sB, bars, nk, tmem);
   else if (warp < 2 + kEpiWarps) epilogue_role<OUT_BF16>(a, bars, tmem);
-  else dequant_role<BITS>(a, sB, bars, nk);
+  else dequant_role<BITS, TRANS>(a, sB, bars, nk);
 
   tc_fence_before();
   __syncthreads();
@@ -440,10 +512,12 @@ int sm_count() {
   return n;
 }
 
-template <int BITS, bool OUT_BF16>
+template <int BITS, bool OUT_BF16, bool TRANS>
 cudaError_t launch_t(const uint16_t *x, const GemmArgs &a, cudaStream_t stream) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
+  // TMA rows of x must start on 16-byte boundaries.
+  if ((static_cast<int64_t>(a.K) * 2) % 16 != 0) return cudaErrorNotSupported;
   CUtensorMap map;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.M)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K) * 2};
@@ -453,7 +527,7 @@ cudaError_t launch_t(const uint16_t *x, const GemmArgs &a, cudaStream_t stream) 
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  auto kern = gemm_kernel<BITS, OUT_BF16>;
+  auto kern = gemm_kernel<BITS, OUT_BF16, TRANS>;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -468,38 +542,52 @@ cudaError_t launch_t(const uint16_t *x, const GemmArgs &a, cudaStream_t stream) 
 }
 
 template <int BITS>
-cudaError_t launch_bits(const uint16_t *x, const GemmArgs &a, bool y_bf16, cudaStream_t stream) {
-  return y_bf16 ? launch_t<BITS, true>(x, a, stream) : launch_t<BITS, false>(x, a, stream);
+cudaError_t launch_bits(const uint16_t *x, const GemmArgs &a, bool transpose, bool y_bf16,
+                        cudaStream_t stream) {
+  if (transpose)
+    return y_bf16 ? launch_t<BITS, true, true>(x, a, stream) : launch_t<BITS, false, true>(x, a, stream);
+  return y_bf16 ? launch_t<BITS, true, false>(x, a, stream) : launch_t<BITS, false, false>(x, a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const uint16_t *x, int64_t M, const PackedWeight &w, bool transpose,
                         void *y, bool y_bf16, cudaStream_t stream) {
-  if (!transpose) return cudaErrorNotSupported;
   GemmArgs a;
   a.w = w.w;
   a.scales = w.scales;
   a.biases = w.biases;
   a.y = y;
   a.M = static_cast<int>(M);
-  a.N = static_cast<int>(w.rows);
-  a.K = static_cast<int>(w.cols);
+  a.N = static_cast<int>(transpose ? w.rows : w.cols);
+  a.K = static_cast<int>(transpose ? w.cols : w.rows);
   a.group_shift = w.group == 32 ? 5 : w.group == 64 ? 6 : 7;
   a.m_tiles = (a.M + BM - 1) / BM;
   a.n_tiles = (a.N + BN - 1) / BN;
   a.err = device_error_word();
   if (!a.err) return cudaErrorInvalidSymbol;
+  cudaError_t e;
   switch (w.bits) {
-    case 1: return launch_bits<1>(x, a, y_bf16, stream);
-    case 2: return launch_bits<2>(x, a, y_bf16, stream);
-    case 3: return launch_bits<3>(x, a, y_bf16, stream);
-    case 4: return launch_bits<4>(x, a, y_bf16, stream);
-    case 5: return launch_bits<5>(x, a, y_bf16, stream);
-    case 6: return launch_bits<6>(x, a, y_bf16, stream);
-    case 8: return launch_bits<8>(x, a, y_bf16, stream);
+    case 1: e = launch_bits<1>(x, a, transpose, y_bf16, stream); break;
+    case 2: e = launch_bits<2>(x, a, transpose, y_bf16, stream); break;
+    case 3: e = launch_bits<3>(x, a, transpose, y_bf16, stream); break;
+    case 4: e = launch_bits<4>(x, a, transpose, y_bf16, stream); break;
+    case 5: e = launch_bits<5>(x, a, transpose, y_bf16, stream); break;
+    case 6: e = launch_bits<6>(x, a, transpose, y_bf16, stream); break;
+    case 8: e = launch_bits<8>(x, a, transpose, y_bf16, stream); break;
     default: return cudaErrorInvalidValue;
   }
+  if (e != cudaErrorNotSupported) return e;
+  // x rows that TMA cannot address (K not a multiple of 8, possible when W is
+  // stored [K, N]): run the decode kernel over 16-row slices of x instead.
+  const size_t ysz = y_bf16 ? 2 : 4;
+  for (int64_t m0 = 0; m0 < M; m0 += 16) {
+    const int64_t rows = M - m0 < 16 ? M - m0 : 16;
+    e = launch_gemv(x + m0 * a.K, rows, w, transpose,
+                    static_cast<char *>(y) + m0 * static_cast<int64_t>(a.N) * ysz, y_bf16, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace qmm

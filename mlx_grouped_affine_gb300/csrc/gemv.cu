@@ -316,42 +316,71 @@ gemv_n_kernel(GemvArgs a) {
 // transpose = true, streamed through bulk copies.  Used when K is a multiple
 // of 128 (so every row segment below is 16-byte aligned and sized).
 //
-// A block owns a 16-row tile and a K range [k0, k1) of at most a few
-// thousand codes; the blocks of a cluster split K.  At kernel start one warp
-// issues the whole working set as cp.async.bulk copies: each row's packed
-// segment and each x row's segment (contiguous in global memory) into shared
-// memory.  Every block of the grid does this at once, so the packed weight is
-// in flight almost entirely within the first few hundred nanoseconds -- the
-// kernel is a single HBM stream with no per-warp load latency to hide.
-// Scales and biases (a few bytes per 32 codes) are read with ordinary loads
-// while the copies land.  Rows are padded in shared memory so that the 8 rows
-// a quarter-warp reads fall in different banks.
+// A block of 8 warps owns a 16-row tile and a K range [k0, k1); when the
+// weight has few rows, the blocks of a cluster split K.  At kernel start one
+// warp issues the block's whole share of the packed weight as cp.async.bulk
+// copies, one per row segment (contiguous in global memory), into shared
+// memory.  Every block does this at once, so the weight is in flight almost
+// entirely within the first few hundred nanoseconds.  Shared rows are padded
+// so that the 8 rows a quarter-warp reads fall in different banks.
 //
-// The 4 warps then take 128-code chunks in turn; lane (g, t) reads its 32
-// codes of rows g and g+8 and 64 bytes of x, and runs the same 8 MMAs per
-// chunk as the kernel above.  Partials meet through shared memory and, across
-// the cluster, distributed shared memory.
+// The copies are issued before griddepcontrol.wait: when the launch allows
+// programmatic dependent launch, a block streams its (read-only) weights
+// while the previous kernel in the stream is still finishing, and only x and
+// y wait for it.  x is then staged once per block, reordered so that each
+// 32-bit word holds the pair of x values that meets one bf16x2 register of
+// dequantized weights (below).
+//
+// Code pairs.  For 1, 2 and 4 bits a word holds 32/bits codes, and codes j
+// and j + 16/bits sit exactly 16 bits apart: one shift and one LOP3
+// ((w >> j*bits) & mask16x2 | 128.0x2) make the bf16x2 pair (128 + c_j,
+// 128 + c_{j+16/bits}); subtracting 128 is exact, then one bf16x2 FMA gives
+// RN(s*c + b) for both.  8-bit codes (above 127) go through fp32, paired
+// (j, j+2); 3, 5 and 6 bits are paired naturally (j, j+1).
+//
+// Warps take 128-code chunks in turn; lane (g, t) handles codes
+// [32t, 32t+32) of rows g and g+8, i.e. 16 pairs per row, and MMA r
+// contracts pairs 2r and 2r+1 with the two x words at the same positions.
 
-constexpr int kBulkWarps = 4;
-constexpr int kBulkMaxChunksPerWarp = 4;  // K range per block <= 4 * 4 * 128 codes
+constexpr int kStreamWarps = 8;
 
-// The two natural pairs 2r and 2r+1 (codes 4r .. 4r+3) of a lane's 32 codes.
+// The lane's 32 codes as 16 pairs: pair i is codes (pair_lo(i),
+// pair_lo(i) + pair_dist) of the 32.
 template <int BITS>
-__device__ __forceinline__ void dequant_step(const uint32_t *v, int r, uint32_t s2, uint32_t b2,
-                                             float sf, float bf, uint32_t &p0, uint32_t &p1) {
-  if constexpr (BITS == 4) {
-    const uint32_t w = v[r >> 1], w4 = w >> 4;
-    const uint32_t i0 = 2u * (r & 1), i1 = i0 + 1;
-    p0 = bf16x2_fma(bf16x2_sub(and_or(prmt(w, w4, 0x0400u | (i0 << 8) | i0), 0x000F000Fu, kMagic), kMagic), s2, b2);
-    p1 = bf16x2_fma(bf16x2_sub(and_or(prmt(w, w4, 0x0400u | (i1 << 8) | i1), 0x000F000Fu, kMagic), kMagic), s2, b2);
+__host__ __device__ constexpr int pair_dist() {
+  return BITS == 1 ? 16 : BITS == 2 ? 8 : BITS == 4 ? 4 : BITS == 8 ? 2 : 1;
+}
+template <int BITS>
+__host__ __device__ constexpr int pair_lo(int i) {
+  return BITS == 1 ? i
+       : BITS == 2 ? (i / 8) * 16 + i % 8
+       : BITS == 4 ? (i / 4) * 8 + i % 4
+       : BITS == 8 ? (i / 2) * 4 + i % 2
+       : 2 * i;
+}
+
+// Pairs 2r and 2r+1 of a lane's 32 codes held in v[] (BITS words).
+template <int BITS>
+__device__ __forceinline__ void dequant_mma_pairs(const uint32_t *v, int r, uint32_t s2, uint32_t b2,
+                                                  float sf, float bf, uint32_t &p0, uint32_t &p1) {
+  if constexpr (BITS == 1 || BITS == 2 || BITS == 4) {
+    constexpr int per_word = 16 / BITS;  // pairs per word
+    constexpr uint32_t mask = ((1u << BITS) - 1u) * 0x00010001u;
+    const int i0 = 2 * r, i1 = 2 * r + 1;
+    const uint32_t w0 = v[i0 / per_word], w1 = v[i1 / per_word];
+    const uint32_t q0 = and_or(w0 >> ((i0 % per_word) * BITS), mask, kMagic);
+    const uint32_t q1 = and_or(w1 >> ((i1 % per_word) * BITS), mask, kMagic);
+    p0 = bf16x2_fma(bf16x2_sub(q0, kMagic), s2, b2);
+    p1 = bf16x2_fma(bf16x2_sub(q1, kMagic), s2, b2);
   } else if constexpr (BITS == 8) {
+    // word r holds codes 4r .. 4r+3; pair 2r = bytes (0, 2), pair 2r+1 = (1, 3)
     const uint32_t w = v[r];
-    float c[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      c[j] = __uint_as_float(prmt(w, 0x4B000000u, 0x7650u | j)) - 8388608.0f;
-    p0 = pack_bf16x2(__fmaf_rn(sf, c[0], bf), __fmaf_rn(sf, c[1], bf));
-    p1 = pack_bf16x2(__fmaf_rn(sf, c[2], bf), __fmaf_rn(sf, c[3], bf));
+    const float c0 = __uint_as_float(prmt(w, 0x4B000000u, 0x7650u)) - 8388608.0f;
+    const float c1 = __uint_as_float(prmt(w, 0x4B000000u, 0x7651u)) - 8388608.0f;
+    const float c2 = __uint_as_float(prmt(w, 0x4B000000u, 0x7652u)) - 8388608.0f;
+    const float c3 = __uint_as_float(prmt(w, 0x4B000000u, 0x7653u)) - 8388608.0f;
+    p0 = pack_bf16x2(__fmaf_rn(sf, c0, bf), __fmaf_rn(sf, c2, bf));
+    p1 = pack_bf16x2(__fmaf_rn(sf, c1, bf), __fmaf_rn(sf, c3, bf));
   } else {
     const uint32_t q0 = code_at<BITS>(v, 4 * r) | (code_at<BITS>(v, 4 * r + 1) << 16) | kMagic;
     const uint32_t q1 = code_at<BITS>(v, 4 * r + 2) | (code_at<BITS>(v, 4 * r + 3) << 16) | kMagic;
@@ -380,18 +409,18 @@ __device__ __forceinline__ void lds_words(const uint8_t *p, uint32_t *v) {
   }
 }
 
-struct BulkLayout {
-  int kr;      // codes per block (multiple of 128)
-  int pitch;   // shared-memory row pitch of the packed segments, bytes
-  int xpitch;  // shared-memory row pitch of the x segments, bytes
-  int x_off;   // offset of the x rows
-  int red_off; // offset of the reduction buffer
-  int bar_off; // offset of the mbarrier
+struct StreamLayout {
+  int kr;       // codes per block (multiple of 128)
+  int pitch;    // shared row pitch of the packed segments, bytes
+  int xpitch;   // shared row pitch of the staged x rows, bytes
+  int x_off;    // offset of the staged x rows
+  int red_off;  // offset of the reduction buffer
+  int bar_off;  // offset of the mbarrier
 };
 
 template <int BITS, int NT, bool OUT_BF16>
-__global__ void __launch_bounds__(32 * kBulkWarps)
-gemv_t_bulk_kernel(GemvArgs a, BulkLayout L, unsigned *err) {
+__global__ void __launch_bounds__(32 * kStreamWarps)
+gemv_t_stream_kernel(GemvArgs a, StreamLayout L, unsigned *err) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L.bar_off);
   float *red = reinterpret_cast<float *>(smem + L.red_off);
@@ -402,12 +431,10 @@ gemv_t_bulk_kernel(GemvArgs a, BulkLayout L, unsigned *err) {
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
   const int n0 = blockIdx.x * 16;
   const int k0 = static_cast<int>(crank) * L.kr;
-  const int k1 = min(a.K, k0 + L.kr);
-  const int ncodes = k1 > k0 ? k1 - k0 : 0;
+  const int ncodes = max(0, min(a.K, k0 + L.kr) - k0);
   const int rows = min(16, a.N - n0);
   const int64_t row_bytes = (static_cast<int64_t>(a.K) * BITS) >> 3;
   const uint32_t seg = static_cast<uint32_t>(ncodes) * BITS / 8;
-  const uint32_t xseg = static_cast<uint32_t>(ncodes) * 2;
 
   if (threadIdx.x == 0) {
     mbar_init(bar, 1);
@@ -415,39 +442,59 @@ gemv_t_bulk_kernel(GemvArgs a, BulkLayout L, unsigned *err) {
   }
   __syncthreads();
   if (warp == 0 && ncodes > 0) {
-    if (lane == 0) mbar_expect_tx(bar, rows * seg + a.M * xseg);
+    if (lane == 0) mbar_expect_tx(bar, rows * seg);
     __syncwarp();
     if (lane < rows)
       bulk_g2s(smem + lane * L.pitch,
-               reinterpret_cast<const uint8_t *>(a.w) + (n0 + lane) * row_bytes + (static_cast<int64_t>(k0) * BITS >> 3),
+               reinterpret_cast<const uint8_t *>(a.w) + (n0 + lane) * row_bytes +
+                   ((static_cast<int64_t>(k0) * BITS) >> 3),
                seg, bar);
-    if (lane >= 16 && lane - 16 < a.M)
-      bulk_g2s(smem + L.x_off + (lane - 16) * L.xpitch,
-               a.x + static_cast<int64_t>(lane - 16) * a.K + k0, xseg, bar);
   }
+  griddep_launch_dependents();
 
-  // Scales and biases of this warp's chunks, while the copies land.
   const int groups = a.K >> a.group_shift;
   const int nchunks = ncodes >> 7;
-  const int row0 = n0 + g, row1 = n0 + g + 8;
-  uint16_t sv[kBulkMaxChunksPerWarp][4];
+  const int row0 = min(n0 + g, a.N - 1), row1 = min(n0 + g + 8, a.N - 1);
+  const uint16_t *s0p = a.scales + static_cast<int64_t>(row0) * groups;
+  const uint16_t *b0p = a.biases + static_cast<int64_t>(row0) * groups;
+  const uint16_t *s1p = a.scales + static_cast<int64_t>(row1) * groups;
+  const uint16_t *b1p = a.biases + static_cast<int64_t>(row1) * groups;
+  auto load_sb = [&](int c, uint16_t (&sv)[4]) {
+    const int gi = (k0 + (c << 7) + 32 * t) >> a.group_shift;
+    sv[0] = __ldg(s0p + gi); sv[1] = __ldg(b0p + gi);
+    sv[2] = __ldg(s1p + gi); sv[3] = __ldg(b1p + gi);
+  };
+  uint16_t sv[4] = {0, 0, 0, 0};
+  if (warp < nchunks) load_sb(warp, sv);
+
+  // x may be written by the previous kernel in the stream: wait for it, then
+  // stage this block's x range, paired the way the weights are.
+  griddep_wait();
+  {
+    constexpr int kSpan = 32;  // codes per staging item
+    const int spans = ncodes / kSpan;
+    for (int it = threadIdx.x; it < a.M * spans; it += blockDim.x) {
+      const int m = it / spans, sp = it - m * spans;
+      const uint4 *src = reinterpret_cast<const uint4 *>(a.x + static_cast<int64_t>(m) * a.K + k0 + kSpan * sp);
+      uint32_t nat[16], out[16];
 #pragma unroll
-  for (int j = 0; j < kBulkMaxChunksPerWarp; ++j) {
-    const int c = warp + kBulkWarps * j;
-    const int kk = k0 + (c << 7) + 32 * t;
-    sv[j][0] = sv[j][1] = sv[j][2] = sv[j][3] = 0;
-    if (c < nchunks) {
-      const int gi = kk >> a.group_shift;
-      if (row0 < a.N) {
-        sv[j][0] = __ldg(a.scales + static_cast<int64_t>(row0) * groups + gi);
-        sv[j][1] = __ldg(a.biases + static_cast<int64_t>(row0) * groups + gi);
+      for (int i = 0; i < 4; ++i) {
+        const uint4 u = __ldg(src + i);
+        nat[4 * i] = u.x; nat[4 * i + 1] = u.y; nat[4 * i + 2] = u.z; nat[4 * i + 3] = u.w;
       }
-      if (row1 < a.N) {
-        sv[j][2] = __ldg(a.scales + static_cast<int64_t>(row1) * groups + gi);
-        sv[j][3] = __ldg(a.biases + static_cast<int64_t>(row1) * groups + gi);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        constexpr int d = pair_dist<BITS>();
+        const int lo = pair_lo<BITS>(i), hi = lo + d;
+        const uint32_t sel = ((lo & 1) ? 0x32u : 0x10u) | (((hi & 1) ? 0x76u : 0x54u) << 8);
+        out[i] = (d == 1) ? nat[i] : prmt(nat[lo >> 1], nat[hi >> 1], sel);
       }
+      uint4 *dst = reinterpret_cast<uint4 *>(smem + L.x_off + m * L.xpitch + 2 * kSpan * sp);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dst[i] = make_uint4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]);
     }
   }
+  __syncthreads();
 
   float acc[NT][4];
 #pragma unroll
@@ -460,25 +507,26 @@ gemv_t_bulk_kernel(GemvArgs a, BulkLayout L, unsigned *err) {
     uint32_t spins = 0;
     while (!mbar_try_wait(bar, 0)) {
       if (++spins > (1u << 24)) {
-        if (threadIdx.x == 0) atomicOr(err, kErrTimeoutBit);
+        if (lane == 0) atomicOr(err, kErrTimeoutBit);
         ready = false;
         break;
       }
     }
   }
   if (ready) {
-#pragma unroll
-    for (int j = 0; j < kBulkMaxChunksPerWarp; ++j) {
-      const int c = warp + kBulkWarps * j;
-      if (c >= nchunks) break;
-      const int cc = (c << 7) + 32 * t;  // this lane's first code within the block's range
+    for (int c = warp; c < nchunks; c += kStreamWarps) {
+      uint16_t cur[4] = {sv[0], sv[1], sv[2], sv[3]};
+      if (c + kStreamWarps < nchunks) load_sb(c + kStreamWarps, sv);
+      const int cc = (c << 7) + 32 * t;  // lane's first code within the block's range
       uint32_t v0[BITS], v1[BITS];
-      lds_words<BITS>(smem + g * L.pitch + (cc * BITS >> 3), v0);
-      lds_words<BITS>(smem + (g + 8) * L.pitch + (cc * BITS >> 3), v1);
+      lds_words<BITS>(smem + g * L.pitch + ((cc * BITS) >> 3), v0);
+      lds_words<BITS>(smem + (g + 8) * L.pitch + ((cc * BITS) >> 3), v1);
       uint32_t xv[NT][16];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int m = g + 8 * nt;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) xv[nt][i] = 0u;
         if (m < a.M) {
           const uint4 *xp = reinterpret_cast<const uint4 *>(smem + L.x_off + m * L.xpitch + 2 * cc);
 #pragma unroll
@@ -486,20 +534,17 @@ gemv_t_bulk_kernel(GemvArgs a, BulkLayout L, unsigned *err) {
             const uint4 u = xp[i];
             xv[nt][4 * i] = u.x; xv[nt][4 * i + 1] = u.y; xv[nt][4 * i + 2] = u.z; xv[nt][4 * i + 3] = u.w;
           }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) xv[nt][i] = 0u;
         }
       }
-      const uint32_t s0 = bcast_bf16x2(sv[j][0]), b0 = bcast_bf16x2(sv[j][1]);
-      const uint32_t s1 = bcast_bf16x2(sv[j][2]), b1 = bcast_bf16x2(sv[j][3]);
-      const float fs0 = bf16_bits_to_f32(sv[j][0]), fb0 = bf16_bits_to_f32(sv[j][1]);
-      const float fs1 = bf16_bits_to_f32(sv[j][2]), fb1 = bf16_bits_to_f32(sv[j][3]);
+      const uint32_t s0 = bcast_bf16x2(cur[0]), b0 = bcast_bf16x2(cur[1]);
+      const uint32_t s1 = bcast_bf16x2(cur[2]), b1 = bcast_bf16x2(cur[3]);
+      const float fs0 = bf16_bits_to_f32(cur[0]), fb0 = bf16_bits_to_f32(cur[1]);
+      const float fs1 = bf16_bits_to_f32(cur[2]), fb1 = bf16_bits_to_f32(cur[3]);
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
         uint32_t a0, a2, a1, a3;
-        dequant_step<BITS>(v0, r, s0, b0, fs0, fb0, a0, a2);
-        dequant_step<BITS>(v1, r, s1, b1, fs1, fb1, a1, a3);
+        dequant_mma_pairs<BITS>(v0, r, s0, b0, fs0, fb0, a0, a2);
+        dequant_mma_pairs<BITS>(v1, r, s1, b1, fs1, fb1, a1, a3);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
           mma_bf16_16816(acc[nt], a0, a1, a2, a3, xv[nt][2 * r], xv[nt][2 * r + 1]);
@@ -512,7 +557,7 @@ gemv_t_bulk_kernel(GemvArgs a, BulkLayout L, unsigned *err) {
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int i = 0; i < 4; ++i) flat[nt * 4 + i] = acc[nt][i];
-  reduce_and_store<NT * 4>(flat, red, kBulkWarps, static_cast<int>(csize), a, OUT_BF16,
+  reduce_and_store<NT * 4>(flat, red, kStreamWarps, static_cast<int>(csize), a, OUT_BF16,
                            [&](int ln, int i, int &m, int &n) {
                              const int gg = ln >> 2, tt = ln & 3, nt = i >> 2, e = i & 3;
                              n = n0 + gg + 8 * (e >> 1);
@@ -541,22 +586,35 @@ Shape pick_shape(int64_t tiles, int64_t ksteps) {
   return s;
 }
 
+template <typename Kern, typename... Args>
+cudaError_t launch_ex(Kern kern, dim3 grid, dim3 block, size_t smem, int cluster, bool pdl,
+                      cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeClusterDimension;
+  attr[n].val.clusterDim.x = 1;
+  attr[n].val.clusterDim.y = cluster;
+  attr[n].val.clusterDim.z = 1;
+  ++n;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <typename Kern>
 cudaError_t launch_clustered(Kern kern, dim3 grid, Shape s, size_t smem, cudaStream_t stream,
                              const GemvArgs &a) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(32 * s.warps);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = s.cluster;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a);
+  return launch_ex(kern, grid, dim3(32 * s.warps), smem, s.cluster, false, stream, a);
 }
 
 template <int BITS, int NT, bool OUT_BF16>
@@ -570,59 +628,42 @@ cudaError_t launch_t(const GemvArgs &a0, cudaStream_t stream) {
                           stream, a);
 }
 
-// Bytes that put consecutive shared-memory rows of packed codes in different
-// banks for the reads of a quarter (or half) warp: a row pitch congruent to
-// 16 * BITS modulo 128 (16 for 8-bit codes).
+// A shared row pitch congruent to 16 * BITS modulo 128 (16 for 8-bit codes)
+// puts the rows read by one quarter (or half) warp in different banks.
 constexpr int row_pad_target(int bits) { return bits == 8 ? 16 : (16 * bits) % 128; }
 
 template <int BITS, int NT, bool OUT_BF16>
-cudaError_t launch_t_bulk(const GemvArgs &a0, cudaStream_t stream) {
-  GemvArgs a = a0;
+cudaError_t launch_t_stream(const GemvArgs &a, bool pdl, cudaStream_t stream) {
   const int64_t tiles = (a.N + 15) / 16;
-  // Split K over a cluster: enough blocks to fill the GPU several times over
-  // with everything resident, and no more than 2048 codes (and a modest
-  // amount of shared memory) per block.
-  int C = 1;
   auto kr_of = [&](int c) { return ((a.K / c + 127) / 128) * 128; };
   auto smem_of = [&](int c) {
     const int kr = kr_of(c);
-    return 16 * (kr * BITS / 8 + 128) + a.M * (2 * kr + 16) + kBulkWarps * NT * 4 * 32 * 4 + 64;
+    return 16 * (kr * BITS / 8 + 128) + a.M * (2 * kr + 16) + kStreamWarps * NT * 4 * 32 * 4 + 64;
   };
-  while (C < 8 && kr_of(2 * C) >= 128 &&
-         (tiles * C < 912 || kr_of(C) > kBulkWarps * kBulkMaxChunksPerWarp * 128 ||
-          smem_of(C) > 48 * 1024))
-    C *= 2;
-  if (kr_of(C) > kBulkWarps * kBulkMaxChunksPerWarp * 128) return cudaErrorNotSupported;
-  BulkLayout L;
+  // Split K over a cluster only when the weight has too few 16-row tiles to
+  // give every SM work, or one block's share would not fit.
+  int C = 1;
+  while (C < 8 && kr_of(2 * C) >= 128 && (tiles * C < 240 || smem_of(C) > 100 * 1024)) C *= 2;
+  if (smem_of(C) > 200 * 1024) return cudaErrorNotSupported;
+  StreamLayout L;
   L.kr = kr_of(C);
   const int seg = L.kr * BITS / 8;
   L.pitch = seg + ((row_pad_target(BITS) - seg % 128) + 128) % 128;
   L.xpitch = 2 * L.kr + 16;
   L.x_off = 16 * L.pitch;
   L.red_off = L.x_off + ((a.M * L.xpitch + 15) / 16) * 16;
-  L.bar_off = L.red_off + kBulkWarps * NT * 4 * 32 * 4;
+  L.bar_off = L.red_off + kStreamWarps * NT * 4 * 32 * 4;
   const size_t smem = L.bar_off + 16;
   unsigned *err = device_error_word();
   if (!err) return cudaErrorInvalidSymbol;
-  auto kern = gemv_t_bulk_kernel<BITS, NT, OUT_BF16>;
+  auto kern = gemv_t_stream_kernel<BITS, NT, OUT_BF16>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(tiles), C);
-  cfg.blockDim = dim3(32 * kBulkWarps);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = C;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a, L, err);
+  return launch_ex(kern, dim3(static_cast<unsigned>(tiles), C), dim3(32 * kStreamWarps), smem, C,
+                   pdl, stream, a, L, err);
 }
 
 template <int BITS, bool OUT_BF16>
@@ -637,13 +678,16 @@ cudaError_t launch_n(const GemvArgs &a0, cudaStream_t stream) {
 }
 
 template <int BITS>
-cudaError_t launch_bits(const GemvArgs &a, bool transpose, bool y_bf16, cudaStream_t stream) {
+cudaError_t launch_bits(const GemvArgs &a, bool transpose, bool y_bf16, bool pdl,
+                        cudaStream_t stream) {
   if (transpose && a.K % 128 == 0) {
     cudaError_t e;
     if (a.M <= 8)
-      e = y_bf16 ? launch_t_bulk<BITS, 1, true>(a, stream) : launch_t_bulk<BITS, 1, false>(a, stream);
+      e = y_bf16 ? launch_t_stream<BITS, 1, true>(a, pdl, stream)
+                 : launch_t_stream<BITS, 1, false>(a, pdl, stream);
     else
-      e = y_bf16 ? launch_t_bulk<BITS, 2, true>(a, stream) : launch_t_bulk<BITS, 2, false>(a, stream);
+      e = y_bf16 ? launch_t_stream<BITS, 2, true>(a, pdl, stream)
+                 : launch_t_stream<BITS, 2, false>(a, pdl, stream);
     if (e != cudaErrorNotSupported) return e;
   }
   if (transpose) {
@@ -668,14 +712,15 @@ cudaError_t launch_gemv(const uint16_t *x, int64_t M, const PackedWeight &w, boo
   a.K = static_cast<int>(transpose ? w.cols : w.rows);
   a.group_shift = w.group == 32 ? 5 : w.group == 64 ? 6 : 7;
   a.parts = 1;
+  const bool pdl = (launch_flags() & kLaunchPdl) != 0;
   switch (w.bits) {
-    case 1: return launch_bits<1>(a, transpose, y_bf16, stream);
-    case 2: return launch_bits<2>(a, transpose, y_bf16, stream);
-    case 3: return launch_bits<3>(a, transpose, y_bf16, stream);
-    case 4: return launch_bits<4>(a, transpose, y_bf16, stream);
-    case 5: return launch_bits<5>(a, transpose, y_bf16, stream);
-    case 6: return launch_bits<6>(a, transpose, y_bf16, stream);
-    case 8: return launch_bits<8>(a, transpose, y_bf16, stream);
+    case 1: return launch_bits<1>(a, transpose, y_bf16, pdl, stream);
+    case 2: return launch_bits<2>(a, transpose, y_bf16, pdl, stream);
+    case 3: return launch_bits<3>(a, transpose, y_bf16, pdl, stream);
+    case 4: return launch_bits<4>(a, transpose, y_bf16, pdl, stream);
+    case 5: return launch_bits<5>(a, transpose, y_bf16, pdl, stream);
+    case 6: return launch_bits<6>(a, transpose, y_bf16, pdl, stream);
+    case 8: return launch_bits<8>(a, transpose, y_bf16, pdl, stream);
     default: return cudaErrorInvalidValue;
   }
 }

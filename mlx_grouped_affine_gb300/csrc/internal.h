@@ -10,6 +10,10 @@ namespace qmm {
 constexpr unsigned kErrIndexBit = 1u;    // a qmm_rows index outside the table
 constexpr unsigned kErrTimeoutBit = 2u;  // a bounded wait inside a kernel ran out
 
+// Launch options of the calling host thread (qmm_set_launch_flags).
+constexpr unsigned kLaunchPdl = 1u;
+unsigned launch_flags();
+
 struct PackedWeight {
   const uint32_t *w;       // [rows, cols*bits/32]
   const uint16_t *scales;  // bf16 [rows, cols/group]

@@ -13,8 +13,9 @@ QMM_OK, QMM_ERR_INVALID_ARG, QMM_ERR_UNSUPPORTED, QMM_ERR_CUDA, QMM_ERR_INDEX, Q
 QMM_F32, QMM_BF16 = 0, 1
 STATUS_NAMES = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED",
                 3: "QMM_ERR_CUDA", 4: "QMM_ERR_INDEX", 5: "QMM_ERR_TIMEOUT"}
+QMM_LAUNCH_PDL = 1
 EXPORTS = ("qmm_dequantize", "qmm_quantized_matmul", "qmm_rows", "qmm_last_error",
-           "qmm_get_device_error")
+           "qmm_get_device_error", "qmm_set_launch_flags")
 
 _lib = None
 
@@ -38,6 +39,8 @@ def lib():
         L.qmm_get_device_error.argtypes = [P]
         for f in ("qmm_dequantize", "qmm_quantized_matmul", "qmm_rows", "qmm_get_device_error"):
             getattr(L, f).restype = I
+        L.qmm_set_launch_flags.argtypes = [ctypes.c_uint]
+        L.qmm_set_launch_flags.restype = ctypes.c_uint
         L.qmm_last_error.argtypes = []
         L.qmm_last_error.restype = ctypes.c_char_p
         _lib = L
@@ -93,3 +96,8 @@ def qmm_rows(w, scales, biases, table_rows, cols, idx, n, group_size, bits, out,
 def qmm_get_device_error(stream=None):
     """The status qmm_get_device_error returns (does not raise)."""
     return lib().qmm_get_device_error(_stream(stream))
+
+
+def qmm_set_launch_flags(flags):
+    """Set this host thread's launch flags (QMM_LAUNCH_PDL); returns the previous ones."""
+    return int(lib().qmm_set_launch_flags(flags))

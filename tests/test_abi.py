@@ -120,3 +120,16 @@ def test_python_binding_raises():
     with pytest.raises(qmm.QmmError) as e:
         qmm.qmm_dequantize(A, A, A, 4, 64, 33, 4, A, qmm.QMM_F32, stream=0)
     assert e.value.status == qmm.QMM_ERR_INVALID_ARG
+
+
+def test_launch_flags_are_per_thread_and_checked():
+    import threading
+    assert qmm.qmm_set_launch_flags(qmm.QMM_LAUNCH_PDL) == 0
+    seen = []
+    t = threading.Thread(target=lambda: seen.append(qmm.qmm_set_launch_flags(0)))
+    t.start()
+    t.join()
+    assert seen == [0]                                   # other thread starts at 0
+    assert qmm.qmm_set_launch_flags(0x10 | qmm.QMM_LAUNCH_PDL) == qmm.QMM_LAUNCH_PDL
+    assert "unknown flag" in qmm.qmm_last_error()
+    assert qmm.qmm_set_launch_flags(0) == qmm.QMM_LAUNCH_PDL   # the unknown bit was dropped

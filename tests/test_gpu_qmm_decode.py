@@ -131,3 +131,27 @@ def test_constant_weight_matmul_exact():
         x = np.full((1, K), 0x3F80, dtype=np.uint16)
         y = run_qmm(x, 1, w, N, K, True, qmm.QMM_F32)
         assert (y.cpu().numpy() == want).all()
+
+
+@pytest.mark.parametrize("bits", (4, 8))
+def test_chained_launches_with_programmatic_dependent_launch(bits):
+    """With QMM_LAUNCH_PDL each decode launch may start before the previous
+    kernel ends; it must still read the x that kernel wrote.  Chain
+    y1 = x0 . W1^T, y2 = y1 . W2^T, y3 = y2 . W3^T back to back, then check
+    every link against the oracle fed with the GPU's own intermediate."""
+    N = K = 2048
+    ws = [synth.quant_weight(900 + i + bits, N, K, bits, 64) for i in range(3)]
+    dws = [weight(w) for w in ws]
+    x0 = synth.x_bf16(901, 1, K)
+    ys = [dev(x0)] + [empty_out((1, N), qmm.QMM_BF16) for _ in ws]
+    prev = qmm.qmm_set_launch_flags(qmm.QMM_LAUNCH_PDL)
+    try:
+        for i, (w, (pw, ps, pb)) in enumerate(zip(ws, dws)):
+            qmm.qmm_quantized_matmul(ys[i], 1, pw, ps, pb, N, K, 1, 64, bits, ys[i + 1], qmm.QMM_BF16)
+        torch.cuda.synchronize()
+    finally:
+        qmm.qmm_set_launch_flags(prev)
+    for i, w in enumerate(ws):
+        x_in = ys[i].cpu().numpy().view(np.uint16)
+        ref, absy = oracle.qmm(x_in, 1, w.packed, w.scales, w.biases, N, K, True, 64, bits)
+        assert_within_tolerance(ys[i + 1], ref, absy, "link %d" % i)

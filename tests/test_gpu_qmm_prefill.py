@@ -95,3 +95,31 @@ def test_sweep_shapes(shape, M, bits):
     w = synth.quant_weight(N + K + bits, N, K, bits, 64)
     x = synth.x_bf16(M + bits, M, K)
     check_sampled(x, M, w, N, K, True, seed=M + N, what="sweep %s M%d b%d" % (shape, M, bits))
+
+
+# -- transpose = false: W stored [K, N], packed and grouped along N ------------
+
+@pytest.mark.parametrize("bits", ALL_BITS)
+@pytest.mark.parametrize("M,N,K,gs", [(17, 256, 64, 64), (200, 320, 136, 32), (300, 512, 96, 128)])
+def test_not_transposed_tensor_core_small(bits, M, N, K, gs):
+    w = synth.quant_weight(3000 + bits + M + N, K, N, bits, gs)     # stored [K, N]
+    x = synth.x_bf16(3100 + M + bits, M, K)
+    check_full(x, M, w, N, K, False, what="t0 b%d M%d N%d K%d g%d" % (bits, M, N, K, gs))
+
+
+def test_not_transposed_odd_k_falls_back():
+    """K = 77: x rows are not 16-byte aligned, so the tensor-map path cannot
+    address them; the call must still be correct."""
+    M, N, K = 40, 128, 77
+    w = synth.quant_weight(41, K, N, 4, 32)
+    x = synth.x_bf16(42, M, K)
+    check_full(x, M, w, N, K, False, qmm.QMM_F32, "t0 odd K")
+
+
+def test_prefill_not_transposed_full_size():
+    """x [2048, 4096] . W with W stored [4096, 14336] at 4 bits, group 64."""
+    p = synth.PREFILL
+    M, N, K = p["M"], p["N"], p["K"]
+    w = synth.quant_weight(13, K, N, 4, 64)
+    x = synth.x_bf16(14, M, K)
+    check_sampled(x, M, w, N, K, False, seed=15, what="prefill t0")
