@@ -491,42 +491,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, GemmArgs a) {
 
 // ----------------------------------------------------------------- host ----
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
-  return n;
-}
-
 template <int BITS, bool OUT_BF16, bool TRANS>
 cudaError_t launch_t(const uint16_t *x, const GemmArgs &a, cudaStream_t stream) {
-  auto fn = encode_fn();
-  if (!fn) return cudaErrorNotSupported;
   // TMA rows of x must start on 16-byte boundaries.
   if ((static_cast<int64_t>(a.K) * 2) % 16 != 0) return cudaErrorNotSupported;
   CUtensorMap map;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.M)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K) * 2};
-  const cuuint32_t box[2] = {BK, BM};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims,
-                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  cudaError_t me = encode_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, a.K, a.M,
+                                 static_cast<uint64_t>(a.K) * 2, BK, BM,
+                                 CU_TENSOR_MAP_SWIZZLE_128B);
+  if (me != cudaSuccess) return me;
   auto kern = gemm_kernel<BITS, OUT_BF16, TRANS>;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {

@@ -313,23 +313,7 @@ gemv_n_kernel(GemvArgs a) {
 }
 
 // ------------------------------------------------------------------------
-// transpose = true, streamed through bulk copies.  Used when K is a multiple
-// of 128 (so every row segment below is 16-byte aligned and sized).
-//
-// A block of 8 warps owns a 16-row tile and a K range [k0, k1); when the
-// weight has few rows, the blocks of a cluster split K.  At kernel start one
-// warp issues the block's whole share of the packed weight as cp.async.bulk
-// copies, one per row segment (contiguous in global memory), into shared
-// memory.  Every block does this at once, so the weight is in flight almost
-// entirely within the first few hundred nanoseconds.  Shared rows are padded
-// so that the 8 rows a quarter-warp reads fall in different banks.
-//
-// The copies are issued before griddepcontrol.wait: when the launch allows
-// programmatic dependent launch, a block streams its (read-only) weights
-// while the previous kernel in the stream is still finishing, and only x and
-// y wait for it.  x is then staged once per block, reordered so that each
-// 32-bit word holds the pair of x values that meets one bf16x2 register of
-// dequantized weights (below).
+// Shared by the transposed decode kernels.
 //
 // Code pairs.  For 1, 2 and 4 bits a word holds 32/bits codes, and codes j
 // and j + 16/bits sit exactly 16 bits apart: one shift and one LOP3
@@ -341,8 +325,6 @@ gemv_n_kernel(GemvArgs a) {
 // Warps take 128-code chunks in turn; lane (g, t) handles codes
 // [32t, 32t+32) of rows g and g+8, i.e. 16 pairs per row, and MMA r
 // contracts pairs 2r and 2r+1 with the two x words at the same positions.
-
-constexpr int kStreamWarps = 8;
 
 // The lane's 32 codes as 16 pairs: pair i is codes (pair_lo(i),
 // pair_lo(i) + pair_dist) of the 32.
@@ -409,20 +391,39 @@ __device__ __forceinline__ void lds_words(const uint8_t *p, uint32_t *v) {
   }
 }
 
-struct StreamLayout {
-  int kr;       // codes per block (multiple of 128)
-  int pitch;    // shared row pitch of the packed segments, bytes
-  int xpitch;   // shared row pitch of the staged x rows, bytes
-  int x_off;    // offset of the staged x rows
-  int red_off;  // offset of the reduction buffer
-  int bar_off;  // offset of the mbarrier
+// ------------------------------------------------------------------------
+// transpose = true, chunk-pipelined through the tensor-memory-access unit.
+// Used when K is a multiple of 128.
+//
+// Every 128-code chunk of the block's 16-row tile is one 2-D TMA box (16 rows
+// x 16*BITS bytes) with its own mbarrier; one thread issues all of them at
+// kernel start, so the weight is in flight at once, and a warp waits only for
+// the chunks it computes -- compute overlaps the stream instead of starting
+// after it.  A box lands densely (row pitch 16*BITS bytes), which keeps the
+// reads of lanes (g, t) in distinct banks for every width but 8 bits; 8-bit
+// boxes use the 128-byte swizzle (16-byte unit q of row r at q ^ (r % 8)).
+// Everything else is as in the kernel above: copies before
+// griddepcontrol.wait, x staged in pair order after it, 8 MMAs per chunk.
+
+struct TmaLayout {
+  int kr;           // codes per block (multiple of 128)
+  int box_bytes;    // shared bytes of one chunk box
+  int x_off;        // offset of the staged x rows
+  int xpitch;       // their pitch, bytes
+  int red_off;      // offset of the reduction buffer
+  int bar_off;      // offset of the chunk mbarriers
 };
 
+constexpr int kTmaWarps = 16;
+
 template <int BITS, int NT, bool OUT_BF16>
-__global__ void __launch_bounds__(32 * kStreamWarps)
-gemv_t_stream_kernel(GemvArgs a, StreamLayout L, unsigned *err) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L.bar_off);
+__global__ void __launch_bounds__(32 * kTmaWarps)
+gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayout L,
+                  unsigned *err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
   float *red = reinterpret_cast<float *>(smem + L.red_off);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -432,28 +433,28 @@ gemv_t_stream_kernel(GemvArgs a, StreamLayout L, unsigned *err) {
   const int n0 = blockIdx.x * 16;
   const int k0 = static_cast<int>(crank) * L.kr;
   const int ncodes = max(0, min(a.K, k0 + L.kr) - k0);
-  const int rows = min(16, a.N - n0);
-  const int64_t row_bytes = (static_cast<int64_t>(a.K) * BITS) >> 3;
-  const uint32_t seg = static_cast<uint32_t>(ncodes) * BITS / 8;
+  const int nchunks = ncodes >> 7;
 
-  if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
+  if (warp == 0) {
+    for (int c = lane; c <= nchunks; c += 32) mbar_init(&bars[c], 1);  // chunks, then x
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  if (warp == 0 && ncodes > 0) {
-    if (lane == 0) mbar_expect_tx(bar, rows * seg);
-    __syncwarp();
-    if (lane < rows)
-      bulk_g2s(smem + lane * L.pitch,
-               reinterpret_cast<const uint8_t *>(a.w) + (n0 + lane) * row_bytes +
-                   ((static_cast<int64_t>(k0) * BITS) >> 3),
-               seg, bar);
+  if (warp == 0) {
+    // Lane c issues chunk c's box (and c + 32, ...).
+    for (int c = lane; c < nchunks; c += 32) {
+      mbar_expect_tx(&bars[c], L.box_bytes);
+      const int xw = ((k0 + (c << 7)) * BITS) >> 5;  // word coordinate
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+          " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem + c * L.box_bytes)),
+          "l"(&wmap), "r"(xw), "r"(n0), "r"(smem_u32(&bars[c]))
+          : "memory");
+    }
   }
   griddep_launch_dependents();
 
   const int groups = a.K >> a.group_shift;
-  const int nchunks = ncodes >> 7;
   const int row0 = min(n0 + g, a.N - 1), row1 = min(n0 + g + 8, a.N - 1);
   const uint16_t *s0p = a.scales + static_cast<int64_t>(row0) * groups;
   const uint16_t *b0p = a.biases + static_cast<int64_t>(row0) * groups;
@@ -467,88 +468,88 @@ gemv_t_stream_kernel(GemvArgs a, StreamLayout L, unsigned *err) {
   uint16_t sv[4] = {0, 0, 0, 0};
   if (warp < nchunks) load_sb(warp, sv);
 
-  // x may be written by the previous kernel in the stream: wait for it, then
-  // stage this block's x range, paired the way the weights are.
+  // x may be written by the previous kernel in the stream.  Each lane reads
+  // its own 32 x values per chunk (L2-resident: every block reads the same x)
+  // and puts them in the pair order of its weights.
   griddep_wait();
-  {
-    constexpr int kSpan = 32;  // codes per staging item
-    const int spans = ncodes / kSpan;
-    for (int it = threadIdx.x; it < a.M * spans; it += blockDim.x) {
-      const int m = it / spans, sp = it - m * spans;
-      const uint4 *src = reinterpret_cast<const uint4 *>(a.x + static_cast<int64_t>(m) * a.K + k0 + kSpan * sp);
-      uint32_t nat[16], out[16];
+  auto load_x = [&](int c, uint32_t (&xv)[NT][16]) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 u = __ldg(src + i);
-        nat[4 * i] = u.x; nat[4 * i + 1] = u.y; nat[4 * i + 2] = u.z; nat[4 * i + 3] = u.w;
+    for (int nt = 0; nt < NT; ++nt) {
+      const int m = g + 8 * nt;
+      uint32_t nat[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) nat[i] = 0u;
+      if (m < a.M) {
+        const uint4 *xp = reinterpret_cast<const uint4 *>(
+            a.x + static_cast<int64_t>(m) * a.K + k0 + (c << 7) + 32 * t);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 u = __ldg(xp + i);
+          nat[4 * i] = u.x; nat[4 * i + 1] = u.y; nat[4 * i + 2] = u.z; nat[4 * i + 3] = u.w;
+        }
       }
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         constexpr int d = pair_dist<BITS>();
         const int lo = pair_lo<BITS>(i), hi = lo + d;
         const uint32_t sel = ((lo & 1) ? 0x32u : 0x10u) | (((hi & 1) ? 0x76u : 0x54u) << 8);
-        out[i] = (d == 1) ? nat[i] : prmt(nat[lo >> 1], nat[hi >> 1], sel);
+        xv[nt][i] = (d == 1) ? nat[i] : prmt(nat[lo >> 1], nat[hi >> 1], sel);
       }
-      uint4 *dst = reinterpret_cast<uint4 *>(smem + L.x_off + m * L.xpitch + 2 * kSpan * sp);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) dst[i] = make_uint4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]);
     }
-  }
-  __syncthreads();
+  };
 
-  float acc[NT][4];
+  // Two accumulator sets (even and odd MMA steps) keep the MMA chain short.
+  float acc[2][NT][4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+  for (int h = 0; h < 2; ++h)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[h][nt][i] = 0.0f;
 
-  bool ready = ncodes > 0;
-  if (ready) {
+  constexpr int kRowBytes = 16 * BITS;  // one row of a chunk box
+  bool ok = true;
+  for (int c = warp; ok && c < nchunks; c += kTmaWarps) {
+    uint16_t cur[4] = {sv[0], sv[1], sv[2], sv[3]};
+    if (c + kTmaWarps < nchunks) load_sb(c + kTmaWarps, sv);
+    uint32_t xv[NT][16];
+    load_x(c, xv);
     uint32_t spins = 0;
-    while (!mbar_try_wait(bar, 0)) {
+    while (!mbar_try_wait(&bars[c], 0)) {
       if (++spins > (1u << 24)) {
         if (lane == 0) atomicOr(err, kErrTimeoutBit);
-        ready = false;
+        ok = false;
         break;
       }
     }
-  }
-  if (ready) {
-    for (int c = warp; c < nchunks; c += kStreamWarps) {
-      uint16_t cur[4] = {sv[0], sv[1], sv[2], sv[3]};
-      if (c + kStreamWarps < nchunks) load_sb(c + kStreamWarps, sv);
-      const int cc = (c << 7) + 32 * t;  // lane's first code within the block's range
-      uint32_t v0[BITS], v1[BITS];
-      lds_words<BITS>(smem + g * L.pitch + ((cc * BITS) >> 3), v0);
-      lds_words<BITS>(smem + (g + 8) * L.pitch + ((cc * BITS) >> 3), v1);
-      uint32_t xv[NT][16];
+    if (!ok) break;
+    const uint8_t *box = smem + c * L.box_bytes;
+    uint32_t v0[BITS], v1[BITS];
+    if constexpr (BITS == 8) {
+      // 128-byte swizzle: the lane's 32 bytes are 16-byte units 2t, 2t+1.
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int m = g + 8 * nt;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) xv[nt][i] = 0u;
-        if (m < a.M) {
-          const uint4 *xp = reinterpret_cast<const uint4 *>(smem + L.x_off + m * L.xpitch + 2 * cc);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint4 u = xp[i];
-            xv[nt][4 * i] = u.x; xv[nt][4 * i + 1] = u.y; xv[nt][4 * i + 2] = u.z; xv[nt][4 * i + 3] = u.w;
-          }
-        }
+      for (int i = 0; i < 2; ++i) {
+        const uint4 u0 = *reinterpret_cast<const uint4 *>(box + g * 128 + (((2 * t + i) ^ g) << 4));
+        const uint4 u1 = *reinterpret_cast<const uint4 *>(box + (g + 8) * 128 + (((2 * t + i) ^ g) << 4));
+        v0[4 * i] = u0.x; v0[4 * i + 1] = u0.y; v0[4 * i + 2] = u0.z; v0[4 * i + 3] = u0.w;
+        v1[4 * i] = u1.x; v1[4 * i + 1] = u1.y; v1[4 * i + 2] = u1.z; v1[4 * i + 3] = u1.w;
       }
-      const uint32_t s0 = bcast_bf16x2(cur[0]), b0 = bcast_bf16x2(cur[1]);
-      const uint32_t s1 = bcast_bf16x2(cur[2]), b1 = bcast_bf16x2(cur[3]);
-      const float fs0 = bf16_bits_to_f32(cur[0]), fb0 = bf16_bits_to_f32(cur[1]);
-      const float fs1 = bf16_bits_to_f32(cur[2]), fb1 = bf16_bits_to_f32(cur[3]);
+    } else {
+      lds_words<BITS>(box + g * kRowBytes + t * 4 * BITS, v0);
+      lds_words<BITS>(box + (g + 8) * kRowBytes + t * 4 * BITS, v1);
+    }
+    const uint32_t s0 = bcast_bf16x2(cur[0]), b0 = bcast_bf16x2(cur[1]);
+    const uint32_t s1 = bcast_bf16x2(cur[2]), b1 = bcast_bf16x2(cur[3]);
+    const float fs0 = bf16_bits_to_f32(cur[0]), fb0 = bf16_bits_to_f32(cur[1]);
+    const float fs1 = bf16_bits_to_f32(cur[2]), fb1 = bf16_bits_to_f32(cur[3]);
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        uint32_t a0, a2, a1, a3;
-        dequant_mma_pairs<BITS>(v0, r, s0, b0, fs0, fb0, a0, a2);
-        dequant_mma_pairs<BITS>(v1, r, s1, b1, fs1, fb1, a1, a3);
+    for (int r = 0; r < 8; ++r) {
+      uint32_t a0, a2, a1, a3;
+      dequant_mma_pairs<BITS>(v0, r, s0, b0, fs0, fb0, a0, a2);
+      dequant_mma_pairs<BITS>(v1, r, s1, b1, fs1, fb1, a1, a3);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          mma_bf16_16816(acc[nt], a0, a1, a2, a3, xv[nt][2 * r], xv[nt][2 * r + 1]);
-      }
+      for (int nt = 0; nt < NT; ++nt)
+        mma_bf16_16816(acc[r & 1][nt], a0, a1, a2, a3, xv[nt][2 * r], xv[nt][2 * r + 1]);
     }
   }
 
@@ -556,8 +557,8 @@ gemv_t_stream_kernel(GemvArgs a, StreamLayout L, unsigned *err) {
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) flat[nt * 4 + i] = acc[nt][i];
-  reduce_and_store<NT * 4>(flat, red, kStreamWarps, static_cast<int>(csize), a, OUT_BF16,
+    for (int i = 0; i < 4; ++i) flat[nt * 4 + i] = acc[0][nt][i] + acc[1][nt][i];
+  reduce_and_store<NT * 4>(flat, red, kTmaWarps, static_cast<int>(csize), a, OUT_BF16,
                            [&](int ln, int i, int &m, int &n) {
                              const int gg = ln >> 2, tt = ln & 3, nt = i >> 2, e = i & 3;
                              n = n0 + gg + 8 * (e >> 1);
@@ -628,42 +629,44 @@ cudaError_t launch_t(const GemvArgs &a0, cudaStream_t stream) {
                           stream, a);
 }
 
-// A shared row pitch congruent to 16 * BITS modulo 128 (16 for 8-bit codes)
-// puts the rows read by one quarter (or half) warp in different banks.
-constexpr int row_pad_target(int bits) { return bits == 8 ? 16 : (16 * bits) % 128; }
-
 template <int BITS, int NT, bool OUT_BF16>
-cudaError_t launch_t_stream(const GemvArgs &a, bool pdl, cudaStream_t stream) {
+cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, cudaStream_t stream) {
   const int64_t tiles = (a.N + 15) / 16;
+  const int box_bytes = 16 * 16 * BITS;
   auto kr_of = [&](int c) { return ((a.K / c + 127) / 128) * 128; };
   auto smem_of = [&](int c) {
     const int kr = kr_of(c);
-    return 16 * (kr * BITS / 8 + 128) + a.M * (2 * kr + 16) + kStreamWarps * NT * 4 * 32 * 4 + 64;
+    return (kr / 128) * (box_bytes + 8) + kTmaWarps * NT * 4 * 32 * 4 + 2048;
   };
   // Split K over a cluster only when the weight has too few 16-row tiles to
   // give every SM work, or one block's share would not fit.
   int C = 1;
   while (C < 8 && kr_of(2 * C) >= 128 && (tiles * C < 240 || smem_of(C) > 100 * 1024)) C *= 2;
   if (smem_of(C) > 200 * 1024) return cudaErrorNotSupported;
-  StreamLayout L;
+  TmaLayout L;
   L.kr = kr_of(C);
-  const int seg = L.kr * BITS / 8;
-  L.pitch = seg + ((row_pad_target(BITS) - seg % 128) + 128) % 128;
-  L.xpitch = 2 * L.kr + 16;
-  L.x_off = 16 * L.pitch;
-  L.red_off = L.x_off + ((a.M * L.xpitch + 15) / 16) * 16;
-  L.bar_off = L.red_off + kStreamWarps * NT * 4 * 32 * 4;
-  const size_t smem = L.bar_off + 16;
+  L.box_bytes = box_bytes;
+  const int nch = L.kr / 128;
+  L.x_off = nch * box_bytes;  // x is read from global memory by each lane
+  L.xpitch = 0;
+  L.red_off = L.x_off;
+  L.bar_off = L.red_off + kTmaWarps * NT * 4 * 32 * 4;
+  const size_t smem = L.bar_off + 8 * (nch + 1) + 1024;  // + slack for the 1024-byte base
+  CUtensorMap wmap;
+  cudaError_t e = encode_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.w,
+                                static_cast<uint64_t>(a.K) * BITS / 32, a.N,
+                                static_cast<uint64_t>(a.K) * BITS / 8, 4 * BITS, 16,
+                                BITS == 8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
   unsigned *err = device_error_word();
   if (!err) return cudaErrorInvalidSymbol;
-  auto kern = gemv_t_stream_kernel<BITS, NT, OUT_BF16>;
+  auto kern = gemv_t_tma_kernel<BITS, NT, OUT_BF16>;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  return launch_ex(kern, dim3(static_cast<unsigned>(tiles), C), dim3(32 * kStreamWarps), smem, C,
-                   pdl, stream, a, L, err);
+  return launch_ex(kern, dim3(static_cast<unsigned>(tiles), C), dim3(32 * kTmaWarps), smem, C,
+                   pdl, stream, wmap, a, L, err);
 }
 
 template <int BITS, bool OUT_BF16>
@@ -683,11 +686,11 @@ cudaError_t launch_bits(const GemvArgs &a, bool transpose, bool y_bf16, bool pdl
   if (transpose && a.K % 128 == 0) {
     cudaError_t e;
     if (a.M <= 8)
-      e = y_bf16 ? launch_t_stream<BITS, 1, true>(a, pdl, stream)
-                 : launch_t_stream<BITS, 1, false>(a, pdl, stream);
+      e = y_bf16 ? launch_t_tma<BITS, 1, true>(a, pdl, stream)
+                 : launch_t_tma<BITS, 1, false>(a, pdl, stream);
     else
-      e = y_bf16 ? launch_t_stream<BITS, 2, true>(a, pdl, stream)
-                 : launch_t_stream<BITS, 2, false>(a, pdl, stream);
+      e = y_bf16 ? launch_t_tma<BITS, 2, true>(a, pdl, stream)
+                 : launch_t_tma<BITS, 2, false>(a, pdl, stream);
     if (e != cudaErrorNotSupported) return e;
   }
   if (transpose) {

@@ -2,6 +2,7 @@
 // Arguments reaching these launchers have already been validated.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace qmm {
@@ -27,6 +28,14 @@ struct PackedWeight {
 unsigned *device_error_word();
 // Synchronize `stream`, read the word and clear it.
 cudaError_t take_device_error(cudaStream_t stream, unsigned *bits);
+
+// tensormap.cpp: a 2-D tiled tensor map over a row-major array of `outer`
+// rows of `inner` elements, `row_bytes` apart; boxes of box_inner x
+// box_outer elements, out-of-range elements read as zero.
+cudaError_t encode_map_2d(CUtensorMap *map, CUtensorMapDataType type, const void *base,
+                          uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                          uint32_t box_outer, CUtensorMapSwizzle swizzle);
+int sm_count();
 
 // dequant.cu: out[r, :] = dequant(W[src(r), :]) for r < out_rows, where
 // src(r) = idx[r] if idx is given (a rows gather) else r.
