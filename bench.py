@@ -147,6 +147,74 @@ class Case:
         return 2 * self.M * self.N * self.K
 
 
+def graph_of(torch, fn):
+    """Run fn once eagerly on a side stream, then capture it in a CUDA graph."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def dequant_rows_detail(torch, qmm, synth, peaks, steps, warmup):
+    """Standalone dequantize to bf16 and the rows gather, as GB/s of their
+    algorithmic bytes (codes + scales + biases read, bf16 written, indices)."""
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(
+        {np.dtype(np.uint32): np.int32, np.dtype(np.uint16): np.int16}[a.dtype])).cuda()
+    out = {}
+    N, K = 14336, 4096
+    for bits in (4, 8):
+        w = synth.quant_weight(40 + bits, N, K, bits, 64)
+        copies = [(dev(np.roll(w.packed, r, 0)), dev(np.roll(w.scales, r, 0)),
+                   dev(np.roll(w.biases, r, 0))) for r in range(2)]
+        o = torch.empty((2, N, K), dtype=torch.int16, device="cuda")
+        def fn():
+            for r in range(2):
+                pw, ps, pb = copies[r]
+                qmm.qmm_dequantize(pw, ps, pb, N, K, 64, bits, o[r], qmm.QMM_BF16)
+        t = time_graph(torch, graph_of(torch, fn), steps, warmup) / 2
+        nbytes = w.nbytes + 2 * N * K
+        out["dequantize_b%d_%dx%d_bf16" % (bits, N, K)] = {
+            "us": round(t * 1e3, 2), "GB/s": round(nbytes / (t * 1e-3) / 1e9, 1),
+            "frac_hbm": round(nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
+        del copies, o
+    T, C = synth.ROWS_TABLE
+    w = synth.quant_weight(2, T, C, 4, 64)
+    pw, ps, pb = dev(w.packed), dev(w.scales), dev(w.biases)
+    idxs = [dev(synth.indices(3 + r, synth.ROWS_GATHER, T)) for r in range(4)]
+    o = torch.empty((4, synth.ROWS_GATHER, C), dtype=torch.int16, device="cuda")
+    def fn():
+        for r in range(4):
+            qmm.qmm_rows(pw, ps, pb, T, C, idxs[r], synth.ROWS_GATHER, 64, 4, o[r], qmm.QMM_BF16)
+    t = time_graph(torch, graph_of(torch, fn), steps, warmup) / 4
+    row_bytes = C * 4 // 8 + 4 * (C // 64)
+    nbytes = synth.ROWS_GATHER * (row_bytes + 2 * C + 4)
+    out["rows_4096_of_%dx%d_b4_bf16" % (T, C)] = {
+        "us": round(t * 1e3, 2), "GB/s": round(nbytes / (t * 1e-3) / 1e9, 1),
+        "frac_hbm": round(nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
+    return out
+
+
+def measured_traffic():
+    """DRAM bytes per launch of the decode kernel from the committed ncu capture,
+    or None if the kernel source changed since it was taken."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "decode_gemv_traffic.json")
+    src = os.path.join(ROOT, "mlx_grouped_affine_gb300", "csrc", "gemv.cu")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return d.get("dram_bytes_per_launch") if d.get("gemv_cu_sha256") == sha else None
+
+
 def time_graph(torch, graph, steps, warmup, barrier=None):
     for _ in range(warmup):
         graph.replay()
@@ -244,6 +312,9 @@ def run_gpu(args):
         del c
         torch.cuda.empty_cache()
     if rank == 0 and not args.quick:
+        detail.update(dequant_rows_detail(torch, qmm, synth, peaks, max(20, args.steps // 50),
+                                          args.warmup))
+        torch.cuda.empty_cache()
         for bits in (4, 8):
             for M in synth.DECODE_M:
                 c = Case(torch, qmm, synth, M, N, K, bits, 64, seed=10 + bits + M)
@@ -269,7 +340,7 @@ def run_gpu(args):
                                 "programmatic dependent launch")},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "traffic": None, "peak_source": peaks["source"]},
+                     "traffic": measured_traffic(), "peak_source": peaks["source"]},
         "clocks": clocks, "e2e": e2e, "gpu_launches": args.steps * head.R,
         "detail": detail,
     }
