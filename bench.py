@@ -46,6 +46,21 @@ def load_peaks():
     return d
 
 
+def max_over_ranks(value, dist=None, device="cpu"):
+    """The largest value over all ranks (the slowest rank's time)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank, world, max_seconds):
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return world * units_per_rank / max_seconds
+
+
 def gemv_bytes(M, N, K, bits, group):
     """Algorithmic bytes of one launch: codes + scales + biases + x + y (bf16)."""
     return N * K * bits // 8 + 4 * N * (K // group) + 2 * M * K + 2 * M * N
@@ -258,13 +273,10 @@ def run_gpu(args):
     with ClockSampler(local) as clk:
         ms = time_graph(torch, head.graph, args.steps, args.warmup, barrier)
     clocks = clk.summary()
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, device="cuda")
     launch_ms = ms / head.R
     per_launch = head.bytes_per_launch()
-    value = world * head.R * per_launch / (ms * 1e-3) / 1e9
+    value = job_value(head.R * per_launch, world, ms * 1e-3) / 1e9
     achieved = per_launch / (launch_ms * 1e-3) / 1e9
 
     # End to end through the public API with host buffers: per step, x for the
@@ -394,7 +406,7 @@ def run_reference(args):
     oracle.qmm(x, 1, w.packed[:probe_rows], w.scales[:probe_rows], w.biases[:probe_rows],
                probe_rows, K, True, 64, 4, nthreads=threads)
     per_row = (time.perf_counter() - t0) / probe_rows
-    budget = 120.0 / max(1, args.steps + args.warmup)
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
     rows = int(max(16, min(N, budget / max(per_row, 1e-9))))
     for _ in range(args.warmup):
         oracle.qmm(x, 1, w.packed[:rows], w.scales[:rows], w.biases[:rows], rows, K, True, 64, 4,
@@ -458,6 +470,8 @@ def main():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-pdl", action="store_true", help="launch decode kernels without PDL")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--ref-seconds", type=float, default=120.0,
+                   help="total CPU time budget of the reference arm")
     args = p.parse_args()
     if args.profile:
         run_profile(args.profile, args.launches)

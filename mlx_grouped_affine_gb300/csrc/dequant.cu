@@ -5,14 +5,15 @@
 // src(r) = idx[r] (maya2_mlx quant.py, `rows`: gather then dequantize, done
 // here in one pass that reads only the gathered rows).
 //
-// HBM-bound: per 8 outputs a thread reads `bits` bytes of codes and writes 16
-// (bf16) or 32 (fp32) bytes, so the kernel is sized for coalesced 16-byte
-// stores.  A block covers 2048 consecutive columns of one output row: thread t
-// owns the 8-code chunk t, whose codes are the `bits` bytes at byte offset
-// 8*bits*t/8 of the row, read through the one or two aligned words that hold
-// them.  Each element is fp32 fma(scale, code, bias): the product of a bf16
-// scale and a code below 2^8 is exact, so this rounds once, at the add
-// (rlx-moshi src/mlx_dequant.rs, `dequantize_affine`: scale * code + bias).
+// HBM-bound: per 32 outputs a thread reads `bits` words of codes (32 codes
+// always take exactly `bits` words, so every thread's codes start on a word
+// boundary and load with the widest aligned vector loads) and writes 64 (bf16)
+// or 128 (fp32) contiguous bytes; consecutive threads cover consecutive code
+// groups, so a warp streams 2 or 4 KB of output.  Each element is fp32
+// fma(scale, code, bias): the product of a bf16 scale and a code below 2^8 is
+// exact, so this rounds once, at the add (rlx-moshi src/mlx_dequant.rs,
+// `dequantize_affine`: scale * code + bias); bf16 output is its
+// round-to-nearest-even.
 #include "common.cuh"
 #include "internal.h"
 
@@ -26,68 +27,51 @@ static __device__ unsigned g_device_error;
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kColsPerBlock = kThreads * 8;
-
-template <int BITS>
-__device__ __forceinline__ uint64_t load_chunk_window(const uint32_t *__restrict__ row,
-                                                      int chunk) {
-  // The chunk's codes start at bit 8*BITS*chunk of the row's stream.
-  const int bit = 8 * BITS * chunk;
-  const int word = bit >> 5, sh = bit & 31;
-  uint32_t lo = __ldg(row + word);
-  uint32_t hi = (sh + 8 * BITS > 32) ? __ldg(row + word + 1) : 0u;
-  return ((static_cast<uint64_t>(hi) << 32) | lo) >> sh;
-}
 
 template <int BITS, bool OUT_BF16, bool GATHER>
 __global__ void __launch_bounds__(kThreads)
 dequant_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ scales,
                const uint16_t *__restrict__ biases, const uint32_t *__restrict__ idx,
-               int64_t out_rows, int64_t table_rows, int64_t cols, int group_shift,
-               int blocks_per_row, void *__restrict__ out, unsigned *err) {
+               int64_t row0, uint32_t groups_total, uint32_t groups_per_row, int64_t table_rows,
+               int64_t cols, int group_shift, void *__restrict__ out, unsigned *err) {
   const int64_t words_per_row = (cols * BITS) >> 5;
-  const int64_t groups = cols >> group_shift;
-  const int chunks_per_row = static_cast<int>(cols >> 3);
-  const int64_t total_blocks = out_rows * blocks_per_row;
-  for (int64_t blk = blockIdx.x; blk < total_blocks; blk += gridDim.x) {
-    const int64_t r = blk / blocks_per_row;
-    const int chunk = static_cast<int>(blk - r * blocks_per_row) * kThreads + threadIdx.x;
-    if (chunk >= chunks_per_row) continue;
+  const int64_t sb_per_row = cols >> group_shift;
+  for (uint32_t gid = blockIdx.x * kThreads + threadIdx.x; gid < groups_total;
+       gid += gridDim.x * kThreads) {
+    const uint32_t rl = gid / groups_per_row, j = gid - rl * groups_per_row;
+    const int64_t r = row0 + rl;
     int64_t src = r;
     bool in_table = true;
     if (GATHER) {
       src = __ldg(idx + r);
       in_table = src < table_rows;
-      if (!in_table && chunk == 0) atomicOr(err, kErrIndexBit);
+      if (!in_table && j == 0) atomicOr(err, kErrIndexBit);
     }
-    float v[8];
+    float v[32];
     if (in_table) {
-      const uint64_t win = load_chunk_window<BITS>(w + src * words_per_row, chunk);
-      const int64_t g = (static_cast<int64_t>(chunk) * 8) >> group_shift;
-      const float s = bf16_bits_to_f32(__ldg(scales + src * groups + g));
-      const float b = bf16_bits_to_f32(__ldg(biases + src * groups + g));
-      constexpr uint32_t mask = (1u << BITS) - 1u;
+      uint32_t words[BITS];
+      load_words<BITS>(w + src * words_per_row + static_cast<int64_t>(j) * BITS, words);
+      const int64_t g = (static_cast<int64_t>(j) * 32) >> group_shift;
+      const float s = bf16_bits_to_f32(__ldg(scales + src * sb_per_row + g));
+      const float b = bf16_bits_to_f32(__ldg(biases + src * sb_per_row + g));
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t code = static_cast<uint32_t>(win >> (j * BITS)) & mask;
-        v[j] = __fmaf_rn(s, static_cast<float>(code), b);
-      }
+      for (int i = 0; i < 32; ++i)
+        v[i] = __fmaf_rn(s, static_cast<float>(code_at<BITS>(words, i)), b);
     } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+      for (int i = 0; i < 32; ++i) v[i] = 0.0f;
     }
-    const int64_t o = r * cols + static_cast<int64_t>(chunk) * 8;
+    const int64_t o = r * cols + static_cast<int64_t>(j) * 32;
     if (OUT_BF16) {
-      uint4 p;
-      p.x = pack_bf16x2(v[0], v[1]);
-      p.y = pack_bf16x2(v[2], v[3]);
-      p.z = pack_bf16x2(v[4], v[5]);
-      p.w = pack_bf16x2(v[6], v[7]);
-      *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + o) = p;
+      uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + o);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        dst[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                            pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
     } else {
       float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(out) + o);
-      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     }
   }
 }
@@ -95,16 +79,27 @@ dequant_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ scal
 template <int BITS, bool OUT_BF16, bool GATHER>
 cudaError_t launch_t(const PackedWeight &pw, const uint32_t *idx, int64_t out_rows,
                      void *out, cudaStream_t stream) {
-  const int blocks_per_row = static_cast<int>((pw.cols + kColsPerBlock - 1) / kColsPerBlock);
-  const int64_t total = out_rows * blocks_per_row;
-  const unsigned grid = static_cast<unsigned>(total < (1ll << 30) ? total : (1ll << 30));
   const int group_shift = pw.group == 32 ? 5 : pw.group == 64 ? 6 : 7;
   unsigned *err = device_error_word();
   if (!err) return cudaErrorInvalidSymbol;
-  dequant_kernel<BITS, OUT_BF16, GATHER><<<grid, kThreads, 0, stream>>>(
-      pw.w, pw.scales, pw.biases, idx, out_rows, pw.rows, pw.cols, group_shift,
-      blocks_per_row, out, err);
-  return cudaGetLastError();
+  const int64_t gpr = pw.cols / 32;
+  if (gpr >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+  // Batches of whole rows with fewer than 2^31 code groups each, so that the
+  // kernel's index arithmetic stays in 32 bits.
+  const int64_t rows_per_batch = ((int64_t(1) << 31) - 1) / gpr;
+  const int max_blocks = 16 * sm_count();
+  for (int64_t r0 = 0; r0 < out_rows; r0 += rows_per_batch) {
+    const int64_t rows = out_rows - r0 < rows_per_batch ? out_rows - r0 : rows_per_batch;
+    const uint32_t total = static_cast<uint32_t>(rows * gpr);
+    const int64_t blocks = (static_cast<int64_t>(total) + kThreads - 1) / kThreads;
+    const unsigned grid = static_cast<unsigned>(blocks < max_blocks ? blocks : max_blocks);
+    dequant_kernel<BITS, OUT_BF16, GATHER><<<grid, kThreads, 0, stream>>>(
+        pw.w, pw.scales, pw.biases, idx, r0, total, static_cast<uint32_t>(gpr), pw.rows,
+        pw.cols, group_shift, out, err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 template <int BITS>

@@ -414,10 +414,13 @@ struct TmaLayout {
   int bar_off;      // offset of the chunk mbarriers
 };
 
-constexpr int kTmaWarps = 16;
+// Warps per block: 16 for one n8 tile of x rows; 8 for two (twice the
+// registers), so that two blocks fit on an SM either way.
+template <int NT>
+__host__ __device__ constexpr int tma_warps() { return NT == 1 ? 16 : 8; }
 
 template <int BITS, int NT, bool OUT_BF16>
-__global__ void __launch_bounds__(32 * kTmaWarps)
+__global__ void __launch_bounds__(32 * tma_warps<NT>())
 gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayout L,
                   unsigned *err) {
   extern __shared__ uint8_t smem_raw[];
@@ -509,9 +512,9 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
 
   constexpr int kRowBytes = 16 * BITS;  // one row of a chunk box
   bool ok = true;
-  for (int c = warp; ok && c < nchunks; c += kTmaWarps) {
+  for (int c = warp; ok && c < nchunks; c += tma_warps<NT>()) {
     uint16_t cur[4] = {sv[0], sv[1], sv[2], sv[3]};
-    if (c + kTmaWarps < nchunks) load_sb(c + kTmaWarps, sv);
+    if (c + tma_warps<NT>() < nchunks) load_sb(c + tma_warps<NT>(), sv);
     uint32_t xv[NT][16];
     load_x(c, xv);
     uint32_t spins = 0;
@@ -558,7 +561,7 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int i = 0; i < 4; ++i) flat[nt * 4 + i] = acc[0][nt][i] + acc[1][nt][i];
-  reduce_and_store<NT * 4>(flat, red, kTmaWarps, static_cast<int>(csize), a, OUT_BF16,
+  reduce_and_store<NT * 4>(flat, red, tma_warps<NT>(), static_cast<int>(csize), a, OUT_BF16,
                            [&](int ln, int i, int &m, int &n) {
                              const int gg = ln >> 2, tt = ln & 3, nt = i >> 2, e = i & 3;
                              n = n0 + gg + 8 * (e >> 1);
@@ -636,7 +639,7 @@ cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, cudaStream_t stream) {
   auto kr_of = [&](int c) { return ((a.K / c + 127) / 128) * 128; };
   auto smem_of = [&](int c) {
     const int kr = kr_of(c);
-    return (kr / 128) * (box_bytes + 8) + kTmaWarps * NT * 4 * 32 * 4 + 2048;
+    return (kr / 128) * (box_bytes + 8) + tma_warps<NT>() * NT * 4 * 32 * 4 + 2048;
   };
   // Split K over a cluster only when the weight has too few 16-row tiles to
   // give every SM work, or one block's share would not fit.
@@ -650,7 +653,7 @@ cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, cudaStream_t stream) {
   L.x_off = nch * box_bytes;  // x is read from global memory by each lane
   L.xpitch = 0;
   L.red_off = L.x_off;
-  L.bar_off = L.red_off + kTmaWarps * NT * 4 * 32 * 4;
+  L.bar_off = L.red_off + tma_warps<NT>() * NT * 4 * 32 * 4;
   const size_t smem = L.bar_off + 8 * (nch + 1) + 1024;  // + slack for the 1024-byte base
   CUtensorMap wmap;
   cudaError_t e = encode_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.w,
@@ -665,7 +668,7 @@ cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, cudaStream_t stream) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  return launch_ex(kern, dim3(static_cast<unsigned>(tiles), C), dim3(32 * kTmaWarps), smem, C,
+  return launch_ex(kern, dim3(static_cast<unsigned>(tiles), C), dim3(32 * tma_warps<NT>()), smem, C,
                    pdl, stream, wmap, a, L, err);
 }
 
