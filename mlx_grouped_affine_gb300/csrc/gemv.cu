@@ -315,12 +315,15 @@ gemv_n_kernel(GemvArgs a) {
 // ------------------------------------------------------------------------
 // Shared by the transposed decode kernels.
 //
-// Code pairs.  For 1, 2 and 4 bits a word holds 32/bits codes, and codes j
-// and j + 16/bits sit exactly 16 bits apart: one shift and one LOP3
+// Code pairs.  For 1 and 2 bits a word holds 32/bits codes, and codes j and
+// j + 16/bits sit exactly 16 bits apart: one shift and one LOP3
 // ((w >> j*bits) & mask16x2 | 128.0x2) make the bf16x2 pair (128 + c_j,
 // 128 + c_{j+16/bits}); subtracting 128 is exact, then one bf16x2 FMA gives
-// RN(s*c + b) for both.  8-bit codes (above 127) go through fp32, paired
-// (j, j+2); 3, 5 and 6 bits are paired naturally (j, j+1).
+// RN(s*c + b) for both.  Such pairs need x in the same order, which costs a
+// permute per x word.  For 4 bits the natural pair (codes 2i, 2i+1: the two
+// nibbles of byte i) is as cheap -- one byte permute against w >> 4 and one
+// LOP3 -- so 4-bit codes and everything wider are paired naturally and x is
+// used as it lies.  8-bit codes (above 127) go through fp32.
 //
 // Warps take 128-code chunks in turn; lane (g, t) handles codes
 // [32t, 32t+32) of rows g and g+8, i.e. 16 pairs per row, and MMA r
@@ -330,22 +333,18 @@ gemv_n_kernel(GemvArgs a) {
 // pair_lo(i) + pair_dist) of the 32.
 template <int BITS>
 __host__ __device__ constexpr int pair_dist() {
-  return BITS == 1 ? 16 : BITS == 2 ? 8 : BITS == 4 ? 4 : BITS == 8 ? 2 : 1;
+  return BITS == 1 ? 16 : BITS == 2 ? 8 : 1;
 }
 template <int BITS>
 __host__ __device__ constexpr int pair_lo(int i) {
-  return BITS == 1 ? i
-       : BITS == 2 ? (i / 8) * 16 + i % 8
-       : BITS == 4 ? (i / 4) * 8 + i % 4
-       : BITS == 8 ? (i / 2) * 4 + i % 2
-       : 2 * i;
+  return BITS == 1 ? i : BITS == 2 ? (i / 8) * 16 + i % 8 : 2 * i;
 }
 
 // Pairs 2r and 2r+1 of a lane's 32 codes held in v[] (BITS words).
 template <int BITS>
 __device__ __forceinline__ void dequant_mma_pairs(const uint32_t *v, int r, uint32_t s2, uint32_t b2,
                                                   float sf, float bf, uint32_t &p0, uint32_t &p1) {
-  if constexpr (BITS == 1 || BITS == 2 || BITS == 4) {
+  if constexpr (BITS == 1 || BITS == 2) {
     constexpr int per_word = 16 / BITS;  // pairs per word
     constexpr uint32_t mask = ((1u << BITS) - 1u) * 0x00010001u;
     const int i0 = 2 * r, i1 = 2 * r + 1;
@@ -354,15 +353,25 @@ __device__ __forceinline__ void dequant_mma_pairs(const uint32_t *v, int r, uint
     const uint32_t q1 = and_or(w1 >> ((i1 % per_word) * BITS), mask, kMagic);
     p0 = bf16x2_fma(bf16x2_sub(q0, kMagic), s2, b2);
     p1 = bf16x2_fma(bf16x2_sub(q1, kMagic), s2, b2);
+  } else if constexpr (BITS == 4) {
+    // codes 4r .. 4r+3 are bytes 2(r%2), 2(r%2)+1 of word r/2 (low nibble
+    // first); byte j of w and of w >> 4 hold codes 2j and 2j+1 in their low
+    // nibbles.
+    const uint32_t w = v[r >> 1], w4 = w >> 4;
+    const uint32_t j0 = 2u * (r & 1), j1 = j0 + 1;
+    const uint32_t q0 = and_or(prmt(w, w4, 0x0400u | (j0 << 8) | j0), 0x000F000Fu, kMagic);
+    const uint32_t q1 = and_or(prmt(w, w4, 0x0400u | (j1 << 8) | j1), 0x000F000Fu, kMagic);
+    p0 = bf16x2_fma(bf16x2_sub(q0, kMagic), s2, b2);
+    p1 = bf16x2_fma(bf16x2_sub(q1, kMagic), s2, b2);
   } else if constexpr (BITS == 8) {
-    // word r holds codes 4r .. 4r+3; pair 2r = bytes (0, 2), pair 2r+1 = (1, 3)
+    // word r holds codes 4r .. 4r+3, one per byte
     const uint32_t w = v[r];
     const float c0 = __uint_as_float(prmt(w, 0x4B000000u, 0x7650u)) - 8388608.0f;
     const float c1 = __uint_as_float(prmt(w, 0x4B000000u, 0x7651u)) - 8388608.0f;
     const float c2 = __uint_as_float(prmt(w, 0x4B000000u, 0x7652u)) - 8388608.0f;
     const float c3 = __uint_as_float(prmt(w, 0x4B000000u, 0x7653u)) - 8388608.0f;
-    p0 = pack_bf16x2(__fmaf_rn(sf, c0, bf), __fmaf_rn(sf, c2, bf));
-    p1 = pack_bf16x2(__fmaf_rn(sf, c1, bf), __fmaf_rn(sf, c3, bf));
+    p0 = pack_bf16x2(__fmaf_rn(sf, c0, bf), __fmaf_rn(sf, c1, bf));
+    p1 = pack_bf16x2(__fmaf_rn(sf, c2, bf), __fmaf_rn(sf, c3, bf));
   } else {
     const uint32_t q0 = code_at<BITS>(v, 4 * r) | (code_at<BITS>(v, 4 * r + 1) << 16) | kMagic;
     const uint32_t q1 = code_at<BITS>(v, 4 * r + 2) | (code_at<BITS>(v, 4 * r + 3) << 16) | kMagic;
@@ -418,6 +427,7 @@ struct TmaLayout {
 // registers), so that two blocks fit on an SM either way.
 template <int NT>
 __host__ __device__ constexpr int tma_warps() { return NT == 1 ? 16 : 8; }
+constexpr int kTmaMaxChunksPerWarp = 4;
 
 template <int BITS, int NT, bool OUT_BF16>
 __global__ void __launch_bounds__(32 * tma_warps<NT>())
@@ -468,38 +478,50 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
     sv[0] = __ldg(s0p + gi); sv[1] = __ldg(b0p + gi);
     sv[2] = __ldg(s1p + gi); sv[3] = __ldg(b1p + gi);
   };
-  uint16_t sv[4] = {0, 0, 0, 0};
-  if (warp < nchunks) load_sb(warp, sv);
+  // Scales and biases of every chunk this warp will compute, before the
+  // wait: they are weights too, and their HBM latency then overlaps the
+  // previous kernel instead of the chunk loop.
+  constexpr int kW = tma_warps<NT>();
+  uint16_t sv[kTmaMaxChunksPerWarp][4];
+#pragma unroll
+  for (int j = 0; j < kTmaMaxChunksPerWarp; ++j) {
+    sv[j][0] = sv[j][1] = sv[j][2] = sv[j][3] = 0;
+    if (warp + j * kW < nchunks) load_sb(warp + j * kW, sv[j]);
+  }
 
   // x may be written by the previous kernel in the stream.  Each lane reads
   // its own 32 x values per chunk (L2-resident: every block reads the same x)
   // and puts them in the pair order of its weights.
   griddep_wait();
+  // Lanes whose x row is beyond M keep zero fragments throughout.
   auto load_x = [&](int c, uint32_t (&xv)[NT][16]) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int m = g + 8 * nt;
-      uint32_t nat[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) nat[i] = 0u;
       if (m < a.M) {
         const uint4 *xp = reinterpret_cast<const uint4 *>(
             a.x + static_cast<int64_t>(m) * a.K + k0 + (c << 7) + 32 * t);
+        uint32_t nat[16];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint4 u = __ldg(xp + i);
           nat[4 * i] = u.x; nat[4 * i + 1] = u.y; nat[4 * i + 2] = u.z; nat[4 * i + 3] = u.w;
         }
-      }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        constexpr int d = pair_dist<BITS>();
-        const int lo = pair_lo<BITS>(i), hi = lo + d;
-        const uint32_t sel = ((lo & 1) ? 0x32u : 0x10u) | (((hi & 1) ? 0x76u : 0x54u) << 8);
-        xv[nt][i] = (d == 1) ? nat[i] : prmt(nat[lo >> 1], nat[hi >> 1], sel);
+        for (int i = 0; i < 16; ++i) {
+          constexpr int d = pair_dist<BITS>();
+          const int lo = pair_lo<BITS>(i), hi = lo + d;
+          const uint32_t sel = ((lo & 1) ? 0x32u : 0x10u) | (((hi & 1) ? 0x76u : 0x54u) << 8);
+          xv[nt][i] = (d == 1) ? nat[i] : prmt(nat[lo >> 1], nat[hi >> 1], sel);
+        }
       }
     }
   };
+  uint32_t xv[NT][16];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) xv[nt][i] = 0u;
 
   // Two accumulator sets (even and odd MMA steps) keep the MMA chain short.
   float acc[2][NT][4];
@@ -512,10 +534,11 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
 
   constexpr int kRowBytes = 16 * BITS;  // one row of a chunk box
   bool ok = true;
-  for (int c = warp; ok && c < nchunks; c += tma_warps<NT>()) {
-    uint16_t cur[4] = {sv[0], sv[1], sv[2], sv[3]};
-    if (c + tma_warps<NT>() < nchunks) load_sb(c + tma_warps<NT>(), sv);
-    uint32_t xv[NT][16];
+#pragma unroll
+  for (int j = 0; j < kTmaMaxChunksPerWarp; ++j) {
+    const int c = warp + j * kW;
+    if (!ok || c >= nchunks) break;
+    const uint16_t *cur = sv[j];
     load_x(c, xv);
     uint32_t spins = 0;
     while (!mbar_try_wait(&bars[c], 0)) {
@@ -644,8 +667,11 @@ cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, cudaStream_t stream) {
   // Split K over a cluster only when the weight has too few 16-row tiles to
   // give every SM work, or one block's share would not fit.
   int C = 1;
-  while (C < 8 && kr_of(2 * C) >= 128 && (tiles * C < 240 || smem_of(C) > 100 * 1024)) C *= 2;
-  if (smem_of(C) > 200 * 1024) return cudaErrorNotSupported;
+  const int max_kr = 128 * kTmaMaxChunksPerWarp * tma_warps<NT>();
+  while (C < 8 && kr_of(2 * C) >= 128 &&
+         (tiles * C < 240 || smem_of(C) > 100 * 1024 || kr_of(C) > max_kr))
+    C *= 2;
+  if (smem_of(C) > 200 * 1024 || kr_of(C) > max_kr) return cudaErrorNotSupported;
   TmaLayout L;
   L.kr = kr_of(C);
   L.box_bytes = box_bytes;
