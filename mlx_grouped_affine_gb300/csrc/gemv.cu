@@ -315,68 +315,105 @@ gemv_n_kernel(GemvArgs a) {
 // ------------------------------------------------------------------------
 // Shared by the transposed decode kernels.
 //
-// Code pairs.  For 1 and 2 bits a word holds 32/bits codes, and codes j and
-// j + 16/bits sit exactly 16 bits apart: one shift and one LOP3
-// ((w >> j*bits) & mask16x2 | 128.0x2) make the bf16x2 pair (128 + c_j,
-// 128 + c_{j+16/bits}); subtracting 128 is exact, then one bf16x2 FMA gives
-// RN(s*c + b) for both.  Such pairs need x in the same order, which costs a
-// permute per x word.  For 4 bits the natural pair (codes 2i, 2i+1: the two
-// nibbles of byte i) is as cheap -- one byte permute against w >> 4 and one
-// LOP3 -- so 4-bit codes and everything wider are paired naturally and x is
-// used as it lies.  8-bit codes (above 127) go through fp32.
+// Code pairs.  Every width is paired naturally: pair p of a lane's 32 codes
+// is (2p, 2p+1), so x is used as it lies.  Each pair becomes one bf16x2
+// register, each half RN(s*c + b), in one of two forms.
+//
+// Fast form.  A bf16 bit pattern P <= 0xFF has the value P * 2^-133 exactly:
+// below 0x80 it is a subnormal, above it the exponent field is 1 and its
+// implicit leading one is worth exactly bit 7 of P.  So a code c sitting at
+// bit o (o + bits <= 8) of an otherwise clear 16-bit half reads as
+// c * 2^(o-133), and one bf16x2 FMA against the multiplier s * 2^(133-o)
+// with addend b yields RN(s*c + b): the product is exactly s*c and the FMA
+// rounds once.  The multiplier is s with 133 - o added to its exponent
+// field, which is exact while the exponent stays below 255; the fast form is
+// used when every scale of the warp's chunk is a normal number below 2^-5.
+// Per pair this costs one byte permute (the pair's byte, or two bytes at
+// 8 bits, into both halves), one mask (none at 8 bits) and the FMA.
+//
+// Exact form, for any scale: the code OR-ed into the mantissa of 128.0 gives
+// bf16 (128 + c), 128 is subtracted exactly, then the same FMA; 8-bit codes
+// go through fp32.
 //
 // Warps take 128-code chunks in turn; lane (g, t) handles codes
 // [32t, 32t+32) of rows g and g+8, i.e. 16 pairs per row, and MMA r
 // contracts pairs 2r and 2r+1 with the two x words at the same positions.
 
-// The lane's 32 codes as 16 pairs: pair i is codes (pair_lo(i),
-// pair_lo(i) + pair_dist) of the 32.
+// Multiplier slots of the fast form: slot k serves the pairs whose codes sit
+// at bit offsets (fast_lo(k), fast_hi(k)) of their halves.
 template <int BITS>
-__host__ __device__ constexpr int pair_dist() {
-  return BITS == 1 ? 16 : BITS == 2 ? 8 : 1;
+__host__ __device__ constexpr int fast_slots() {
+  return BITS == 1 ? 4 : BITS == 2 ? 2 : 1;
 }
 template <int BITS>
-__host__ __device__ constexpr int pair_lo(int i) {
-  return BITS == 1 ? i : BITS == 2 ? (i / 8) * 16 + i % 8 : 2 * i;
+__host__ __device__ constexpr int fast_lo(int k) {
+  return BITS == 1 ? 2 * k : BITS == 2 ? 4 * k : 0;
+}
+template <int BITS>
+__host__ __device__ constexpr int fast_hi(int k) {
+  return BITS == 1 ? 2 * k + 1 : BITS == 2 ? 4 * k + 2 : BITS == 4 ? 4 : 0;
 }
 
-// Pairs 2r and 2r+1 of a lane's 32 codes held in v[] (BITS words).
+// Whether the bf16 scale h is a normal number of magnitude below 2^-5.
+__device__ __forceinline__ bool fast_scale(uint32_t h) {
+  return ((h >> 7) & 0xFFu) - 1u < 121u;
+}
+
+// (s * 2^(133 - lo), s * 2^(133 - hi)) for every slot, from the scale bits h.
 template <int BITS>
-__device__ __forceinline__ void dequant_mma_pairs(const uint32_t *v, int r, uint32_t s2, uint32_t b2,
-                                                  float sf, float bf, uint32_t &p0, uint32_t &p1) {
-  if constexpr (BITS == 1 || BITS == 2) {
-    constexpr int per_word = 16 / BITS;  // pairs per word
-    constexpr uint32_t mask = ((1u << BITS) - 1u) * 0x00010001u;
-    const int i0 = 2 * r, i1 = 2 * r + 1;
-    const uint32_t w0 = v[i0 / per_word], w1 = v[i1 / per_word];
-    const uint32_t q0 = and_or(w0 >> ((i0 % per_word) * BITS), mask, kMagic);
-    const uint32_t q1 = and_or(w1 >> ((i1 % per_word) * BITS), mask, kMagic);
-    p0 = bf16x2_fma(bf16x2_sub(q0, kMagic), s2, b2);
-    p1 = bf16x2_fma(bf16x2_sub(q1, kMagic), s2, b2);
+__device__ __forceinline__ void fast_muls(uint32_t h, uint32_t (&m)[fast_slots<BITS>()]) {
+#pragma unroll
+  for (int k = 0; k < fast_slots<BITS>(); ++k)
+    m[k] = h * 0x00010001u + ((static_cast<uint32_t>(133 - fast_lo<BITS>(k)) << 7) |
+                              (static_cast<uint32_t>(133 - fast_hi<BITS>(k)) << 23));
+}
+
+template <int BITS>
+__device__ __forceinline__ uint32_t pair_fast(const uint32_t *v, int p,
+                                              const uint32_t (&m)[fast_slots<BITS>()],
+                                              uint32_t b2) {
+  if constexpr (BITS == 8) {
+    // bytes 2i, 2i+1 of word p/2 into the low bytes of the halves
+    const uint32_t i = p & 1;
+    return bf16x2_fma(prmt(v[p >> 1], 0u, 0x4040u | (2 * i) | ((2 * i + 1) << 8)), m[0], b2);
   } else if constexpr (BITS == 4) {
-    // codes 4r .. 4r+3 are bytes 2(r%2), 2(r%2)+1 of word r/2 (low nibble
-    // first); byte j of w and of w >> 4 hold codes 2j and 2j+1 in their low
-    // nibbles.
-    const uint32_t w = v[r >> 1], w4 = w >> 4;
-    const uint32_t j0 = 2u * (r & 1), j1 = j0 + 1;
-    const uint32_t q0 = and_or(prmt(w, w4, 0x0400u | (j0 << 8) | j0), 0x000F000Fu, kMagic);
-    const uint32_t q1 = and_or(prmt(w, w4, 0x0400u | (j1 << 8) | j1), 0x000F000Fu, kMagic);
-    p0 = bf16x2_fma(bf16x2_sub(q0, kMagic), s2, b2);
-    p1 = bf16x2_fma(bf16x2_sub(q1, kMagic), s2, b2);
-  } else if constexpr (BITS == 8) {
-    // word r holds codes 4r .. 4r+3, one per byte
-    const uint32_t w = v[r];
-    const float c0 = __uint_as_float(prmt(w, 0x4B000000u, 0x7650u)) - 8388608.0f;
-    const float c1 = __uint_as_float(prmt(w, 0x4B000000u, 0x7651u)) - 8388608.0f;
-    const float c2 = __uint_as_float(prmt(w, 0x4B000000u, 0x7652u)) - 8388608.0f;
-    const float c3 = __uint_as_float(prmt(w, 0x4B000000u, 0x7653u)) - 8388608.0f;
-    p0 = pack_bf16x2(__fmaf_rn(sf, c0, bf), __fmaf_rn(sf, c1, bf));
-    p1 = pack_bf16x2(__fmaf_rn(sf, c2, bf), __fmaf_rn(sf, c3, bf));
+    // byte j of word p/4 holds the pair as its two nibbles
+    const uint32_t j = p & 3;
+    const uint32_t t = prmt(v[p >> 2], 0u, 0x4040u | j | (j << 8)) & 0x00F0000Fu;
+    return bf16x2_fma(t, m[0], b2);
+  } else if constexpr (BITS == 2) {
+    // byte j of word p/8 holds pairs 2j, 2j+1 of the word at bits 0..3, 4..7
+    const uint32_t j = (p >> 1) & 3, k = p & 1;
+    const uint32_t t = prmt(v[p >> 3], 0u, 0x4040u | j | (j << 8)) & (0x000C0003u << (4 * k));
+    return bf16x2_fma(t, m[k], b2);
+  } else if constexpr (BITS == 1) {
+    // byte j of word p/16 holds pairs 4j .. 4j+3 of the word at bits 2k, 2k+1
+    const uint32_t j = (p >> 2) & 3, k = p & 3;
+    const uint32_t t = prmt(v[p >> 4], 0u, 0x4040u | j | (j << 8)) & (0x00020001u << (2 * k));
+    return bf16x2_fma(t, m[k], b2);
   } else {
-    const uint32_t q0 = code_at<BITS>(v, 4 * r) | (code_at<BITS>(v, 4 * r + 1) << 16) | kMagic;
-    const uint32_t q1 = code_at<BITS>(v, 4 * r + 2) | (code_at<BITS>(v, 4 * r + 3) << 16) | kMagic;
-    p0 = bf16x2_fma(bf16x2_sub(q0, kMagic), s2, b2);
-    p1 = bf16x2_fma(bf16x2_sub(q1, kMagic), s2, b2);
+    const uint32_t t = code_at<BITS>(v, 2 * p) | (code_at<BITS>(v, 2 * p + 1) << 16);
+    return bf16x2_fma(t, m[0], b2);
+  }
+}
+
+template <int BITS>
+__device__ __forceinline__ uint32_t pair_exact(const uint32_t *v, int p, uint32_t s2, uint32_t b2,
+                                               float sf, float bf) {
+  if constexpr (BITS == 8) {
+    // fp32 2^23 + byte, exact; minus 2^23 gives the code exactly.
+    const uint32_t w = v[p >> 1], i = p & 1;
+    const float c0 = __uint_as_float(prmt(w, 0x4B000000u, 0x7650u | (2 * i))) - 8388608.0f;
+    const float c1 = __uint_as_float(prmt(w, 0x4B000000u, 0x7650u | (2 * i + 1))) - 8388608.0f;
+    return pack_bf16x2(__fmaf_rn(sf, c0, bf), __fmaf_rn(sf, c1, bf));
+  } else if constexpr (BITS == 4) {
+    // byte j of w and of w >> 4 hold codes 2j and 2j+1 in their low nibbles
+    const uint32_t w = v[p >> 2], j = p & 3;
+    const uint32_t q = and_or(prmt(w, w >> 4, 0x0400u | j | (j << 8)), 0x000F000Fu, kMagic);
+    return bf16x2_fma(bf16x2_sub(q, kMagic), s2, b2);
+  } else {
+    const uint32_t q = code_at<BITS>(v, 2 * p) | (code_at<BITS>(v, 2 * p + 1) << 16) | kMagic;
+    return bf16x2_fma(bf16x2_sub(q, kMagic), s2, b2);
   }
 }
 
@@ -411,8 +448,8 @@ __device__ __forceinline__ void lds_words(const uint8_t *p, uint32_t *v) {
 // after it.  A box lands densely (row pitch 16*BITS bytes), which keeps the
 // reads of lanes (g, t) in distinct banks for every width but 8 bits; 8-bit
 // boxes use the 128-byte swizzle (16-byte unit q of row r at q ^ (r % 8)).
-// Everything else is as in the kernel above: copies before
-// griddepcontrol.wait, x staged in pair order after it, 8 MMAs per chunk.
+// The weight copies and the scale/bias loads come before griddepcontrol.wait;
+// x, which the previous kernel may write, is read after it; 8 MMAs per chunk.
 
 struct TmaLayout {
   int kr;           // codes per block (multiple of 128)
@@ -490,8 +527,8 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
   }
 
   // x may be written by the previous kernel in the stream.  Each lane reads
-  // its own 32 x values per chunk (L2-resident: every block reads the same x)
-  // and puts them in the pair order of its weights.
+  // its own 32 x values per chunk (L2-resident: every block reads the same x),
+  // natural pairs like the weights.
   griddep_wait();
   // Lanes whose x row is beyond M keep zero fragments throughout.
   auto load_x = [&](int c, uint32_t (&xv)[NT][16]) {
@@ -501,18 +538,10 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
       if (m < a.M) {
         const uint4 *xp = reinterpret_cast<const uint4 *>(
             a.x + static_cast<int64_t>(m) * a.K + k0 + (c << 7) + 32 * t);
-        uint32_t nat[16];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint4 u = __ldg(xp + i);
-          nat[4 * i] = u.x; nat[4 * i + 1] = u.y; nat[4 * i + 2] = u.z; nat[4 * i + 3] = u.w;
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          constexpr int d = pair_dist<BITS>();
-          const int lo = pair_lo<BITS>(i), hi = lo + d;
-          const uint32_t sel = ((lo & 1) ? 0x32u : 0x10u) | (((hi & 1) ? 0x76u : 0x54u) << 8);
-          xv[nt][i] = (d == 1) ? nat[i] : prmt(nat[lo >> 1], nat[hi >> 1], sel);
+          xv[nt][4 * i] = u.x; xv[nt][4 * i + 1] = u.y; xv[nt][4 * i + 2] = u.z; xv[nt][4 * i + 3] = u.w;
         }
       }
     }
@@ -564,18 +593,33 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
       lds_words<BITS>(box + g * kRowBytes + t * 4 * BITS, v0);
       lds_words<BITS>(box + (g + 8) * kRowBytes + t * 4 * BITS, v1);
     }
-    const uint32_t s0 = bcast_bf16x2(cur[0]), b0 = bcast_bf16x2(cur[1]);
-    const uint32_t s1 = bcast_bf16x2(cur[2]), b1 = bcast_bf16x2(cur[3]);
-    const float fs0 = bf16_bits_to_f32(cur[0]), fb0 = bf16_bits_to_f32(cur[1]);
-    const float fs1 = bf16_bits_to_f32(cur[2]), fb1 = bf16_bits_to_f32(cur[3]);
+    const uint32_t b0 = bcast_bf16x2(cur[1]), b1 = bcast_bf16x2(cur[3]);
+    if (__all_sync(0xffffffffu, fast_scale(cur[0]) && fast_scale(cur[2]))) {
+      uint32_t m0[fast_slots<BITS>()], m1[fast_slots<BITS>()];
+      fast_muls<BITS>(cur[0], m0);
+      fast_muls<BITS>(cur[2], m1);
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      uint32_t a0, a2, a1, a3;
-      dequant_mma_pairs<BITS>(v0, r, s0, b0, fs0, fb0, a0, a2);
-      dequant_mma_pairs<BITS>(v1, r, s1, b1, fs1, fb1, a1, a3);
+      for (int r = 0; r < 8; ++r) {
+        const uint32_t a0 = pair_fast<BITS>(v0, 2 * r, m0, b0), a2 = pair_fast<BITS>(v0, 2 * r + 1, m0, b0);
+        const uint32_t a1 = pair_fast<BITS>(v1, 2 * r, m1, b1), a3 = pair_fast<BITS>(v1, 2 * r + 1, m1, b1);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-        mma_bf16_16816(acc[r & 1][nt], a0, a1, a2, a3, xv[nt][2 * r], xv[nt][2 * r + 1]);
+        for (int nt = 0; nt < NT; ++nt)
+          mma_bf16_16816(acc[r & 1][nt], a0, a1, a2, a3, xv[nt][2 * r], xv[nt][2 * r + 1]);
+      }
+    } else {
+      const uint32_t s0 = bcast_bf16x2(cur[0]), s1 = bcast_bf16x2(cur[2]);
+      const float fs0 = bf16_bits_to_f32(cur[0]), fb0 = bf16_bits_to_f32(cur[1]);
+      const float fs1 = bf16_bits_to_f32(cur[2]), fb1 = bf16_bits_to_f32(cur[3]);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const uint32_t a0 = pair_exact<BITS>(v0, 2 * r, s0, b0, fs0, fb0);
+        const uint32_t a2 = pair_exact<BITS>(v0, 2 * r + 1, s0, b0, fs0, fb0);
+        const uint32_t a1 = pair_exact<BITS>(v1, 2 * r, s1, b1, fs1, fb1);
+        const uint32_t a3 = pair_exact<BITS>(v1, 2 * r + 1, s1, b1, fs1, fb1);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          mma_bf16_16816(acc[r & 1][nt], a0, a1, a2, a3, xv[nt][2 * r], xv[nt][2 * r + 1]);
+      }
     }
   }
 
