@@ -47,6 +47,18 @@ def test_transposed_all_widths(bits, gs, M):
     check(x, M, w, N, K, True, what="bits=%d gs=%d M=%d" % (bits, gs, M))
 
 
+@pytest.mark.parametrize("bits", ALL_BITS)
+@pytest.mark.parametrize("M", (1, 8, 16))
+def test_transposed_many_tiles_ragged(bits, M):
+    # N = 3000: 188 tiles of 16 rows, more than a GB300 has SMs and fewer than
+    # two per SM; the last tile is ragged.  K = 640 = five chunks, fewer than
+    # a block has warps.
+    N, K = 3000, 640
+    w = synth.quant_weight(300 + bits, N, K, bits, 64)
+    x = synth.x_bf16(301 + M, M, K)
+    check(x, M, w, N, K, True, qmm.QMM_F32, "many tiles bits=%d M=%d" % (bits, M))
+
+
 @pytest.mark.parametrize("bits", (3, 4, 8))
 def test_transposed_partial_chunk(bits):
     # K = 608 = 4 full 128-code chunks and 96 codes.
