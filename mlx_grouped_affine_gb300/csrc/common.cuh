@@ -159,6 +159,96 @@ __device__ __forceinline__ void dequant_pairs(const uint32_t *v, uint32_t s2, ui
   }
 }
 
+// Natural code pairs of a run of 32 codes held in v[] (bits words), pair p =
+// codes (2p, 2p+1), each half RN(scale * code + bias), in two forms.
+//
+// Fast form: a bf16 bit pattern P <= 0xFF is worth exactly P * 2^-133
+// (subnormal below 0x80; exponent field 1 above, whose implicit one is bit 7
+// of P).  A code c at bit o (o + bits <= 8) of an otherwise clear half reads
+// as c * 2^(o-133), so one bf16x2 FMA with the multiplier s * 2^(133-o) and
+// addend b gives RN(s*c + b): the product is exact and the FMA rounds once.
+// The multiplier is s with 133 - o added to its exponent field, exact while
+// that stays below 255: taken when the scale is a normal number below 2^-5.
+// Exact form, for any scale: the code OR-ed into the mantissa of 128.0,
+// minus 128 exactly, then the FMA; 8-bit codes through fp32.
+// Multiplier slots of the fast form: slot k serves the pairs whose codes sit
+// at bit offsets (fast_lo(k), fast_hi(k)) of their halves.
+template <int BITS>
+__host__ __device__ constexpr int fast_slots() {
+  return BITS == 1 ? 4 : BITS == 2 ? 2 : 1;
+}
+template <int BITS>
+__host__ __device__ constexpr int fast_lo(int k) {
+  return BITS == 1 ? 2 * k : BITS == 2 ? 4 * k : 0;
+}
+template <int BITS>
+__host__ __device__ constexpr int fast_hi(int k) {
+  return BITS == 1 ? 2 * k + 1 : BITS == 2 ? 4 * k + 2 : BITS == 4 ? 4 : 0;
+}
+
+// Whether the bf16 scale h is a normal number of magnitude below 2^-5.
+__device__ __forceinline__ bool fast_scale(uint32_t h) {
+  return ((h >> 7) & 0xFFu) - 1u < 121u;
+}
+
+// (s * 2^(133 - lo), s * 2^(133 - hi)) for every slot, from the scale bits h.
+template <int BITS>
+__device__ __forceinline__ void fast_muls(uint32_t h, uint32_t (&m)[fast_slots<BITS>()]) {
+#pragma unroll
+  for (int k = 0; k < fast_slots<BITS>(); ++k)
+    m[k] = h * 0x00010001u + ((static_cast<uint32_t>(133 - fast_lo<BITS>(k)) << 7) |
+                              (static_cast<uint32_t>(133 - fast_hi<BITS>(k)) << 23));
+}
+
+template <int BITS>
+__device__ __forceinline__ uint32_t pair_fast(const uint32_t *v, int p,
+                                              const uint32_t (&m)[fast_slots<BITS>()],
+                                              uint32_t b2) {
+  if constexpr (BITS == 8) {
+    // bytes 2i, 2i+1 of word p/2 into the low bytes of the halves
+    const uint32_t i = p & 1;
+    return bf16x2_fma(prmt(v[p >> 1], 0u, 0x4040u | (2 * i) | ((2 * i + 1) << 8)), m[0], b2);
+  } else if constexpr (BITS == 4) {
+    // byte j of word p/4 holds the pair as its two nibbles
+    const uint32_t j = p & 3;
+    const uint32_t t = prmt(v[p >> 2], 0u, 0x4040u | j | (j << 8)) & 0x00F0000Fu;
+    return bf16x2_fma(t, m[0], b2);
+  } else if constexpr (BITS == 2) {
+    // byte j of word p/8 holds pairs 2j, 2j+1 of the word at bits 0..3, 4..7
+    const uint32_t j = (p >> 1) & 3, k = p & 1;
+    const uint32_t t = prmt(v[p >> 3], 0u, 0x4040u | j | (j << 8)) & (0x000C0003u << (4 * k));
+    return bf16x2_fma(t, m[k], b2);
+  } else if constexpr (BITS == 1) {
+    // byte j of word p/16 holds pairs 4j .. 4j+3 of the word at bits 2k, 2k+1
+    const uint32_t j = (p >> 2) & 3, k = p & 3;
+    const uint32_t t = prmt(v[p >> 4], 0u, 0x4040u | j | (j << 8)) & (0x00020001u << (2 * k));
+    return bf16x2_fma(t, m[k], b2);
+  } else {
+    const uint32_t t = code_at<BITS>(v, 2 * p) | (code_at<BITS>(v, 2 * p + 1) << 16);
+    return bf16x2_fma(t, m[0], b2);
+  }
+}
+
+template <int BITS>
+__device__ __forceinline__ uint32_t pair_exact(const uint32_t *v, int p, uint32_t s2, uint32_t b2,
+                                               float sf, float bf) {
+  if constexpr (BITS == 8) {
+    // fp32 2^23 + byte, exact; minus 2^23 gives the code exactly.
+    const uint32_t w = v[p >> 1], i = p & 1;
+    const float c0 = __uint_as_float(prmt(w, 0x4B000000u, 0x7650u | (2 * i))) - 8388608.0f;
+    const float c1 = __uint_as_float(prmt(w, 0x4B000000u, 0x7650u | (2 * i + 1))) - 8388608.0f;
+    return pack_bf16x2(__fmaf_rn(sf, c0, bf), __fmaf_rn(sf, c1, bf));
+  } else if constexpr (BITS == 4) {
+    // byte j of w and of w >> 4 hold codes 2j and 2j+1 in their low nibbles
+    const uint32_t w = v[p >> 2], j = p & 3;
+    const uint32_t q = and_or(prmt(w, w >> 4, 0x0400u | j | (j << 8)), 0x000F000Fu, kMagic);
+    return bf16x2_fma(bf16x2_sub(q, kMagic), s2, b2);
+  } else {
+    const uint32_t q = code_at<BITS>(v, 2 * p) | (code_at<BITS>(v, 2 * p + 1) << 16) | kMagic;
+    return bf16x2_fma(bf16x2_sub(q, kMagic), s2, b2);
+  }
+}
+
 // Load n words from p (4-byte aligned, and 8/16-byte aligned when the width
 // allows it) as wide as the alignment lets us.
 template <int BITS>

@@ -15,9 +15,10 @@
 //               D[2 x 128 x 256] fp32 in TMEM (all 512 columns)
 //   warps 2-5   epilogue: tcgen05.ld of the accumulators, convert, store y
 //   warps 6-21  dequantize: packed W -> bf16 (one rounding per weight,
-//               RN(scale * code + bias)) written in the same 128-byte swizzle
-//               the MMA descriptor expects, then fence.proxy.async and arrive;
-//               the packed codes of the next two stages are kept in flight
+//               RN(scale * code + bias)), 32 codes a thread per stage, written
+//               in the same 128-byte swizzle the MMA descriptor expects, then
+//               fence.proxy.async and arrive; the packed codes of the next two
+//               stages are kept in flight
 // Stage hand-off uses mbarriers; every wait is bounded, and a wait that runs
 // out sets the device error word, makes every role stop, and the block still
 // waits for its own copies and MMAs and frees its tensor memory.
@@ -44,9 +45,8 @@ constexpr int BN = 256;   // weight rows per tile (MMA N)
 constexpr int BK = 64;    // codes per stage: one 128-byte swizzle atom of bf16
 constexpr int STAGES = 3;
 constexpr int kEpiWarps = 4;
-constexpr int kDeqWarps = 16;
-constexpr int kRowsPerPass = kDeqWarps * 4;     // 8 chunk-threads per 64-code row
-constexpr int kChunks = BN / kRowsPerPass;      // 8-code chunks per thread per stage
+constexpr int kDeqWarps = 16;  // one 32-code item of a stage per thread
+static_assert(32 * kDeqWarps == BN * BK / 32, "one item per dequant thread");
 constexpr int kThreads = 32 * (2 + kEpiWarps + kDeqWarps);
 constexpr uint32_t A_BYTES = BM * BK * 2;
 constexpr uint32_t A_HALF = UM * BK * 2;
@@ -182,55 +182,71 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint32_t (&v)[
 
 // ---------------------------------------------------------------- roles ----
 
-// Dequant side: the 8-code chunk (k .. k+7) of weight row n.
+// Dequant side: 32 consecutive codes of one stored row (`bits` words) with
+// their group's scale and bias (s | b << 16).  32 codes never straddle a
+// group (group_size >= 32) and start on a word boundary.
 template <int BITS>
-struct ChunkLoad {
-  uint32_t win[2];
-  uint16_t s, b;
+struct ItemLoad {
+  uint32_t v[BITS];
+  uint32_t sb;
 };
 
-// The 8 codes starting at column `col` of stored row `row` (stored [N, K] when
-// TRANS, else [K, N]; codes and groups run along the stored columns).
+// The 32 codes from column `col` (a multiple of 32) of stored row `row`
+// (stored [N, K] when TRANS, else [K, N]; codes and groups run along the
+// stored columns).  Words past the end of the row read as zero.
 template <int BITS, bool TRANS>
-__device__ __forceinline__ void load_chunk(const GemmArgs &a, int row, int col, ChunkLoad<BITS> &c) {
+__device__ __forceinline__ void load_item(const GemmArgs &a, int row, int col, ItemLoad<BITS> &it) {
   const int rows = TRANS ? a.N : a.K, cols = TRANS ? a.K : a.N;
-  c.win[0] = c.win[1] = 0u;
-  c.s = c.b = 0;
+#pragma unroll
+  for (int i = 0; i < BITS; ++i) it.v[i] = 0u;
+  it.sb = 0u;
   if (row < rows && col < cols) {
     const int64_t wpr = (static_cast<int64_t>(cols) * BITS) >> 5;
-    const int cbit = col * BITS, cword = cbit >> 5, csh = cbit & 31;
-    const uint32_t *rp = a.w + static_cast<int64_t>(row) * wpr + cword;
-    const uint32_t lo = __ldg(rp);
-    const uint32_t hi = (csh + 8 * BITS > 32) ? __ldg(rp + 1) : 0u;
-    c.win[0] = csh ? __funnelshift_r(lo, hi, csh) : lo;
-    c.win[1] = csh ? (hi >> csh) : hi;
+    const int64_t w0 = static_cast<int64_t>(row) * wpr + (col >> 5) * BITS;
+    const uint32_t *rp = a.w + w0;
+    constexpr int kAlign = BITS % 4 == 0 ? 4 : BITS % 2 == 0 ? 2 : 1;  // words
+    if ((col >> 5) * BITS + BITS <= wpr && (w0 & (kAlign - 1)) == 0) {
+      load_words<BITS>(rp, it.v);
+    } else {
+      const int64_t left = wpr - (col >> 5) * BITS;
+#pragma unroll
+      for (int i = 0; i < BITS; ++i)
+        if (i < left) it.v[i] = __ldg(rp + i);
+    }
     const int64_t g = static_cast<int64_t>(row) * (cols >> a.group_shift) + (col >> a.group_shift);
-    c.s = __ldg(a.scales + g);
-    c.b = __ldg(a.biases + g);
+    it.sb = __ldg(a.scales + g) | (static_cast<uint32_t>(__ldg(a.biases + g)) << 16);
   }
 }
 
-// Shared-memory byte offset of the 16-byte chunk holding the 8 dequantized
-// weights a thread produces, and the (row, column) those 8 start at.
+// The item a dequant thread owns in a stage, and the shared-memory byte
+// offsets of its four 16-byte chunks (8 dequantized weights each).
 //  TRANS: the W tile is K-major (as the x tile): 256 weight rows of 128 bytes;
-//    thread chunk c (of 8 per 64-code row) of row r.
-//  !TRANS: the W tile is MN-major: 8 consecutive n of one k row per chunk.
-//    Swizzle atoms of 64 n x 8 k (1024 bytes) sit at ((n/64) * 8 + k/8) * 1024:
-//    8192 bytes between atoms along N, 1024 along K.
+//    thread (r, h) takes codes [32h, 32h+32) of the stage in row r, chunks
+//    4h .. 4h+3 of the row, at chunk position c ^ (r % 8).
+//  !TRANS: the W tile is MN-major: a chunk is 8 consecutive n of one k row.
+//    Swizzle atoms of 64 n x 8 k (1024 bytes) sit at ((n/64) * 8 + k/8) *
+//    1024; inside an atom, k row kw is at kw * 128 and n chunk j at position
+//    j ^ kw.  Thread (k row kr, segment q) takes n [32q, 32q+32), chunks
+//    4q .. 4q+3; the 8 lanes of a quarter warp take 8 consecutive k rows, so
+//    their stores land in 8 distinct bank groups.
 template <bool TRANS>
-__device__ __forceinline__ void chunk_place(int dt, int i, int tile_n0, int kb, int &row, int &col,
-                                            uint32_t &off) {
+__device__ __forceinline__ void item_place(int dt, int tile_n0, int kb, int &row, int &col,
+                                           uint32_t (&off)[4]) {
   if (TRANS) {
-    const int c = dt & 7, r = (dt >> 3) + kRowsPerPass * i;
+    const int r = dt >> 1, h = dt & 1;
     row = tile_n0 + r;
-    col = kb * BK + 8 * c;
-    off = r * 128 + ((c ^ (r & 7)) << 4);
+    col = kb * BK + 32 * h;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) off[j] = r * 128 + (((4 * h + j) ^ (r & 7)) << 4);
   } else {
-    const int j = dt & 31, kr = (dt >> 5) + (32 * kDeqWarps / 32) * i;  // k row in the stage
+    const int kr = (dt >> 6) * 8 + (dt & 7), q = (dt >> 3) & 7, kw = kr & 7;
     row = kb * BK + kr;
-    col = tile_n0 + 8 * j;
-    const int kw = kr & 7;
-    off = ((j >> 3) * 8 + (kr >> 3)) * 1024 + kw * 128 + (((j & 7) ^ kw) << 4);
+    col = tile_n0 + 32 * q;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int jn = 4 * q + j;
+      off[j] = ((jn >> 3) * 8 + (kr >> 3)) * 1024 + kw * 128 + (((jn & 7) ^ kw) << 4);
+    }
   }
 }
 
@@ -246,41 +262,53 @@ __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int
   auto advance = [&](int &t, int &k) {
     if (++k == nk) { k = 0; t += gridDim.x; }
   };
-  auto prefetch = [&](ChunkLoad<BITS> (&buf)[kChunks]) {
+  auto prefetch = [&](ItemLoad<BITS> &buf) {
     if (ptile >= num_tiles) return;
-    const int n0 = (ptile / a.m_tiles) * BN;
-#pragma unroll
-    for (int i = 0; i < kChunks; ++i) {
-      int row, col;
-      uint32_t off;
-      chunk_place<TRANS>(dt, i, n0, pkb, row, col, off);
-      load_chunk<BITS, TRANS>(a, row, col, buf[i]);
-    }
+    int row, col;
+    uint32_t off[4];
+    item_place<TRANS>(dt, (ptile / a.m_tiles) * BN, pkb, row, col, off);
+    load_item<BITS, TRANS>(a, row, col, buf);
     advance(ptile, pkb);
   };
-  ChunkLoad<BITS> buf0[kChunks], buf1[kChunks];
+  ItemLoad<BITS> buf0, buf1;
   prefetch(buf0);
   prefetch(buf1);
   int s = 0;
   uint32_t ph = 0;
+  uint32_t off[4];
+  {
+    int row, col;
+    item_place<TRANS>(dt, 0, 0, row, col, off);
+  }
   // One stage out of `buf`, which is then refilled; false when done or stopped.
-  auto step = [&](ChunkLoad<BITS> (&buf)[kChunks]) -> bool {
+  auto step = [&](ItemLoad<BITS> &buf) -> bool {
     if (tile >= num_tiles) return false;
-    ChunkLoad<BITS> cur[kChunks];
-#pragma unroll
-    for (int i = 0; i < kChunks; ++i) cur[i] = buf[i];
+    const ItemLoad<BITS> cur = buf;
     prefetch(buf);
     if (!wait_warp(&bars->empty[s], ph ^ 1u, abort, a.err)) return false;
     const uint32_t base = smem_u32(sB + s * B_BYTES);
+    const uint32_t hs = cur.sb & 0xFFFFu, hb = cur.sb >> 16;
+    const uint32_t b2 = hb * 0x00010001u;
+    if (__all_sync(0xffffffffu, fast_scale(hs))) {
+      uint32_t m[fast_slots<BITS>()];
+      fast_muls<BITS>(hs, m);
 #pragma unroll
-    for (int i = 0; i < kChunks; ++i) {
-      int row, col;
-      uint32_t off;
-      chunk_place<TRANS>(dt, i, 0, 0, row, col, off);
-      uint32_t v[4];
-      dequant_pairs<BITS, 4>(cur[i].win, bcast_bf16x2(cur[i].s), bcast_bf16x2(cur[i].b),
-                             bf16_bits_to_f32(cur[i].s), bf16_bits_to_f32(cur[i].b), v);
-      st_shared_v4(base + off, v);
+      for (int j = 0; j < 4; ++j) {
+        uint32_t v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = pair_fast<BITS>(cur.v, 4 * j + i, m, b2);
+        st_shared_v4(base + off[j], v);
+      }
+    } else {
+      const uint32_t s2 = hs * 0x00010001u;
+      const float sf = bf16_bits_to_f32(hs), bf = bf16_bits_to_f32(hb);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = pair_exact<BITS>(cur.v, 4 * j + i, s2, b2, sf, bf);
+        st_shared_v4(base + off[j], v);
+      }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_arrive(&bars->full_b[s]);
