@@ -43,9 +43,15 @@ constexpr int UM = 128;   // rows of one MMA (x rows)
 constexpr int BM = 2 * UM; // x rows per tile: two MMAs share each dequantized W tile
 constexpr int BN = 256;   // weight rows per tile (MMA N)
 constexpr int BK = 64;    // codes per stage: one 128-byte swizzle atom of bf16
-constexpr int STAGES = 3;
+// Separate rings for the x tiles and the dequantized W tiles.  Measured on
+// the 2048 x 14336 x 4096 case: the MMA waits mostly on W (the dequant warps
+// can only start a stage once the MMAs have freed its slot), so W gets the
+// deeper ring.
+constexpr int SA = 2;  // x stages
+constexpr int SB = 4;  // W stages
 constexpr int kEpiWarps = 4;
 constexpr int kDeqWarps = 16;  // one 32-code item of a stage per thread
+constexpr int kLoadAhead = 2;  // stages of packed codes in flight per dequant thread
 static_assert(32 * kDeqWarps == BN * BK / 32, "one item per dequant thread");
 constexpr int kThreads = 32 * (2 + kEpiWarps + kDeqWarps);
 constexpr uint32_t A_BYTES = BM * BK * 2;
@@ -55,13 +61,13 @@ constexpr uint32_t TMEM_COLS = 2 * BN;  // accumulators of the two x halves
 constexpr uint32_t kSpinLimit = 1u << 24;
 
 struct Barriers {
-  uint64_t full_a[STAGES], full_b[STAGES], empty[STAGES];
+  uint64_t full_a[SA], empty_a[SA], full_b[SB], empty_b[SB];
   uint64_t tmem_full, tmem_empty, mma_done;
   uint32_t tmem_base;
   int abort;
 };
 
-constexpr size_t kSmemBytes = STAGES * (A_BYTES + B_BYTES) + sizeof(Barriers) + 1024;
+constexpr size_t kSmemBytes = SA * A_BYTES + SB * B_BYTES + sizeof(Barriers) + 1024;
 
 struct GemmArgs {
   const uint32_t *w;
@@ -255,8 +261,8 @@ __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int
   const int dt = threadIdx.x - 32 * (2 + kEpiWarps);  // 0 .. 32 * kDeqWarps - 1
   const int num_tiles = a.m_tiles * a.n_tiles;
   volatile int *abort = &bars->abort;
-  // Stages are consumed in order (tile, kb); the codes of the next two stages
-  // are always in flight in two register buffers while one is dequantized.
+  // Stages are consumed in order (tile, kb); the codes of the next kLoadAhead
+  // stages are always in flight in register buffers while one is dequantized.
   int tile = blockIdx.x, kb = 0;    // next stage to dequantize
   int ptile = tile, pkb = 0;        // next stage to load
   auto advance = [&](int &t, int &k) {
@@ -270,9 +276,9 @@ __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int
     load_item<BITS, TRANS>(a, row, col, buf);
     advance(ptile, pkb);
   };
-  ItemLoad<BITS> buf0, buf1;
-  prefetch(buf0);
-  prefetch(buf1);
+  ItemLoad<BITS> buf[kLoadAhead];
+#pragma unroll
+  for (int i = 0; i < kLoadAhead; ++i) prefetch(buf[i]);
   int s = 0;
   uint32_t ph = 0;
   uint32_t off[4];
@@ -285,7 +291,7 @@ __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int
     if (tile >= num_tiles) return false;
     const ItemLoad<BITS> cur = buf;
     prefetch(buf);
-    if (!wait_warp(&bars->empty[s], ph ^ 1u, abort, a.err)) return false;
+    if (!wait_warp(&bars->empty_b[s], ph ^ 1u, abort, a.err)) return false;
     const uint32_t base = smem_u32(sB + s * B_BYTES);
     const uint32_t hs = cur.sb & 0xFFFFu, hb = cur.sb >> 16;
     const uint32_t b2 = hb * 0x00010001u;
@@ -310,13 +316,19 @@ __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int
         st_shared_v4(base + off[j], v);
       }
     }
+    // Each thread makes its stores visible to the tensor cores, then one
+    // arrival per warp.
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_arrive(&bars->full_b[s]);
-    if (++s == STAGES) { s = 0; ph ^= 1u; }
+    __syncwarp();
+    if ((dt & 31) == 0) mbar_arrive(&bars->full_b[s]);
+    if (++s == SB) { s = 0; ph ^= 1u; }
     advance(tile, kb);
     return true;
   };
-  while (step(buf0) && step(buf1)) {
+  for (bool more = true; more;) {
+#pragma unroll
+    for (int i = 0; i < kLoadAhead; ++i)
+      if (more) more = step(buf[i]);
   }
 }
 
@@ -329,25 +341,25 @@ __device__ void tma_role(const CUtensorMap *tmap, const GemmArgs &a, uint8_t *sA
   uint32_t ph = 0;
   // Parity of the last load issued into each stage that has not been seen to
   // land, so that a role that stops early can wait for its copies.
-  int pending[STAGES];
-  for (int i = 0; i < STAGES; ++i) pending[i] = -1;
+  int pending[SA];
+  for (int i = 0; i < SA; ++i) pending[i] = -1;
   bool ok = true;
   for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
     const int m0 = (tile % a.m_tiles) * BM;
     for (int kb = 0; kb < nk; ++kb) {
-      if (!wait_warp(&bars->empty[s], ph ^ 1u, abort, a.err)) { ok = false; break; }
+      if (!wait_warp(&bars->empty_a[s], ph ^ 1u, abort, a.err)) { ok = false; break; }
       if (lane == 0) {
         mbar_expect_tx(&bars->full_a[s], A_BYTES);
         tma_load_2d(smem_u32(sA + s * A_BYTES), tmap, kb * BK, m0, &bars->full_a[s]);
       }
       __syncwarp();
       pending[s] = static_cast<int>(ph);
-      if (++s == STAGES) { s = 0; ph ^= 1u; }
+      if (++s == SA) { s = 0; ph ^= 1u; }
     }
   }
   if (!ok) {
     // Stopped early: wait (bounded) for the copies still in flight.
-    for (int i = 0; i < STAGES; ++i) {
+    for (int i = 0; i < SA; ++i) {
       if (pending[i] < 0) continue;
       for (uint32_t spin = 0; spin < kSpinLimit; ++spin)
         if (__all_sync(0xffffffffu, mbar_try_wait(&bars->full_a[i], pending[i]))) break;
@@ -365,8 +377,8 @@ __device__ void mma_role(const GemmArgs &a, uint8_t *sA, uint8_t *sB, Barriers *
   const int lane = threadIdx.x & 31;
   const int num_tiles = a.m_tiles * a.n_tiles;
   volatile int *abort = &bars->abort;
-  int s = 0, it = 0;
-  uint32_t ph = 0;
+  int sa = 0, sb = 0, it = 0;
+  uint32_t pha = 0, phb = 0;
   bool ok = true;
   for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++it) {
     // The epilogue must have drained the accumulators of the previous tile.
@@ -375,16 +387,16 @@ __device__ void mma_role(const GemmArgs &a, uint8_t *sA, uint8_t *sB, Barriers *
     // The second 128-row half only when this tile has x rows there.
     const bool two = (tile % a.m_tiles) * BM + UM < a.M;
     for (int kb = 0; kb < nk; ++kb) {
-      if (!wait_warp(&bars->full_a[s], ph, abort, a.err) ||
-          !wait_warp(&bars->full_b[s], ph, abort, a.err)) {
+      if (!wait_warp(&bars->full_a[sa], pha, abort, a.err) ||
+          !wait_warp(&bars->full_b[sb], phb, abort, a.err)) {
         ok = false;
         break;
       }
       tc_fence_after();
       if (lane == 0) {
-        const uint64_t da0 = sw128_kmajor_desc(smem_u32(sA + s * A_BYTES));
-        const uint64_t da1 = sw128_kmajor_desc(smem_u32(sA + s * A_BYTES + A_HALF));
-        const uint32_t bs = smem_u32(sB + s * B_BYTES);
+        const uint64_t da0 = sw128_kmajor_desc(smem_u32(sA + sa * A_BYTES));
+        const uint64_t da1 = sw128_kmajor_desc(smem_u32(sA + sa * A_BYTES + A_HALF));
+        const uint32_t bs = smem_u32(sB + sb * B_BYTES);
         const uint64_t db = TRANS ? sw128_kmajor_desc(bs) : sw128_mnmajor_desc(bs);
 #pragma unroll
         for (int j = 0; j < BK / 16; ++j) {
@@ -392,10 +404,12 @@ __device__ void mma_role(const GemmArgs &a, uint8_t *sA, uint8_t *sB, Barriers *
           umma<idesc>(tmem, da0 + 2 * j, db + b_step * j, accumulate);
           if (two) umma<idesc>(tmem + BN, da1 + 2 * j, db + b_step * j, accumulate);
         }
-        umma_commit(&bars->empty[s]);
+        umma_commit(&bars->empty_a[sa]);
+        umma_commit(&bars->empty_b[sb]);
       }
       __syncwarp();
-      if (++s == STAGES) { s = 0; ph ^= 1u; }
+      if (++sa == SA) { sa = 0; pha ^= 1u; }
+      if (++sb == SB) { sb = 0; phb ^= 1u; }
     }
     if (!ok) break;
     if (lane == 0) umma_commit(&bars->tmem_full);
@@ -474,15 +488,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, GemmArgs a) {
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;
-  uint8_t *sB = smem + STAGES * A_BYTES;
-  Barriers *bars = reinterpret_cast<Barriers *>(sB + STAGES * B_BYTES);
+  uint8_t *sB = smem + SA * A_BYTES;
+  Barriers *bars = reinterpret_cast<Barriers *>(sB + SB * B_BYTES);
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
+    for (int i = 0; i < SA; ++i) {
       mbar_init(&bars->full_a[i], 1);
-      mbar_init(&bars->full_b[i], 32 * kDeqWarps);
-      mbar_init(&bars->empty[i], 1);
+      mbar_init(&bars->empty_a[i], 1);
+    }
+    for (int i = 0; i < SB; ++i) {
+      mbar_init(&bars->full_b[i], kDeqWarps);
+      mbar_init(&bars->empty_b[i], 1);
     }
     mbar_init(&bars->tmem_full, 1);
     mbar_init(&bars->tmem_empty, 32 * kEpiWarps);
