@@ -221,13 +221,22 @@ def measured_traffic():
     or None if the kernel source changed since it was taken."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "decode_gemv_traffic.json")
-    src = os.path.join(ROOT, "mlx_grouped_affine_gb300", "csrc", "gemv.cu")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    return d.get("dram_bytes_per_launch") if d.get("gemv_cu_sha256") == sha else None
+    return d.get("dram_bytes_per_launch") if d.get("sources_sha256") == decode_sources_sha() else None
+
+
+def decode_sources_sha():
+    """sha256 over the decode kernel's sources (the kernel file, then the
+    device helpers it includes)."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("gemv.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "mlx_grouped_affine_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def time_graph(torch, graph, steps, warmup, barrier=None):
