@@ -216,6 +216,59 @@ def dequant_rows_detail(torch, qmm, synth, peaks, steps, warmup):
     return out
 
 
+def sweep_detail(torch, qmm, synth, peaks, warmup):
+    """The remaining workloads, one line each: odd widths at M=1, the prefill
+    GEMM with W stored [K, N], the layer-shape sweep (GB/s and TFLOP/s, both
+    against their measured peaks), and bf16 dequantize of each sweep weight."""
+    out = {}
+
+    def one(name, M, N, K, bits, group, transpose, seed):
+        c = Case(torch, qmm, synth, M, N, K, bits, group, transpose=transpose, seed=seed)
+        c.capture()
+        steps = 200 if M <= 16 else 30 if M <= 128 else 4
+        t = time_graph(torch, c.graph, steps, warmup) / c.R
+        gbs = c.bytes_per_launch() / (t * 1e-3) / 1e9
+        tf = c.flops_per_launch() / (t * 1e-3) / 1e12
+        out[name] = {"us": round(t * 1e3, 3), "GB/s": round(gbs, 1),
+                     "frac_hbm": round(gbs / peaks["hbm_gbs"], 3), "TFLOP/s": round(tf, 2),
+                     "frac_bf16": round(tf / peaks["bf16_tflops"], 4)}
+        del c
+        torch.cuda.empty_cache()
+
+    N, K = synth.ODD_SHAPE
+    for bits in synth.ODD_BITS:
+        for g in synth.ODD_GROUPS:
+            one("odd_b%d_g%d_%dx%d_M1" % (bits, g, N, K), 1, N, K, bits, g, True, 60 + bits + g)
+    p = synth.PREFILL
+    one("prefill_b4_M2048_w_stored_KxN", p["M"], p["N"], p["K"], 4, 64, False, 31)
+    for (N, K) in synth.SWEEP_SHAPES:
+        for bits in (4, 8):
+            for M in synth.SWEEP_M:
+                one("sweep_b%d_%dx%d_M%d" % (bits, N, K, M), M, N, K, bits, 64, True, 70 + M + bits)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(
+        {np.dtype(np.uint32): np.int32, np.dtype(np.uint16): np.int16}[a.dtype])).cuda()
+    for (N, K) in synth.SWEEP_SHAPES:
+        for bits in (4, 8):
+            w = synth.quant_weight(90 + bits, N, K, bits, 64)
+            R = 2
+            copies = [(dev(np.roll(w.packed, r, 0)), dev(np.roll(w.scales, r, 0)),
+                       dev(np.roll(w.biases, r, 0))) for r in range(R)]
+            o = torch.empty((R, N, K), dtype=torch.int16, device="cuda")
+
+            def fn():
+                for r in range(R):
+                    pw, ps, pb = copies[r]
+                    qmm.qmm_dequantize(pw, ps, pb, N, K, 64, bits, o[r], qmm.QMM_BF16)
+            t = time_graph(torch, graph_of(torch, fn), 20, warmup) / R
+            nbytes = w.nbytes + 2 * N * K
+            out["sweep_dequantize_b%d_%dx%d_bf16" % (bits, N, K)] = {
+                "us": round(t * 1e3, 2), "GB/s": round(nbytes / (t * 1e-3) / 1e9, 1),
+                "frac_hbm": round(nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
+            del copies, o
+            torch.cuda.empty_cache()
+    return out
+
+
 def measured_traffic():
     """DRAM bytes per launch of the decode kernel from the committed ncu capture,
     or None if the kernel source changed since it was taken."""
@@ -346,6 +399,7 @@ def run_gpu(args):
                     "frac_hbm": round(c.bytes_per_launch() / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
                 del c
                 torch.cuda.empty_cache()
+        detail.update(sweep_detail(torch, qmm, synth, peaks, args.warmup))
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,

@@ -17,11 +17,14 @@
  *   - w = scale * code + bias.
  *
  * Conventions shared by every entry point:
- *   - Every pointer is a DEVICE pointer owned by the caller (the library
- *     allocates nothing on these paths and never frees caller memory, as
- *     spark_runtime's `MlxInt8Weight` leaves buffers to their owner).  Every
- *     pointer must be 16-byte aligned.  bf16 values are passed as their
- *     16-bit patterns (uint16_t).
+ *   - Every pointer is a DEVICE pointer owned by the caller (the library never
+ *     frees caller memory, as spark_runtime's `MlxInt8Weight` leaves buffers
+ *     to their owner).  Every pointer must be 16-byte aligned.  bf16 values
+ *     are passed as their 16-bit patterns (uint16_t).
+ *   - The only memory the library takes is the split-K workspace of
+ *     qmm_quantized_matmul (see there): stream-ordered, from the current
+ *     device's default memory pool, returned on the same stream by the same
+ *     call.  Every other path allocates nothing.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream) and run on the current CUDA device.  Results follow
  *     stream order.
@@ -97,6 +100,15 @@ qmm_status qmm_dequantize(const uint32_t *w, const uint16_t *scales,
  * multiple of group_size (K when transpose, N otherwise); M, N >= 0;
  * transpose in {0, 1}.  M <= 16 runs the decode kernel, larger M the
  * tensor-core (tcgen05) kernel.
+ *
+ * Split-K: when M > 16 gives fewer 256 x 256 output tiles than half the SMs,
+ * the K range of each tile is split over several blocks; their fp32 partials
+ * go to a workspace of splits * M * N * 4 bytes (never more than one tile
+ * per SM, about 40 MB on a GB300) and a second kernel adds them in a fixed
+ * order, so results repeat bit for bit.  The workspace comes from
+ * cudaMallocAsync on `stream` and goes back with cudaFreeAsync on `stream`
+ * (under stream capture, as graph allocation and free nodes).  If it cannot
+ * be had, the call runs without split-K.
  */
 qmm_status qmm_quantized_matmul(const uint16_t *x, int64_t M, const uint32_t *w,
                                 const uint16_t *scales, const uint16_t *biases,

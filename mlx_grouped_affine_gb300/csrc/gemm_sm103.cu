@@ -76,8 +76,26 @@ struct GemmArgs {
   int M, N, K;
   int group_shift;
   int m_tiles, n_tiles;
+  int splits;   // K ranges per output tile (split-K when > 1)
+  float *ws;    // split-K partials: slice s at ws + s * M * N, fp32 [M, N]
   unsigned *err;
 };
+
+// A unit of work: one output tile over one K range (k-blocks [kb0, kb1)).
+struct Unit {
+  int tile, split, kb0, kb1;
+};
+
+// (splits <= 32 and nk < 2^26 keep the products in 32 bits.)
+__device__ __forceinline__ Unit unit_of(const GemmArgs &a, int u, int nk) {
+  Unit r;
+  const unsigned sp = static_cast<unsigned>(a.splits);
+  r.tile = static_cast<int>(static_cast<unsigned>(u) / sp);
+  r.split = u - r.tile * a.splits;
+  r.kb0 = static_cast<int>(static_cast<unsigned>(r.split) * static_cast<unsigned>(nk) / sp);
+  r.kb1 = static_cast<int>(static_cast<unsigned>(r.split + 1) * static_cast<unsigned>(nk) / sp);
+  return r;
+}
 
 // ------------------------------------------------------------- PTX glue ----
 
@@ -259,22 +277,33 @@ __device__ __forceinline__ void item_place(int dt, int tile_n0, int kb, int &row
 template <int BITS, bool TRANS>
 __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int nk) {
   const int dt = threadIdx.x - 32 * (2 + kEpiWarps);  // 0 .. 32 * kDeqWarps - 1
-  const int num_tiles = a.m_tiles * a.n_tiles;
+  const int num_units = a.m_tiles * a.n_tiles * a.splits;
   volatile int *abort = &bars->abort;
-  // Stages are consumed in order (tile, kb); the codes of the next kLoadAhead
+  // Stages are consumed in order (unit, kb); the codes of the next kLoadAhead
   // stages are always in flight in register buffers while one is dequantized.
-  int tile = blockIdx.x, kb = 0;    // next stage to dequantize
-  int ptile = tile, pkb = 0;        // next stage to load
-  auto advance = [&](int &t, int &k) {
-    if (++k == nk) { k = 0; t += gridDim.x; }
+  // The unit being dequantized and the unit being loaded, each with its
+  // k-block; a unit's range is worked out once, when a thread moves to it.
+  int unit = blockIdx.x;
+  Unit cu = unit_of(a, unit < num_units ? unit : 0, nk);
+  int kb = cu.kb0;
+  int punit = unit, pkb = kb;
+  Unit pu = cu;
+  auto advance = [&](int &u, Unit &un, int &k) {
+    if (++k == un.kb1) {
+      u += gridDim.x;
+      if (u < num_units) {
+        un = unit_of(a, u, nk);
+        k = un.kb0;
+      }
+    }
   };
   auto prefetch = [&](ItemLoad<BITS> &buf) {
-    if (ptile >= num_tiles) return;
+    if (punit >= num_units) return;
     int row, col;
     uint32_t off[4];
-    item_place<TRANS>(dt, (ptile / a.m_tiles) * BN, pkb, row, col, off);
+    item_place<TRANS>(dt, (pu.tile / a.m_tiles) * BN, pkb, row, col, off);
     load_item<BITS, TRANS>(a, row, col, buf);
-    advance(ptile, pkb);
+    advance(punit, pu, pkb);
   };
   ItemLoad<BITS> buf[kLoadAhead];
 #pragma unroll
@@ -288,7 +317,7 @@ __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int
   }
   // One stage out of `buf`, which is then refilled; false when done or stopped.
   auto step = [&](ItemLoad<BITS> &buf) -> bool {
-    if (tile >= num_tiles) return false;
+    if (unit >= num_units) return false;
     const ItemLoad<BITS> cur = buf;
     prefetch(buf);
     if (!wait_warp(&bars->empty_b[s], ph ^ 1u, abort, a.err)) return false;
@@ -322,7 +351,7 @@ __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int
     __syncwarp();
     if ((dt & 31) == 0) mbar_arrive(&bars->full_b[s]);
     if (++s == SB) { s = 0; ph ^= 1u; }
-    advance(tile, kb);
+    advance(unit, cu, kb);
     return true;
   };
   for (bool more = true; more;) {
@@ -335,7 +364,7 @@ __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int
 __device__ void tma_role(const CUtensorMap *tmap, const GemmArgs &a, uint8_t *sA, Barriers *bars,
                          int nk) {
   const int lane = threadIdx.x & 31;
-  const int num_tiles = a.m_tiles * a.n_tiles;
+  const int num_units = a.m_tiles * a.n_tiles * a.splits;
   volatile int *abort = &bars->abort;
   int s = 0;
   uint32_t ph = 0;
@@ -344,9 +373,10 @@ __device__ void tma_role(const CUtensorMap *tmap, const GemmArgs &a, uint8_t *sA
   int pending[SA];
   for (int i = 0; i < SA; ++i) pending[i] = -1;
   bool ok = true;
-  for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-    const int m0 = (tile % a.m_tiles) * BM;
-    for (int kb = 0; kb < nk; ++kb) {
+  for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+    const Unit un = unit_of(a, u, nk);
+    const int m0 = (un.tile % a.m_tiles) * BM;
+    for (int kb = un.kb0; kb < un.kb1; ++kb) {
       if (!wait_warp(&bars->empty_a[s], ph ^ 1u, abort, a.err)) { ok = false; break; }
       if (lane == 0) {
         mbar_expect_tx(&bars->full_a[s], A_BYTES);
@@ -375,18 +405,19 @@ __device__ void mma_role(const GemmArgs &a, uint8_t *sA, uint8_t *sB, Barriers *
   // two 8-row K atoms (2048 bytes) in the MN-major tile; in units of 16 bytes.
   constexpr uint64_t b_step = TRANS ? 2 : 128;
   const int lane = threadIdx.x & 31;
-  const int num_tiles = a.m_tiles * a.n_tiles;
+  const int num_units = a.m_tiles * a.n_tiles * a.splits;
   volatile int *abort = &bars->abort;
   int sa = 0, sb = 0, it = 0;
   uint32_t pha = 0, phb = 0;
   bool ok = true;
-  for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++it) {
-    // The epilogue must have drained the accumulators of the previous tile.
+  for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x, ++it) {
+    const Unit un = unit_of(a, u, nk);
+    // The epilogue must have drained the accumulators of the previous unit.
     if (!wait_warp(&bars->tmem_empty, (it & 1) ^ 1u, abort, a.err)) break;
     tc_fence_after();
     // The second 128-row half only when this tile has x rows there.
-    const bool two = (tile % a.m_tiles) * BM + UM < a.M;
-    for (int kb = 0; kb < nk; ++kb) {
+    const bool two = (un.tile % a.m_tiles) * BM + UM < a.M;
+    for (int kb = un.kb0; kb < un.kb1; ++kb) {
       if (!wait_warp(&bars->full_a[sa], pha, abort, a.err) ||
           !wait_warp(&bars->full_b[sb], phb, abort, a.err)) {
         ok = false;
@@ -400,7 +431,7 @@ __device__ void mma_role(const GemmArgs &a, uint8_t *sA, uint8_t *sB, Barriers *
         const uint64_t db = TRANS ? sw128_kmajor_desc(bs) : sw128_mnmajor_desc(bs);
 #pragma unroll
         for (int j = 0; j < BK / 16; ++j) {
-          const uint32_t accumulate = (kb | j) != 0 ? 1u : 0u;
+          const uint32_t accumulate = (kb != un.kb0 || j != 0) ? 1u : 0u;
           umma<idesc>(tmem, da0 + 2 * j, db + b_step * j, accumulate);
           if (two) umma<idesc>(tmem + BN, da1 + 2 * j, db + b_step * j, accumulate);
         }
@@ -426,13 +457,15 @@ template <bool OUT_BF16>
 __device__ void epilogue_role(const GemmArgs &a, Barriers *bars, uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;  // TMEM lane quarter this warp may access
-  const int num_tiles = a.m_tiles * a.n_tiles;
+  const int num_units = a.m_tiles * a.n_tiles * a.splits;
   volatile int *abort = &bars->abort;
   const bool vec = OUT_BF16 ? (a.N % 8 == 0) : (a.N % 4 == 0);
+  const bool vec_ws = a.N % 4 == 0;
   int it = 0;
-  for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+  for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++it) {
     if (!wait_warp(&bars->tmem_full, it & 1, abort, a.err)) return;
     tc_fence_after();
+    const int tile = u / a.splits, split = u - tile * a.splits;
     const int n0 = (tile / a.m_tiles) * BN;
 #pragma unroll 1
     for (int hc = 0; hc < 2 * (BN / 32); ++hc) {
@@ -444,7 +477,21 @@ __device__ void epilogue_role(const GemmArgs &a, Barriers *bars, uint32_t tmem) 
       const int n = n0 + 32 * cc;
       if (m >= a.M || n >= a.N) continue;
       const int64_t o = static_cast<int64_t>(m) * a.N + n;
-      if (OUT_BF16) {
+      if (a.splits > 1) {
+        // A partial of a split tile: fp32 into this split's slice.
+        float *wp = a.ws + static_cast<int64_t>(split) * a.M * a.N + o;
+        if (vec_ws && n + 32 <= a.N) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            reinterpret_cast<float4 *>(wp)[j] =
+                make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                            __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (n + j < a.N) wp[j] = __uint_as_float(r[j]);
+        }
+      } else if (OUT_BF16) {
         uint16_t *yp = static_cast<uint16_t *>(a.y) + o;
         if (vec && n + 32 <= a.N) {
 #pragma unroll
@@ -534,7 +581,57 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, GemmArgs a) {
   }
 }
 
+// Split-K: y = the sum of the `splits` fp32 partial slices, added in slice
+// order (deterministic), converted to the output type.  Four outputs a thread
+// with 16-byte loads when the slices are 16-byte aligned.
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(256)
+splitk_finalize(const float *__restrict__ ws, int splits, int64_t mn, void *__restrict__ y) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  if (mn % 4 == 0) {
+    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4; i < mn;
+         i += stride * 4) {
+      float4 acc = *reinterpret_cast<const float4 *>(ws + i);
+      for (int sl = 1; sl < splits; ++sl) {
+        const float4 v = *reinterpret_cast<const float4 *>(ws + sl * mn + i);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      if (OUT_BF16) {
+        uint2 o;
+        o.x = pack_bf16x2(acc.x, acc.y);
+        o.y = pack_bf16x2(acc.z, acc.w);
+        *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(y) + i) = o;
+      } else {
+        *reinterpret_cast<float4 *>(static_cast<float *>(y) + i) = acc;
+      }
+    }
+  } else {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < mn; i += stride) {
+      float acc = ws[i];
+      for (int sl = 1; sl < splits; ++sl) acc += ws[sl * mn + i];
+      if (OUT_BF16) static_cast<uint16_t *>(y)[i] = f32_to_bf16_bits(acc);
+      else static_cast<float *>(y)[i] = acc;
+    }
+  }
+}
+
 // ----------------------------------------------------------------- host ----
+
+// One persistent block per SM.  With fewer output tiles than SMs, each tile's
+// K range is split so that the units fill the SMs (at least two k-blocks a
+// unit); the partials then need splits * M * N fp32 of workspace, never more
+// than one 256 x 256 tile per SM.
+int choose_splits(int tiles, int nk, int sms) {
+  if (tiles * 2 > sms) return 1;
+  int s = sms / tiles;
+  if (s > nk / 2) s = nk / 2;
+  if (s > 32) s = 32;
+  return s < 1 ? 1 : s;
+}
+
+size_t splitk_bytes(const GemmArgs &a) {
+  return static_cast<size_t>(a.splits) * a.M * a.N * sizeof(float);
+}
 
 template <int BITS, bool OUT_BF16, bool TRANS>
 cudaError_t launch_t(const uint16_t *x, const GemmArgs &a, cudaStream_t stream) {
@@ -553,9 +650,16 @@ cudaError_t launch_t(const uint16_t *x, const GemmArgs &a, cudaStream_t stream) 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int tiles = a.m_tiles * a.n_tiles;
-  const int grid = tiles < sm_count() ? tiles : sm_count();
+  const int units = a.m_tiles * a.n_tiles * a.splits;
+  const int grid = units < sm_count() ? units : sm_count();
   kern<<<grid, kThreads, kSmemBytes, stream>>>(map, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || a.splits == 1) return e;
+  const int64_t mn = static_cast<int64_t>(a.M) * a.N;
+  int64_t blocks = (mn / 4 + 255) / 256;
+  if (blocks > 4 * sm_count()) blocks = 4 * sm_count();
+  if (blocks < 1) blocks = 1;
+  splitk_finalize<OUT_BF16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.ws, a.splits, mn, a.y);
   return cudaGetLastError();
 }
 
@@ -584,6 +688,20 @@ cudaError_t launch_gemm(const uint16_t *x, int64_t M, const PackedWeight &w, boo
   a.n_tiles = (a.N + BN - 1) / BN;
   a.err = device_error_word();
   if (!a.err) return cudaErrorInvalidSymbol;
+  a.splits = choose_splits(a.m_tiles * a.n_tiles, (a.K + BK - 1) / BK, sm_count());
+  a.ws = nullptr;
+  if (a.splits > 1) {
+    // Stream-ordered: the workspace belongs to this call on this stream
+    // (a graph captures it as allocation and free nodes).  Without one the
+    // call runs unsplit.
+    void *p = nullptr;
+    if (cudaMallocAsync(&p, splitk_bytes(a), stream) == cudaSuccess) {
+      a.ws = static_cast<float *>(p);
+    } else {
+      cudaGetLastError();
+      a.splits = 1;
+    }
+  }
   cudaError_t e;
   switch (w.bits) {
     case 1: e = launch_bits<1>(x, a, transpose, y_bf16, stream); break;
@@ -593,7 +711,11 @@ cudaError_t launch_gemm(const uint16_t *x, int64_t M, const PackedWeight &w, boo
     case 5: e = launch_bits<5>(x, a, transpose, y_bf16, stream); break;
     case 6: e = launch_bits<6>(x, a, transpose, y_bf16, stream); break;
     case 8: e = launch_bits<8>(x, a, transpose, y_bf16, stream); break;
-    default: return cudaErrorInvalidValue;
+    default: e = cudaErrorInvalidValue;
+  }
+  if (a.ws) {
+    const cudaError_t fe = cudaFreeAsync(a.ws, stream);
+    if (e == cudaSuccess) e = fe;
   }
   if (e != cudaErrorNotSupported) return e;
   // x rows that TMA cannot address (K not a multiple of 8, possible when W is

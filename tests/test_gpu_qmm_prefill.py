@@ -123,3 +123,34 @@ def test_prefill_not_transposed_full_size():
     w = synth.quant_weight(13, K, N, 4, 64)
     x = synth.x_bf16(14, M, K)
     check_sampled(x, M, w, N, K, False, seed=15, what="prefill t0")
+
+
+# Split-K: with fewer output tiles than SMs, each tile's K range is split and
+# the fp32 partials are added by a second kernel.
+@pytest.mark.parametrize("bits", (3, 4, 8))
+@pytest.mark.parametrize("y_dtype", (qmm.QMM_F32, qmm.QMM_BF16))
+def test_split_k_ragged_n(bits, y_dtype):
+    # N = 202: not a multiple of 4, so the partials are added one element at a
+    # time; one 256-row tile, so K = 1024 (16 k-blocks) is split 8 ways.
+    M, N, K = 40, 202, 1024
+    w = synth.quant_weight(500 + bits, N, K, bits, 32)
+    x = synth.x_bf16(501 + bits, M, K)
+    check_full(x, M, w, N, K, True, y_dtype, "split-K ragged N bits=%d" % bits)
+
+
+@pytest.mark.parametrize("bits", (2, 4, 6))
+def test_split_k_not_transposed(bits):
+    M, N, K = 64, 256, 1024
+    w = synth.quant_weight(510 + bits, K, N, bits, 64)
+    x = synth.x_bf16(511 + bits, M, K)
+    check_full(x, M, w, N, K, False, qmm.QMM_F32, "split-K W stored [K, N] bits=%d" % bits)
+
+
+def test_split_k_repeats_bit_for_bit():
+    # The partials are added in a fixed order: two runs give the same bits.
+    M, N, K = 128, 1024, 4096
+    w = synth.quant_weight(520, N, K, 4, 64)
+    x = synth.x_bf16(521, M, K)
+    a = run_qmm(x, M, w, N, K, True, qmm.QMM_F32).cpu()
+    b = run_qmm(x, M, w, N, K, True, qmm.QMM_F32).cpu()
+    assert torch.equal(a, b)
