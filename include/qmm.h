@@ -117,6 +117,35 @@ qmm_status qmm_quantized_matmul(const uint16_t *x, int64_t M, const uint32_t *w,
                                 qmm_dtype y_dtype, qmm_stream_t stream);
 
 /*
+ * qmm_quantized_matmul_noalloc -- qmm_quantized_matmul for callers that cannot
+ * allocate device memory while they run: code that owns every byte of the
+ * device through its own allocator, or that records work where no allocation
+ * call may appear.  (The pages have no counterpart: MLX allocates its
+ * outputs and scratch through its own allocator.)
+ *
+ * Same arguments, checks, kernels and results as qmm_quantized_matmul.  The
+ * only difference: the split-K partials (M > 16 with few output tiles) go to
+ * a fixed 24 MiB scratch array inside the library instead of a stream-ordered
+ * allocation, so the call allocates and frees nothing.  Every GPU that loads
+ * the library holds that array until the process exits.
+ *   - A call whose partials would need more than 24 MiB (splits * M * N * 4
+ *     bytes) returns QMM_ERR_INVALID_ARG, says how much it needs, and runs
+ *     nothing; qmm_quantized_matmul has no such limit.
+ *   - The first call on each device looks up the array's device address
+ *     (set-up, once per device, with that device current); make that first
+ *     call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind (nothing in it needs to start at zero).  Calls whose kernels
+ *     overlap on the GPU -- on different streams without ordering between
+ *     them -- race on it and give wrong results; keep them ordered.
+ */
+qmm_status qmm_quantized_matmul_noalloc(const uint16_t *x, int64_t M, const uint32_t *w,
+                                        const uint16_t *scales, const uint16_t *biases,
+                                        int64_t N, int64_t K, int transpose,
+                                        int group_size, int bits, void *y,
+                                        qmm_dtype y_dtype, qmm_stream_t stream);
+
+/*
  * qmm_rows -- out[i, :] = dequant(W[idx[i], :]) for i < n: an embedding
  * lookup that dequantizes only the gathered rows in one pass.
  * (maya2_mlx quant.py, `rows`: dequantize(q[idx], scales[idx], biases[idx]).)

@@ -161,6 +161,51 @@ qmm_status qmm_quantized_matmul(const uint16_t *x, int64_t M, const uint32_t *w,
   return cuda_status(e, op);
 }
 
+// For callers that cannot allocate device memory: the checks and kernels of
+// qmm_quantized_matmul, with split-K partials in the library's static scratch.
+qmm_status qmm_quantized_matmul_noalloc(const uint16_t *x, int64_t M, const uint32_t *w,
+                                        const uint16_t *scales, const uint16_t *biases,
+                                        int64_t N, int64_t K, int transpose, int group_size,
+                                        int bits, void *y, qmm_dtype y_dtype,
+                                        qmm_stream_t stream) {
+  const char *op = "qmm_quantized_matmul_noalloc";
+  qmm_status st;
+  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
+  if ((st = check_dtype(op, y_dtype)) != QMM_OK) return st;
+  if (transpose != 0 && transpose != 1)
+    return fail(QMM_ERR_INVALID_ARG, "%s: transpose must be 0 or 1, got %d", op, transpose);
+  if (M < 0 || N < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative M or N", op);
+  if (K <= 0) return fail(QMM_ERR_INVALID_ARG, "%s: K must be positive, got %lld", op, (long long)K);
+  const int64_t rows = transpose ? N : K, cols = transpose ? K : N;
+  if (transpose || N > 0) {
+    if ((st = check_weight(op, w, scales, biases, rows, cols, group_size)) != QMM_OK) return st;
+  }
+  if (M == 0 || N == 0) return QMM_OK;
+  if (!x || !aligned16(x))
+    return fail(QMM_ERR_INVALID_ARG, "%s: x must be a non-null 16-byte aligned pointer", op);
+  if (!y || !aligned16(y))
+    return fail(QMM_ERR_INVALID_ARG, "%s: y must be a non-null 16-byte aligned pointer", op);
+  if (M > (int64_t(1) << 31) || K > (int64_t(1) << 31) || N > (int64_t(1) << 31))
+    return fail(QMM_ERR_INVALID_ARG, "%s: M, N and K must each be below 2^31", op);
+  // Set-up on the first call on this device: the scratch's device address.
+  float *scratch = qmm::static_scratch();
+  if (!scratch)
+    return fail(QMM_ERR_CUDA, "%s: cannot look up the static scratch on the current device", op);
+  qmm::PackedWeight pw{w, scales, biases, rows, cols, group_size, bits};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool bf16 = y_dtype == QMM_BF16;
+  if (M <= 16) return cuda_status(qmm::launch_gemv(x, M, pw, transpose != 0, y, bf16, s), op);
+  size_t needed = 0;
+  const cudaError_t e =
+      qmm::launch_gemm_static_scratch(x, M, pw, transpose != 0, y, bf16, scratch, s, &needed);
+  if (e == cudaErrorInvalidValue && needed > qmm::static_scratch_bytes())
+    return fail(QMM_ERR_INVALID_ARG,
+                "%s: M=%lld N=%lld K=%lld needs %zu bytes of split-K scratch, more than the "
+                "%zu this entry point holds (qmm_quantized_matmul has no such limit)",
+                op, (long long)M, (long long)N, (long long)K, needed, qmm::static_scratch_bytes());
+  return cuda_status(e, op);
+}
+
 qmm_status qmm_get_device_error(qmm_stream_t stream) {
   unsigned bits = 0;
   cudaError_t e = qmm::take_device_error(reinterpret_cast<cudaStream_t>(stream), &bits);

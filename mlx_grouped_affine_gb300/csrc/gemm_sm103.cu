@@ -730,4 +730,79 @@ cudaError_t launch_gemm(const uint16_t *x, int64_t M, const PackedWeight &w, boo
   return cudaSuccess;
 }
 
+// ------------------------------------------- static-scratch variant ----
+// For callers that cannot allocate device memory at call time: the same
+// kernels as launch_gemm, with the split-K partials in a fixed array of
+// kStaticScratchBytes that every device loading this library holds until
+// the process exits.  All calls on a device share it.
+namespace {
+constexpr size_t kStaticScratchFloats = size_t(6) << 20;  // 24 MiB of fp32
+static __device__ __align__(256) float g_static_scratch[kStaticScratchFloats];
+}  // namespace
+
+size_t static_scratch_bytes() { return kStaticScratchFloats * sizeof(float); }
+
+// The array's device address on the current device, looked up once per
+// device (with that device current); nullptr if the lookup fails.
+float *static_scratch() {
+  constexpr int kMaxDevices = 64;
+  static float *addr[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    float *p = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_static_scratch) != cudaSuccess)
+      return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+cudaError_t launch_gemm_static_scratch(const uint16_t *x, int64_t M, const PackedWeight &w,
+                                       bool transpose, void *y, bool y_bf16, float *scratch,
+                                       cudaStream_t stream, size_t *needed) {
+  GemmArgs a;
+  a.w = w.w;
+  a.scales = w.scales;
+  a.biases = w.biases;
+  a.y = y;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(transpose ? w.rows : w.cols);
+  a.K = static_cast<int>(transpose ? w.cols : w.rows);
+  a.group_shift = w.group == 32 ? 5 : w.group == 64 ? 6 : 7;
+  a.m_tiles = (a.M + BM - 1) / BM;
+  a.n_tiles = (a.N + BN - 1) / BN;
+  a.err = device_error_word();
+  if (!a.err) return cudaErrorInvalidSymbol;
+  // Same split as launch_gemm; x rows TMA cannot address take the decode
+  // kernel below and need no partials.
+  const bool tma_rows = (static_cast<int64_t>(a.K) * 2) % 16 == 0;
+  a.splits = tma_rows ? choose_splits(a.m_tiles * a.n_tiles, (a.K + BK - 1) / BK, sm_count()) : 1;
+  *needed = a.splits > 1 ? splitk_bytes(a) : 0;
+  if (*needed > static_scratch_bytes()) return cudaErrorInvalidValue;
+  a.ws = a.splits > 1 ? scratch : nullptr;
+  cudaError_t e;
+  switch (w.bits) {
+    case 1: e = launch_bits<1>(x, a, transpose, y_bf16, stream); break;
+    case 2: e = launch_bits<2>(x, a, transpose, y_bf16, stream); break;
+    case 3: e = launch_bits<3>(x, a, transpose, y_bf16, stream); break;
+    case 4: e = launch_bits<4>(x, a, transpose, y_bf16, stream); break;
+    case 5: e = launch_bits<5>(x, a, transpose, y_bf16, stream); break;
+    case 6: e = launch_bits<6>(x, a, transpose, y_bf16, stream); break;
+    case 8: e = launch_bits<8>(x, a, transpose, y_bf16, stream); break;
+    default: e = cudaErrorInvalidValue;
+  }
+  if (e != cudaErrorNotSupported) return e;
+  const size_t ysz = y_bf16 ? 2 : 4;
+  for (int64_t m0 = 0; m0 < M; m0 += 16) {
+    const int64_t rows = M - m0 < 16 ? M - m0 : 16;
+    e = launch_gemv(x + m0 * a.K, rows, w, transpose,
+                    static_cast<char *>(y) + m0 * static_cast<int64_t>(a.N) * ysz, y_bf16, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace qmm

@@ -53,4 +53,14 @@ cudaError_t launch_gemm(const uint16_t *x, int64_t M, const PackedWeight &w,
                         bool transpose, void *y, bool y_bf16,
                         cudaStream_t stream);
 
+// The variant of launch_gemm whose split-K partials go to `scratch` (the
+// library's static array, see static_scratch) instead of a stream-ordered
+// allocation.  *needed gets the partials' bytes; cudaErrorInvalidValue, with
+// nothing launched, when they exceed static_scratch_bytes().
+size_t static_scratch_bytes();
+float *static_scratch();
+cudaError_t launch_gemm_static_scratch(const uint16_t *x, int64_t M, const PackedWeight &w,
+                                       bool transpose, void *y, bool y_bf16, float *scratch,
+                                       cudaStream_t stream, size_t *needed);
+
 }  // namespace qmm
