@@ -151,6 +151,33 @@ def qmm(x, M, packed, scales, biases, N, K, transpose, group_size, bits, nthread
     return y, a
 
 
+def gather_qmm(x, x_batches, M, packed, scales, biases, w_batches, N, K, lhs, rhs, transpose,
+               group_size, bits, nthreads=None):
+    """(y, absy): fp64 [B, M, N] each.  Output batch i is x[lhs[i]] times
+    dequant(w[rhs[i]]) transposed (or not), each batch an ordinary
+    quantized_matmul (nuvec_core quantized.rs, `gather_qmm` doc: the indices
+    address the flattened batch dimensions of x [..., M, K] and of w, scales,
+    biases; either index array defaults to every batch of its operand in
+    order).  lhs, rhs: uint32 [B] (already broadcast) or None.  An index past
+    its operand gives a batch of zeros (the pages are silent; as rows)."""
+    rows, cols = (N, K) if transpose else (K, N)
+    xs = np.asarray(x).reshape(x_batches, M, K)
+    pk = np.asarray(packed).reshape(w_batches, rows, -1)
+    sc = np.asarray(scales).reshape(w_batches, rows, -1)
+    bi = np.asarray(biases).reshape(w_batches, rows, -1)
+    B = len(lhs) if lhs is not None else len(rhs) if rhs is not None else x_batches
+    y = np.zeros((B, M, N), dtype=np.float64)
+    a = np.zeros((B, M, N), dtype=np.float64)
+    for i in range(B):
+        xi = int(lhs[i]) if lhs is not None else i
+        wi = int(rhs[i]) if rhs is not None else i
+        if xi >= x_batches or wi >= w_batches:
+            continue
+        y[i], a[i] = qmm(xs[xi], M, pk[wi], sc[wi], bi[wi], N, K, transpose, group_size, bits,
+                         nthreads)
+    return y, a
+
+
 def qmm_sampled(x, M, packed, scales, biases, N, K, transpose, group_size, bits,
                 ms, ns, nthreads=None):
     """(y, absy) at the sampled positions (ms[i], ns[i])."""

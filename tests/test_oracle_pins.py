@@ -268,3 +268,49 @@ def test_rows_out_of_table_gives_zero_row():
     assert (out[1] == 0).all() and (out[2] == 0).all()
     full = oracle.dequantize(w.packed, w.scales, w.biases, 10, 64, 32, 4, "bf16")
     assert (out[0] == full[3]).all() and (out[3] == full[9]).all()
+
+
+# -- gather_qmm -----------------------------------------------------------------
+
+def test_gather_qmm_doctest_values():
+    g = load_golden("gather_qmm_experts.txt")
+    E, N, K, bits, gs = (int(g[k][0]) for k in ("experts", "N", "K", "bits", "group_size"))
+    rhs = np.array(ints(g["rhs"]), dtype=np.uint32)
+    packed = np.zeros((E, N, K * bits // 32), dtype=np.uint32)
+    s = np.full((E, N, K // gs), 0x3F80, dtype=np.uint16)                  # scale 1.0
+    b = np.stack([np.full((N, K // gs), int(np.float32(e + 1).view(np.uint32) >> 16),
+                          dtype=np.uint16) for e in range(E)])             # bias e + 1
+    x = np.full((len(rhs), 1, K), 0x3F80, dtype=np.uint16)                 # ones
+    y, _ = oracle.gather_qmm(x, len(rhs), 1, packed, s, b, E, N, K, None, rhs, True, gs, bits)
+    assert y.shape == (len(rhs), 1, N)
+    assert list(y.reshape(-1)[:5]) == [float(v) for v in g["expect_first5"]]
+
+
+@pytest.mark.parametrize("transpose", (True, False))
+def test_gather_qmm_matches_numpy_gather_then_matmul(transpose):
+    # Independent route: numpy's unpacker for dense weights, fancy indexing for
+    # the gather, numpy matmul for the product.
+    E, XB, M, N, K, bits, gs = 3, 4, 2, 32, 64, 5, 32
+    rows, cols = (N, K) if transpose else (K, N)
+    ws = [synth.quant_weight(900 + e, rows, cols, bits, gs) for e in range(E)]
+    packed = np.stack([w.packed for w in ws]); s = np.stack([w.scales for w in ws])
+    b = np.stack([w.biases for w in ws])
+    x = synth.x_bf16(901, XB * M, K).reshape(XB, M, K)
+    lhs = np.array([3, 0, 0, 2, 1], dtype=np.uint32)
+    rhs = np.array([2, 2, 0, 1, 0], dtype=np.uint32)
+    y, _ = oracle.gather_qmm(x, XB, M, packed, s, b, E, N, K, lhs, rhs, transpose, gs, bits)
+    dense = np.stack([np_dense_f64(w) for w in ws])                        # [E, rows, cols]
+    xf = bf16_f64(x)
+    for i in range(len(lhs)):
+        wd = dense[rhs[i]]
+        want = xf[lhs[i]] @ (wd.T if transpose else wd)
+        np.testing.assert_allclose(y[i], want, rtol=1e-12, atol=1e-12)
+
+
+def test_gather_qmm_out_of_range_index_gives_zero_batch():
+    E, N, K = 2, 4, 64
+    w = synth.quant_weight(910, E * N, K, 4, 64)
+    x = synth.x_bf16(911, 2, K).reshape(2, 1, K)
+    y, a = oracle.gather_qmm(x, 2, 1, w.packed, w.scales, w.biases, E, N, K, None,
+                             np.array([1, 7], dtype=np.uint32), True, 64, 4)
+    assert (y[1] == 0).all() and (a[1] == 0).all() and (y[0] != 0).any()
