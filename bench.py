@@ -269,6 +269,39 @@ def sweep_detail(torch, qmm, synth, peaks, warmup):
     return out
 
 
+def gather_detail(torch, qmm, synth, peaks, warmup):
+    """Mixture-of-experts decode through gather_qmm: 8 experts [14336, 4096]
+    4-bit g64, 32 routed token slots (16 tokens x top 2, one x row each),
+    indices drawn once (seeded).  GB/s counts the bytes of the experts used
+    (each read once) plus x and y; sorted = the slots grouped by expert."""
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(
+        {np.dtype(np.uint32): np.int32, np.dtype(np.uint16): np.int16}[a.dtype])).cuda()
+    E, N, K, B = 8, 14336, 4096, 32
+    ws = [synth.quant_weight(120 + e, N, K, 4, 64) for e in range(E)]
+    packed = dev(np.stack([w.packed for w in ws]))
+    sc = dev(np.stack([w.scales for w in ws]))
+    bi = dev(np.stack([w.biases for w in ws]))
+    rhs_host = synth.indices(121, B, E)
+    used = len(set(rhs_host.tolist()))
+    nbytes = used * ws[0].nbytes + B * K * 2 + B * N * 2
+    x = dev(synth.x_bf16(122, B, K))
+    y = torch.empty((B, 1, N), dtype=torch.int16, device="cuda")
+    out = {}
+    for name, rhs, sorted_ in (("sorted", np.sort(rhs_host), 1), ("unsorted", rhs_host, 0)):
+        r = dev(rhs.astype(np.uint32))
+
+        def fn():
+            qmm.qmm_gather_qmm(x, B, 1, packed, sc, bi, E, N, K, None, r, B, 1, 64, 4, sorted_,
+                               y, qmm.QMM_BF16)
+        t = time_graph(torch, graph_of(torch, fn), 100, warmup)
+        out["gather_qmm_moe_8x%dx%d_b4_32slots_%s" % (N, K, name)] = {
+            "us": round(t * 1e3, 2), "experts_used": used, "GB/s": round(nbytes / (t * 1e-3) / 1e9, 1),
+            "frac_hbm": round(nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
+    del packed, sc, bi
+    torch.cuda.empty_cache()
+    return out
+
+
 def measured_traffic():
     """DRAM bytes per launch of the decode kernel from the committed ncu capture,
     or None if the kernel source changed since it was taken."""
@@ -400,6 +433,7 @@ def run_gpu(args):
                 del c
                 torch.cuda.empty_cache()
         detail.update(sweep_detail(torch, qmm, synth, peaks, args.warmup))
+        detail.update(gather_detail(torch, qmm, synth, peaks, args.warmup))
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,

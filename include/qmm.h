@@ -117,6 +117,42 @@ qmm_status qmm_quantized_matmul(const uint16_t *x, int64_t M, const uint32_t *w,
                                 qmm_dtype y_dtype, qmm_stream_t stream);
 
 /*
+ * qmm_gather_qmm -- quantized matmuls of gathered batches (mixture-of-experts
+ * layers): output batch b is x[lhs_indices[b]] . dequant(w[rhs_indices[b]])^T
+ * (transpose = 1) or without the transpose.
+ * (nuvec_core quantized.rs, `gather_qmm`: the indices address the flattened
+ *  batch dimensions of x and w; either defaults to every batch of its operand
+ *  in order; sorted_indices promises sorted rhs_indices, so that each weight
+ *  batch can be walked once.)
+ *
+ *   x            bf16 [x_batches, M, K]
+ *   w, scales, biases  w_batches weights one after another, each laid out
+ *                as qmm_quantized_matmul's (transpose = 1: w [N, K*bits/32],
+ *                scales/biases [N, K/group_size]; transpose = 0:
+ *                [K, N*bits/32] and [K, N/group_size])
+ *   lhs_indices  uint32 [batches] on the device, or NULL: batch b uses x[b]
+ *   rhs_indices  uint32 [batches] on the device, or NULL: batch b uses w[b]
+ *   y            [batches, M, N] of y_dtype
+ *
+ * The index arrays are the broadcast of the caller's index shapes, flattened
+ * (the caller broadcasts).  NULL indices need x_batches (resp. w_batches)
+ * equal to batches.  An index past its operand gives a batch of zeros and is
+ * reported by qmm_get_device_error as QMM_ERR_INDEX.  sorted_indices = 1
+ * with M == 1, NULL lhs_indices and non-decreasing rhs_indices lets one block
+ * stream each weight tile once for all the batches that use it; if the
+ * promise is false the results are wrong (nothing is read out of bounds).
+ * Same tolerance as qmm_quantized_matmul.  The kernels are the decode ones
+ * (M is walked in 8- or 16-row passes), launched without programmatic
+ * dependent launch: the indices may come from the previous kernel.
+ */
+qmm_status qmm_gather_qmm(const uint16_t *x, int64_t x_batches, int64_t M, const uint32_t *w,
+                          const uint16_t *scales, const uint16_t *biases, int64_t w_batches,
+                          int64_t N, int64_t K, const uint32_t *lhs_indices,
+                          const uint32_t *rhs_indices, int64_t batches, int transpose,
+                          int group_size, int bits, int sorted_indices, void *y,
+                          qmm_dtype y_dtype, qmm_stream_t stream);
+
+/*
  * qmm_quantized_matmul_noalloc -- qmm_quantized_matmul for callers that cannot
  * allocate device memory while they run: code that owns every byte of the
  * device through its own allocator, or that records work where no allocation

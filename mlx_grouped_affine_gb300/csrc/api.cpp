@@ -161,6 +161,56 @@ qmm_status qmm_quantized_matmul(const uint16_t *x, int64_t M, const uint32_t *w,
   return cuda_status(e, op);
 }
 
+qmm_status qmm_gather_qmm(const uint16_t *x, int64_t x_batches, int64_t M, const uint32_t *w,
+                          const uint16_t *scales, const uint16_t *biases, int64_t w_batches,
+                          int64_t N, int64_t K, const uint32_t *lhs_indices,
+                          const uint32_t *rhs_indices, int64_t batches, int transpose,
+                          int group_size, int bits, int sorted_indices, void *y,
+                          qmm_dtype y_dtype, qmm_stream_t stream) {
+  const char *op = "qmm_gather_qmm";
+  qmm_status st;
+  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
+  if ((st = check_dtype(op, y_dtype)) != QMM_OK) return st;
+  if (transpose != 0 && transpose != 1)
+    return fail(QMM_ERR_INVALID_ARG, "%s: transpose must be 0 or 1, got %d", op, transpose);
+  if (sorted_indices != 0 && sorted_indices != 1)
+    return fail(QMM_ERR_INVALID_ARG, "%s: sorted_indices must be 0 or 1, got %d", op, sorted_indices);
+  if (M < 0 || N < 0 || batches < 0)
+    return fail(QMM_ERR_INVALID_ARG, "%s: negative M, N or batch count", op);
+  if (K <= 0) return fail(QMM_ERR_INVALID_ARG, "%s: K must be positive, got %lld", op, (long long)K);
+  if (x_batches < 1 || w_batches < 1)
+    return fail(QMM_ERR_INVALID_ARG, "%s: x and w need at least one batch each", op);
+  if (!lhs_indices && x_batches != batches)
+    return fail(QMM_ERR_INVALID_ARG,
+                "%s: without lhs_indices x must hold one batch per output batch (%lld, not %lld)",
+                op, (long long)batches, (long long)x_batches);
+  if (!rhs_indices && w_batches != batches)
+    return fail(QMM_ERR_INVALID_ARG,
+                "%s: without rhs_indices w must hold one batch per output batch (%lld, not %lld)",
+                op, (long long)batches, (long long)w_batches);
+  const int64_t rows = transpose ? N : K, cols = transpose ? K : N;
+  if (transpose || N > 0) {
+    // One weight batch is [rows, cols]; all of them are checked as one table.
+    if ((st = check_weight(op, w, scales, biases, rows, cols, group_size)) != QMM_OK) return st;
+  }
+  if (M == 0 || N == 0 || batches == 0) return QMM_OK;
+  if (!x || !aligned16(x))
+    return fail(QMM_ERR_INVALID_ARG, "%s: x must be a non-null 16-byte aligned pointer", op);
+  if (!y || !aligned16(y))
+    return fail(QMM_ERR_INVALID_ARG, "%s: y must be a non-null 16-byte aligned pointer", op);
+  if ((lhs_indices && !aligned16(lhs_indices)) || (rhs_indices && !aligned16(rhs_indices)))
+    return fail(QMM_ERR_INVALID_ARG, "%s: index arrays must be 16-byte aligned", op);
+  const int64_t lim = int64_t(1) << 31;
+  if (M >= lim || K >= lim || N >= lim || batches >= lim || x_batches >= lim || w_batches >= lim ||
+      x_batches * M * K >= (int64_t(1) << 62) || w_batches * rows >= lim)
+    return fail(QMM_ERR_INVALID_ARG, "%s: sizes out of range (each below 2^31, w_batches*rows too)", op);
+  qmm::PackedWeight pw{w, scales, biases, rows, cols, group_size, bits};
+  cudaError_t e = qmm::launch_gather(x, x_batches, M, pw, w_batches, lhs_indices, rhs_indices,
+                                     batches, transpose != 0, sorted_indices != 0, y,
+                                     y_dtype == QMM_BF16, reinterpret_cast<cudaStream_t>(stream));
+  return cuda_status(e, op);
+}
+
 // For callers that cannot allocate device memory: the checks and kernels of
 // qmm_quantized_matmul, with split-K partials in the library's static scratch.
 qmm_status qmm_quantized_matmul_noalloc(const uint16_t *x, int64_t M, const uint32_t *w,

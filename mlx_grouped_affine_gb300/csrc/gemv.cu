@@ -51,6 +51,64 @@ struct GemvArgs {
   int parts;  // K parts = cluster size * warps per block
 };
 
+// gather_qmm (nuvec_core quantized.rs, `gather_qmm`): output batch b is
+// x[lhs[b]] times weight batch rhs[b].  blockIdx.z (+ z0) is the output
+// batch, or -- sorted -- the weight batch whose run of tokens the block walks.
+struct GatherArgs {
+  const uint32_t *lhs, *rhs;       // device [batches], or null: batch b itself
+  int x_batches, w_batches, batches;
+  int z0;                          // first batch (or weight batch) of this launch
+  int sorted;                      // runs of equal, sorted rhs; M == 1 and lhs null
+  int64_t x_bstride, y_bstride;    // elements between batches of x and of y
+  int64_t w_bstride, sb_bstride;   // words between weight batches; elements between scale batches
+  int64_t x_off, y_off;            // elements: the 16-row slice of a batch this launch covers
+};
+
+// First position in the sorted v[0, n) whose value is >= key.
+__device__ __forceinline__ int lower_bound_u32(const uint32_t *v, int n, uint32_t key) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(v + mid) < key) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// Zero outputs y[m, n] for m < rows, n in [n0, n0 + cols) (clipped to N): the
+// part of an output batch a block owns, when its index is out of range.
+__device__ __forceinline__ void zero_y_tile(void *y, bool out_bf16, int rows, int N, int n0, int cols) {
+  for (int i = threadIdx.x; i < rows * cols; i += blockDim.x) {
+    const int m = i / cols, n = n0 + (i - m * cols);
+    if (n >= N) continue;
+    const int64_t o = static_cast<int64_t>(m) * N + n;
+    if (out_bf16) static_cast<uint16_t *>(y)[o] = 0;
+    else static_cast<float *>(y)[o] = 0.0f;
+  }
+}
+
+// Unsorted gather for the kernels that read W with plain loads: point `a` at
+// the block's batches.  False (after zeroing the block's outputs and raising
+// the index bit) when an index is out of range.
+template <bool OUT_BF16>
+__device__ __forceinline__ bool gather_point(GemvArgs &a, const GatherArgs &g, int n0, int cols,
+                                             unsigned *err) {
+  const int z = g.z0 + static_cast<int>(blockIdx.z);
+  const uint32_t wb = g.rhs ? __ldg(g.rhs + z) : static_cast<uint32_t>(z);
+  const uint32_t xb = g.lhs ? __ldg(g.lhs + z) : static_cast<uint32_t>(z);
+  a.y = static_cast<char *>(a.y) + (z * g.y_bstride + g.y_off) * (OUT_BF16 ? 2 : 4);
+  if (wb >= static_cast<uint32_t>(g.w_batches) || xb >= static_cast<uint32_t>(g.x_batches)) {
+    zero_y_tile(a.y, OUT_BF16, a.M, a.N, n0, cols);
+    if (threadIdx.x == 0) atomicOr(err, kErrIndexBit);
+    return false;
+  }
+  a.x += xb * g.x_bstride + g.x_off;
+  a.w += wb * g.w_bstride;
+  a.scales += wb * g.sb_bstride;
+  a.biases += wb * g.sb_bstride;
+  return true;
+}
+
 // ------------------------------------------------------------------------
 // Cross-warp and cross-block reduction of ACC fp32 values per lane, then the
 // store.  Every warp of every block in the cluster holds a partial of the
@@ -122,9 +180,9 @@ __device__ __forceinline__ void reduce_and_store(float (&acc)[ACC], float *red, 
 // (2t, 2t+1) with physical codes 32t+4r, +1 and logical (2t+8, 2t+9) with
 // 32t+4r+2, +3, so the matching x values are the two words of x at
 // k = 32t + 4r: lane (g, t) reads x[m][32t .. 32t+32) with four 16-byte loads.
-template <int BITS, int NT, bool OUT_BF16>
+template <int BITS, int NT, bool OUT_BF16, bool GATHER>
 __global__ void __launch_bounds__(512)
-gemv_t_kernel(GemvArgs a) {
+gemv_t_kernel(GemvArgs a, GatherArgs ga, unsigned *err) {
   extern __shared__ float red[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, warps = blockDim.x >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -132,6 +190,9 @@ gemv_t_kernel(GemvArgs a) {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
   const int n0 = blockIdx.x * 16;
+  if constexpr (GATHER) {
+    if (!gather_point<OUT_BF16>(a, ga, n0, 16, err)) return;
+  }
   const int part = static_cast<int>(crank) * warps + warp;
   const int nchunks = (a.K + 127) >> 7;
   const int c_begin = static_cast<int>(static_cast<int64_t>(nchunks) * part / a.parts);
@@ -222,9 +283,9 @@ gemv_t_kernel(GemvArgs a) {
 // whose rows are k and whose column 2t+e is n = 8t + 2j + e; movmatrix.trans
 // turns Q_j into the B fragment of n8-tile j, whose column c is
 // n = 8(c/2) + 2j + (c%2).  x is the A operand (natural pairs along K).
-template <int BITS, bool OUT_BF16>
+template <int BITS, bool OUT_BF16, bool GATHER>
 __global__ void __launch_bounds__(512)
-gemv_n_kernel(GemvArgs a) {
+gemv_n_kernel(GemvArgs a, GatherArgs ga, unsigned *err) {
   extern __shared__ float red[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, warps = blockDim.x >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -232,6 +293,9 @@ gemv_n_kernel(GemvArgs a) {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
   const int n0 = blockIdx.x * 32;
+  if constexpr (GATHER) {
+    if (!gather_point<OUT_BF16>(a, ga, n0, 32, err)) return;
+  }
   const int part = static_cast<int>(crank) * warps + warp;
   const int nsteps = (a.K + 15) >> 4;  // K (the stored row count) may be any size
   const int s_begin = static_cast<int>(static_cast<int64_t>(nsteps) * part / a.parts);
@@ -389,10 +453,12 @@ template <int NT>
 __host__ __device__ constexpr int tma_warps() { return NT == 1 ? 16 : 8; }
 constexpr int kTmaMaxChunksPerWarp = 4;
 
-template <int BITS, int NT, bool OUT_BF16>
-__global__ void __launch_bounds__(32 * tma_warps<NT>())
+// (A minimum of 0 blocks leaves the register budget to the compiler, as with
+// no minimum given; the gather instantiations are held to two blocks per SM.)
+template <int BITS, int NT, bool OUT_BF16, bool GATHER>
+__global__ void __launch_bounds__(32 * tma_warps<NT>(), GATHER ? 2 : 0)
 gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayout L,
-                  unsigned *err) {
+                  unsigned *err, GatherArgs ga) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -407,6 +473,44 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
   const int k0 = static_cast<int>(crank) * L.kr;
   const int ncodes = max(0, min(a.K, k0 + L.kr) - k0);
   const int nchunks = ncodes >> 7;
+  // The block's weight rows start at wrow0 (its weight batch's first row in
+  // the tensor map); it computes `rows` rows of x from xbase into ybase.
+  int wrow0 = 0, rows = a.M;
+  const uint16_t *xbase = a.x;
+  char *ybase = static_cast<char *>(a.y);
+  if constexpr (GATHER) {
+    constexpr int ysz = OUT_BF16 ? 2 : 4;
+    const int z = ga.z0 + static_cast<int>(blockIdx.z);
+    uint32_t wb;
+    if (ga.sorted) {
+      // Weight batch z walks its run [lo, hi) of the sorted rhs (one x row per
+      // batch); z == w_batches takes the indices past the weights.
+      const int lo = lower_bound_u32(ga.rhs, ga.batches, static_cast<uint32_t>(z));
+      const int hi = z < ga.w_batches ? lower_bound_u32(ga.rhs, ga.batches, static_cast<uint32_t>(z + 1))
+                                      : ga.batches;
+      if (hi <= lo) return;
+      ybase += static_cast<int64_t>(lo) * a.N * ysz;
+      if (z >= ga.w_batches) {
+        if (crank == 0) zero_y_tile(ybase, OUT_BF16, hi - lo, a.N, n0, 16);
+        if (threadIdx.x == 0) atomicOr(err, kErrIndexBit);
+        return;
+      }
+      wb = static_cast<uint32_t>(z);
+      rows = hi - lo;
+      xbase = a.x + static_cast<int64_t>(lo) * a.K;
+    } else {
+      wb = ga.rhs ? __ldg(ga.rhs + z) : static_cast<uint32_t>(z);
+      const uint32_t xb = ga.lhs ? __ldg(ga.lhs + z) : static_cast<uint32_t>(z);
+      ybase += z * ga.y_bstride * ysz;
+      if (wb >= static_cast<uint32_t>(ga.w_batches) || xb >= static_cast<uint32_t>(ga.x_batches)) {
+        if (crank == 0) zero_y_tile(ybase, OUT_BF16, a.M, a.N, n0, 16);
+        if (threadIdx.x == 0) atomicOr(err, kErrIndexBit);
+        return;
+      }
+      xbase = a.x + xb * ga.x_bstride;
+    }
+    wrow0 = static_cast<int>(wb) * a.N;
+  }
 
   if (warp == 0) {
     for (int c = lane; c <= nchunks; c += 32) mbar_init(&bars[c], 1);  // chunks, then x
@@ -421,14 +525,14 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
       asm volatile(
           "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
           " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem + c * L.box_bytes)),
-          "l"(&wmap), "r"(xw), "r"(n0), "r"(smem_u32(&bars[c]))
+          "l"(&wmap), "r"(xw), "r"(wrow0 + n0), "r"(smem_u32(&bars[c]))
           : "memory");
     }
   }
   griddep_launch_dependents();
 
   const int groups = a.K >> a.group_shift;
-  const int row0 = min(n0 + g, a.N - 1), row1 = min(n0 + g + 8, a.N - 1);
+  const int row0 = wrow0 + min(n0 + g, a.N - 1), row1 = wrow0 + min(n0 + g + 8, a.N - 1);
   const uint16_t *s0p = a.scales + static_cast<int64_t>(row0) * groups;
   const uint16_t *b0p = a.biases + static_cast<int64_t>(row0) * groups;
   const uint16_t *s1p = a.scales + static_cast<int64_t>(row1) * groups;
@@ -453,110 +557,126 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
   // its own 32 x values per chunk (L2-resident: every block reads the same x),
   // natural pairs like the weights.
   griddep_wait();
-  // Lanes whose x row is beyond M keep zero fragments throughout.
-  auto load_x = [&](int c, uint32_t (&xv)[NT][16]) {
+  bool ok = true;
+  // One pass computes mrows <= 8 * NT rows of x, from xc, into yc.
+  auto pass = [&](const uint16_t *xc, void *yc, int mrows) {
+    GemvArgs ac = a;
+    ac.x = xc;
+    ac.y = yc;
+    ac.M = mrows;
+    // Lanes whose x row is beyond M keep zero fragments throughout.
+    auto load_x = [&](int c, uint32_t (&xv)[NT][16]) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int m = g + 8 * nt;
-      if (m < a.M) {
-        const uint4 *xp = reinterpret_cast<const uint4 *>(
-            a.x + static_cast<int64_t>(m) * a.K + k0 + (c << 7) + 32 * t);
+      for (int nt = 0; nt < NT; ++nt) {
+        const int m = g + 8 * nt;
+        if (m < ac.M) {
+          const uint4 *xp = reinterpret_cast<const uint4 *>(
+              ac.x + static_cast<int64_t>(m) * a.K + k0 + (c << 7) + 32 * t);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint4 u = __ldg(xp + i);
-          xv[nt][4 * i] = u.x; xv[nt][4 * i + 1] = u.y; xv[nt][4 * i + 2] = u.z; xv[nt][4 * i + 3] = u.w;
+          for (int i = 0; i < 4; ++i) {
+            const uint4 u = __ldg(xp + i);
+            xv[nt][4 * i] = u.x; xv[nt][4 * i + 1] = u.y; xv[nt][4 * i + 2] = u.z; xv[nt][4 * i + 3] = u.w;
+          }
         }
       }
-    }
-  };
-  uint32_t xv[NT][16];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int i = 0; i < 16; ++i) xv[nt][i] = 0u;
-
-  // Two accumulator sets (even and odd MMA steps) keep the MMA chain short.
-  float acc[2][NT][4];
-#pragma unroll
-  for (int h = 0; h < 2; ++h)
+    };
+    uint32_t xv[NT][16];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[h][nt][i] = 0.0f;
+      for (int i = 0; i < 16; ++i) xv[nt][i] = 0u;
 
-  constexpr int kRowBytes = 16 * BITS;  // one row of a chunk box
-  bool ok = true;
+    // Two accumulator sets (even and odd MMA steps) keep the MMA chain short.
+    float acc[2][NT][4];
 #pragma unroll
-  for (int j = 0; j < kTmaMaxChunksPerWarp; ++j) {
-    const int c = warp + j * kW;
-    if (!ok || c >= nchunks) break;
-    const uint16_t *cur = sv[j];
-    load_x(c, xv);
-    uint32_t spins = 0;
-    while (!mbar_try_wait(&bars[c], 0)) {
-      if (++spins > (1u << 24)) {
-        if (lane == 0) atomicOr(err, kErrTimeoutBit);
-        ok = false;
-        break;
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[h][nt][i] = 0.0f;
+
+    constexpr int kRowBytes = 16 * BITS;  // one row of a chunk box
+#pragma unroll
+    for (int j = 0; j < kTmaMaxChunksPerWarp; ++j) {
+      const int c = warp + j * kW;
+      if (!ok || c >= nchunks) break;
+      const uint16_t *cur = sv[j];
+      load_x(c, xv);
+      uint32_t spins = 0;
+      while (!mbar_try_wait(&bars[c], 0)) {
+        if (++spins > (1u << 24)) {
+          if (lane == 0) atomicOr(err, kErrTimeoutBit);
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) break;
+      const uint8_t *box = smem + c * L.box_bytes;
+      uint32_t v0[BITS], v1[BITS];
+      if constexpr (BITS == 8) {
+        // 128-byte swizzle: the lane's 32 bytes are 16-byte units 2t, 2t+1.
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const uint4 u0 = *reinterpret_cast<const uint4 *>(box + g * 128 + (((2 * t + i) ^ g) << 4));
+          const uint4 u1 = *reinterpret_cast<const uint4 *>(box + (g + 8) * 128 + (((2 * t + i) ^ g) << 4));
+          v0[4 * i] = u0.x; v0[4 * i + 1] = u0.y; v0[4 * i + 2] = u0.z; v0[4 * i + 3] = u0.w;
+          v1[4 * i] = u1.x; v1[4 * i + 1] = u1.y; v1[4 * i + 2] = u1.z; v1[4 * i + 3] = u1.w;
+        }
+      } else {
+        lds_words<BITS>(box + g * kRowBytes + t * 4 * BITS, v0);
+        lds_words<BITS>(box + (g + 8) * kRowBytes + t * 4 * BITS, v1);
+      }
+      const uint32_t b0 = bcast_bf16x2(cur[1]), b1 = bcast_bf16x2(cur[3]);
+      if (__all_sync(0xffffffffu, fast_scale(cur[0]) && fast_scale(cur[2]))) {
+        uint32_t m0[fast_slots<BITS>()], m1[fast_slots<BITS>()];
+        fast_muls<BITS>(cur[0], m0);
+        fast_muls<BITS>(cur[2], m1);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const uint32_t a0 = pair_fast<BITS>(v0, 2 * r, m0, b0), a2 = pair_fast<BITS>(v0, 2 * r + 1, m0, b0);
+          const uint32_t a1 = pair_fast<BITS>(v1, 2 * r, m1, b1), a3 = pair_fast<BITS>(v1, 2 * r + 1, m1, b1);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma_bf16_16816(acc[r & 1][nt], a0, a1, a2, a3, xv[nt][2 * r], xv[nt][2 * r + 1]);
+        }
+      } else {
+        const uint32_t s0 = bcast_bf16x2(cur[0]), s1 = bcast_bf16x2(cur[2]);
+        const float fs0 = bf16_bits_to_f32(cur[0]), fb0 = bf16_bits_to_f32(cur[1]);
+        const float fs1 = bf16_bits_to_f32(cur[2]), fb1 = bf16_bits_to_f32(cur[3]);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const uint32_t a0 = pair_exact<BITS>(v0, 2 * r, s0, b0, fs0, fb0);
+          const uint32_t a2 = pair_exact<BITS>(v0, 2 * r + 1, s0, b0, fs0, fb0);
+          const uint32_t a1 = pair_exact<BITS>(v1, 2 * r, s1, b1, fs1, fb1);
+          const uint32_t a3 = pair_exact<BITS>(v1, 2 * r + 1, s1, b1, fs1, fb1);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma_bf16_16816(acc[r & 1][nt], a0, a1, a2, a3, xv[nt][2 * r], xv[nt][2 * r + 1]);
+        }
       }
     }
-    if (!ok) break;
-    const uint8_t *box = smem + c * L.box_bytes;
-    uint32_t v0[BITS], v1[BITS];
-    if constexpr (BITS == 8) {
-      // 128-byte swizzle: the lane's 32 bytes are 16-byte units 2t, 2t+1.
+
+    float flat[NT * 4];
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const uint4 u0 = *reinterpret_cast<const uint4 *>(box + g * 128 + (((2 * t + i) ^ g) << 4));
-        const uint4 u1 = *reinterpret_cast<const uint4 *>(box + (g + 8) * 128 + (((2 * t + i) ^ g) << 4));
-        v0[4 * i] = u0.x; v0[4 * i + 1] = u0.y; v0[4 * i + 2] = u0.z; v0[4 * i + 3] = u0.w;
-        v1[4 * i] = u1.x; v1[4 * i + 1] = u1.y; v1[4 * i + 2] = u1.z; v1[4 * i + 3] = u1.w;
-      }
-    } else {
-      lds_words<BITS>(box + g * kRowBytes + t * 4 * BITS, v0);
-      lds_words<BITS>(box + (g + 8) * kRowBytes + t * 4 * BITS, v1);
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) flat[nt * 4 + i] = acc[0][nt][i] + acc[1][nt][i];
+    reduce_and_store<NT * 4>(flat, red, tma_warps<NT>(), static_cast<int>(csize), ac, OUT_BF16,
+                             [&](int ln, int i, int &m, int &n) {
+                               const int gg = ln >> 2, tt = ln & 3, nt = i >> 2, e = i & 3;
+                               n = n0 + gg + 8 * (e >> 1);
+                               m = 8 * nt + 2 * tt + (e & 1);
+                             });
+  };
+  if constexpr (GATHER) {
+    for (int mc = 0; mc < rows; mc += 8 * NT) {
+      if (mc > 0) __syncthreads();  // the previous pass's reduction has read `red`
+      pass(xbase + static_cast<int64_t>(mc) * a.K,
+           ybase + static_cast<int64_t>(mc) * a.N * (OUT_BF16 ? 2 : 4), min(8 * NT, rows - mc));
     }
-    const uint32_t b0 = bcast_bf16x2(cur[1]), b1 = bcast_bf16x2(cur[3]);
-    if (__all_sync(0xffffffffu, fast_scale(cur[0]) && fast_scale(cur[2]))) {
-      uint32_t m0[fast_slots<BITS>()], m1[fast_slots<BITS>()];
-      fast_muls<BITS>(cur[0], m0);
-      fast_muls<BITS>(cur[2], m1);
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const uint32_t a0 = pair_fast<BITS>(v0, 2 * r, m0, b0), a2 = pair_fast<BITS>(v0, 2 * r + 1, m0, b0);
-        const uint32_t a1 = pair_fast<BITS>(v1, 2 * r, m1, b1), a3 = pair_fast<BITS>(v1, 2 * r + 1, m1, b1);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          mma_bf16_16816(acc[r & 1][nt], a0, a1, a2, a3, xv[nt][2 * r], xv[nt][2 * r + 1]);
-      }
-    } else {
-      const uint32_t s0 = bcast_bf16x2(cur[0]), s1 = bcast_bf16x2(cur[2]);
-      const float fs0 = bf16_bits_to_f32(cur[0]), fb0 = bf16_bits_to_f32(cur[1]);
-      const float fs1 = bf16_bits_to_f32(cur[2]), fb1 = bf16_bits_to_f32(cur[3]);
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const uint32_t a0 = pair_exact<BITS>(v0, 2 * r, s0, b0, fs0, fb0);
-        const uint32_t a2 = pair_exact<BITS>(v0, 2 * r + 1, s0, b0, fs0, fb0);
-        const uint32_t a1 = pair_exact<BITS>(v1, 2 * r, s1, b1, fs1, fb1);
-        const uint32_t a3 = pair_exact<BITS>(v1, 2 * r + 1, s1, b1, fs1, fb1);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          mma_bf16_16816(acc[r & 1][nt], a0, a1, a2, a3, xv[nt][2 * r], xv[nt][2 * r + 1]);
-      }
-    }
+  } else {
+    pass(xbase, ybase, rows);
   }
-
-  float flat[NT * 4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) flat[nt * 4 + i] = acc[0][nt][i] + acc[1][nt][i];
-  reduce_and_store<NT * 4>(flat, red, tma_warps<NT>(), static_cast<int>(csize), a, OUT_BF16,
-                           [&](int ln, int i, int &m, int &n) {
-                             const int gg = ln >> 2, tt = ln & 3, nt = i >> 2, e = i & 3;
-                             n = n0 + gg + 8 * (e >> 1);
-                             m = 8 * nt + 2 * tt + (e & 1);
-                           });
 }
 
 // ------------------------------------------------------------------------
@@ -605,25 +725,44 @@ cudaError_t launch_ex(Kern kern, dim3 grid, dim3 block, size_t smem, int cluster
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-template <typename Kern>
-cudaError_t launch_clustered(Kern kern, dim3 grid, Shape s, size_t smem, cudaStream_t stream,
-                             const GemvArgs &a) {
-  return launch_ex(kern, grid, dim3(32 * s.warps), smem, s.cluster, false, stream, a);
+// The z extent of a launch: 1, or the batches of a gather (output batches,
+// or weight batches + 1 when sorted), with the arguments its kernels read.
+struct Batches {
+  GatherArgs g{};
+  int64_t count = 1;
+};
+
+// Launches over z in pieces the grid's z dimension can hold.
+template <typename Launch>
+cudaError_t over_z(const Batches &b, Launch launch) {
+  constexpr int64_t kMaxZ = 65535;
+  GatherArgs g = b.g;
+  for (int64_t z0 = 0; z0 < b.count; z0 += kMaxZ) {
+    g.z0 = static_cast<int>(z0);
+    const cudaError_t e = launch(g, static_cast<unsigned>(b.count - z0 < kMaxZ ? b.count - z0 : kMaxZ));
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
-template <int BITS, int NT, bool OUT_BF16>
-cudaError_t launch_t(const GemvArgs &a0, cudaStream_t stream) {
+template <int BITS, int NT, bool OUT_BF16, bool GATHER>
+cudaError_t launch_t(const GemvArgs &a0, const Batches &b, cudaStream_t stream) {
   GemvArgs a = a0;
   const int64_t tiles = (a.N + 15) / 16;
   Shape s = pick_shape(tiles, (a.K + 127) / 128);
   a.parts = s.warps * s.cluster;
   const size_t smem = sizeof(float) * s.warps * NT * 4 * 32;
-  return launch_clustered(gemv_t_kernel<BITS, NT, OUT_BF16>, dim3(tiles, s.cluster), s, smem,
-                          stream, a);
+  unsigned *err = device_error_word();
+  if (!err) return cudaErrorInvalidSymbol;
+  return over_z(b, [&](const GatherArgs &g, unsigned nz) {
+    return launch_ex(gemv_t_kernel<BITS, NT, OUT_BF16, GATHER>,
+                     dim3(static_cast<unsigned>(tiles), s.cluster, nz), dim3(32 * s.warps), smem,
+                     s.cluster, false, stream, a, g, err);
+  });
 }
 
-template <int BITS, int NT, bool OUT_BF16>
-cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, cudaStream_t stream) {
+template <int BITS, int NT, bool OUT_BF16, bool GATHER>
+cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, const Batches &b, cudaStream_t stream) {
   const int64_t tiles = (a.N + 15) / 16;
   const int box_bytes = 16 * 16 * BITS;
   auto kr_of = [&](int c) { return ((a.K / c + 127) / 128) * 128; };
@@ -648,52 +787,113 @@ cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, cudaStream_t stream) {
   L.red_off = L.x_off;
   L.bar_off = L.red_off + tma_warps<NT>() * NT * 4 * 32 * 4;
   const size_t smem = L.bar_off + 8 * (nch + 1) + 1024;  // + slack for the 1024-byte base
+  // The tensor map spans every weight batch: batch e's row n is row e*N + n.
+  const uint64_t map_rows = static_cast<uint64_t>(a.N) * (GATHER ? b.g.w_batches : 1);
+  if (map_rows >= (uint64_t(1) << 31)) return cudaErrorNotSupported;
   CUtensorMap wmap;
   cudaError_t e = encode_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.w,
-                                static_cast<uint64_t>(a.K) * BITS / 32, a.N,
+                                static_cast<uint64_t>(a.K) * BITS / 32, map_rows,
                                 static_cast<uint64_t>(a.K) * BITS / 8, 4 * BITS, 16,
                                 BITS == 8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
   unsigned *err = device_error_word();
   if (!err) return cudaErrorInvalidSymbol;
-  auto kern = gemv_t_tma_kernel<BITS, NT, OUT_BF16>;
+  auto kern = gemv_t_tma_kernel<BITS, NT, OUT_BF16, GATHER>;
   if (smem > 48 * 1024) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  return launch_ex(kern, dim3(static_cast<unsigned>(tiles), C), dim3(32 * tma_warps<NT>()), smem, C,
-                   pdl, stream, wmap, a, L, err);
+  return over_z(b, [&](const GatherArgs &g, unsigned nz) {
+    return launch_ex(kern, dim3(static_cast<unsigned>(tiles), C, nz), dim3(32 * tma_warps<NT>()),
+                     smem, C, pdl, stream, wmap, a, L, err, g);
+  });
 }
 
-template <int BITS, bool OUT_BF16>
-cudaError_t launch_n(const GemvArgs &a0, cudaStream_t stream) {
+template <int BITS, bool OUT_BF16, bool GATHER>
+cudaError_t launch_n(const GemvArgs &a0, const Batches &b, cudaStream_t stream) {
   GemvArgs a = a0;
   const int64_t tiles = (a.N + 31) / 32;
   Shape s = pick_shape(tiles, (a.K + 15) / 16);
   a.parts = s.warps * s.cluster;
   const size_t smem = sizeof(float) * s.warps * 16 * 32;
-  return launch_clustered(gemv_n_kernel<BITS, OUT_BF16>, dim3(tiles, s.cluster), s, smem,
-                          stream, a);
+  unsigned *err = device_error_word();
+  if (!err) return cudaErrorInvalidSymbol;
+  return over_z(b, [&](const GatherArgs &g, unsigned nz) {
+    return launch_ex(gemv_n_kernel<BITS, OUT_BF16, GATHER>,
+                     dim3(static_cast<unsigned>(tiles), s.cluster, nz), dim3(32 * s.warps), smem,
+                     s.cluster, false, stream, a, g, err);
+  });
 }
 
 template <int BITS>
 cudaError_t launch_bits(const GemvArgs &a, bool transpose, bool y_bf16, bool pdl,
                         cudaStream_t stream) {
+  const Batches one;
   if (transpose && a.K % 128 == 0) {
     cudaError_t e;
     if (a.M <= 8)
-      e = y_bf16 ? launch_t_tma<BITS, 1, true>(a, pdl, stream)
-                 : launch_t_tma<BITS, 1, false>(a, pdl, stream);
+      e = y_bf16 ? launch_t_tma<BITS, 1, true, false>(a, pdl, one, stream)
+                 : launch_t_tma<BITS, 1, false, false>(a, pdl, one, stream);
     else
-      e = y_bf16 ? launch_t_tma<BITS, 2, true>(a, pdl, stream)
-                 : launch_t_tma<BITS, 2, false>(a, pdl, stream);
+      e = y_bf16 ? launch_t_tma<BITS, 2, true, false>(a, pdl, one, stream)
+                 : launch_t_tma<BITS, 2, false, false>(a, pdl, one, stream);
     if (e != cudaErrorNotSupported) return e;
   }
   if (transpose) {
-    if (a.M <= 8) return y_bf16 ? launch_t<BITS, 1, true>(a, stream) : launch_t<BITS, 1, false>(a, stream);
-    return y_bf16 ? launch_t<BITS, 2, true>(a, stream) : launch_t<BITS, 2, false>(a, stream);
+    if (a.M <= 8)
+      return y_bf16 ? launch_t<BITS, 1, true, false>(a, one, stream)
+                    : launch_t<BITS, 1, false, false>(a, one, stream);
+    return y_bf16 ? launch_t<BITS, 2, true, false>(a, one, stream)
+                  : launch_t<BITS, 2, false, false>(a, one, stream);
   }
-  return y_bf16 ? launch_n<BITS, true>(a, stream) : launch_n<BITS, false>(a, stream);
+  return y_bf16 ? launch_n<BITS, true, false>(a, one, stream)
+                : launch_n<BITS, false, false>(a, one, stream);
+}
+
+// gather_qmm.  Transposed W with K a multiple of 128 takes the TMA kernel,
+// which walks each block's x rows in passes of 8 * NT (so any M); sorted
+// batches (one x row each, lhs absent) let a block stream one weight tile
+// for its whole run.  Otherwise the plain-load kernels, over 16-row slices
+// of each batch.  No programmatic dependent launch: the indices may come
+// from the previous kernel.
+template <int BITS>
+cudaError_t launch_gather_bits(const GemvArgs &a0, const Batches &b0, bool transpose, bool y_bf16,
+                               bool sorted, cudaStream_t stream) {
+  if (transpose && a0.K % 128 == 0) {
+    cudaError_t e;
+    if (sorted) {
+      Batches bs = b0;
+      bs.g.sorted = 1;
+      bs.count = b0.g.w_batches + 1;
+      e = y_bf16 ? launch_t_tma<BITS, 1, true, true>(a0, false, bs, stream)
+                 : launch_t_tma<BITS, 1, false, true>(a0, false, bs, stream);
+    } else if (a0.M <= 8) {
+      e = y_bf16 ? launch_t_tma<BITS, 1, true, true>(a0, false, b0, stream)
+                 : launch_t_tma<BITS, 1, false, true>(a0, false, b0, stream);
+    } else {
+      e = y_bf16 ? launch_t_tma<BITS, 2, true, true>(a0, false, b0, stream)
+                 : launch_t_tma<BITS, 2, false, true>(a0, false, b0, stream);
+    }
+    if (e != cudaErrorNotSupported) return e;
+  }
+  for (int64_t m0 = 0; m0 < a0.M; m0 += 16) {
+    GemvArgs a = a0;
+    a.M = static_cast<int>(a0.M - m0 < 16 ? a0.M - m0 : 16);
+    Batches b = b0;
+    b.g.x_off = m0 * a0.K;
+    b.g.y_off = m0 * a0.N;
+    cudaError_t e;
+    if (transpose) {
+      if (a.M <= 8)
+        e = y_bf16 ? launch_t<BITS, 1, true, true>(a, b, stream) : launch_t<BITS, 1, false, true>(a, b, stream);
+      else
+        e = y_bf16 ? launch_t<BITS, 2, true, true>(a, b, stream) : launch_t<BITS, 2, false, true>(a, b, stream);
+    } else {
+      e = y_bf16 ? launch_n<BITS, true, true>(a, b, stream) : launch_n<BITS, false, true>(a, b, stream);
+    }
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -720,6 +920,49 @@ cudaError_t launch_gemv(const uint16_t *x, int64_t M, const PackedWeight &w, boo
     case 5: return launch_bits<5>(a, transpose, y_bf16, pdl, stream);
     case 6: return launch_bits<6>(a, transpose, y_bf16, pdl, stream);
     case 8: return launch_bits<8>(a, transpose, y_bf16, pdl, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_gather(const uint16_t *x, int64_t x_batches, int64_t M, const PackedWeight &w,
+                          int64_t w_batches, const uint32_t *lhs, const uint32_t *rhs,
+                          int64_t batches, bool transpose, bool sorted, void *y, bool y_bf16,
+                          cudaStream_t stream) {
+  GemvArgs a;
+  a.x = x;
+  a.w = w.w;
+  a.scales = w.scales;
+  a.biases = w.biases;
+  a.y = y;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(transpose ? w.rows : w.cols);
+  a.K = static_cast<int>(transpose ? w.cols : w.rows);
+  a.group_shift = w.group == 32 ? 5 : w.group == 64 ? 6 : 7;
+  a.parts = 1;
+  Batches b;
+  b.g.lhs = lhs;
+  b.g.rhs = rhs;
+  b.g.x_batches = static_cast<int>(x_batches);
+  b.g.w_batches = static_cast<int>(w_batches);
+  b.g.batches = static_cast<int>(batches);
+  b.g.sorted = 0;
+  b.g.x_bstride = M * a.K;
+  b.g.y_bstride = M * a.N;
+  b.g.w_bstride = w.rows * ((w.cols * w.bits) / 32);
+  b.g.sb_bstride = w.rows * (w.cols / w.group);
+  b.g.x_off = b.g.y_off = 0;
+  b.count = batches;
+  // One weight tile streamed per run: batches sorted by weight batch, one x
+  // row each, x batches in order.
+  const bool by_runs = sorted && M == 1 && !lhs && rhs;
+  switch (w.bits) {
+    case 1: return launch_gather_bits<1>(a, b, transpose, y_bf16, by_runs, stream);
+    case 2: return launch_gather_bits<2>(a, b, transpose, y_bf16, by_runs, stream);
+    case 3: return launch_gather_bits<3>(a, b, transpose, y_bf16, by_runs, stream);
+    case 4: return launch_gather_bits<4>(a, b, transpose, y_bf16, by_runs, stream);
+    case 5: return launch_gather_bits<5>(a, b, transpose, y_bf16, by_runs, stream);
+    case 6: return launch_gather_bits<6>(a, b, transpose, y_bf16, by_runs, stream);
+    case 8: return launch_gather_bits<8>(a, b, transpose, y_bf16, by_runs, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -53,6 +53,15 @@ cudaError_t launch_gemm(const uint16_t *x, int64_t M, const PackedWeight &w,
                         bool transpose, void *y, bool y_bf16,
                         cudaStream_t stream);
 
+// gather_qmm: output batch b (of `batches`) is x[lhs[b]] (M x K, of
+// x_batches) times weight batch rhs[b] (of w_batches, each shaped as w);
+// lhs / rhs null means b itself.  `sorted` promises rhs is sorted.  Device
+// indices out of range zero their batch and raise kErrIndexBit.
+cudaError_t launch_gather(const uint16_t *x, int64_t x_batches, int64_t M, const PackedWeight &w,
+                          int64_t w_batches, const uint32_t *lhs, const uint32_t *rhs,
+                          int64_t batches, bool transpose, bool sorted, void *y, bool y_bf16,
+                          cudaStream_t stream);
+
 // The variant of launch_gemm whose split-K partials go to `scratch` (the
 // library's static array, see static_scratch) instead of a stream-ordered
 // allocation.  *needed gets the partials' bytes; cudaErrorInvalidValue, with

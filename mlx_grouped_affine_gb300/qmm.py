@@ -14,8 +14,9 @@ QMM_F32, QMM_BF16 = 0, 1
 STATUS_NAMES = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED",
                 3: "QMM_ERR_CUDA", 4: "QMM_ERR_INDEX", 5: "QMM_ERR_TIMEOUT"}
 QMM_LAUNCH_PDL = 1
-EXPORTS = ("qmm_dequantize", "qmm_quantized_matmul", "qmm_quantized_matmul_noalloc", "qmm_rows",
-           "qmm_last_error", "qmm_get_device_error", "qmm_set_launch_flags")
+EXPORTS = ("qmm_dequantize", "qmm_quantized_matmul", "qmm_quantized_matmul_noalloc",
+           "qmm_gather_qmm", "qmm_rows", "qmm_last_error", "qmm_get_device_error",
+           "qmm_set_launch_flags")
 
 _lib = None
 
@@ -36,10 +37,11 @@ def lib():
         L.qmm_dequantize.argtypes = [P, P, P, I64, I64, I, I, P, I, P]
         L.qmm_quantized_matmul.argtypes = [P, I64, P, P, P, I64, I64, I, I, I, P, I, P]
         L.qmm_quantized_matmul_noalloc.argtypes = [P, I64, P, P, P, I64, I64, I, I, I, P, I, P]
+        L.qmm_gather_qmm.argtypes = [P, I64, I64, P, P, P, I64, I64, I64, P, P, I64, I, I, I, I, P, I, P]
         L.qmm_rows.argtypes = [P, P, P, I64, I64, P, I64, I, I, P, I, P]
         L.qmm_get_device_error.argtypes = [P]
         for f in ("qmm_dequantize", "qmm_quantized_matmul", "qmm_quantized_matmul_noalloc",
-                  "qmm_rows", "qmm_get_device_error"):
+                  "qmm_gather_qmm", "qmm_rows", "qmm_get_device_error"):
             getattr(L, f).restype = I
         L.qmm_set_launch_flags.argtypes = [ctypes.c_uint]
         L.qmm_set_launch_flags.restype = ctypes.c_uint
@@ -96,6 +98,14 @@ def qmm_quantized_matmul_noalloc(x, M, w, scales, biases, N, K, transpose, group
     _check(lib().qmm_quantized_matmul_noalloc(_ptr(x), M, _ptr(w), _ptr(scales), _ptr(biases), N,
                                               K, int(transpose), group_size, bits, _ptr(y),
                                               y_dtype, _stream(stream)))
+
+
+def qmm_gather_qmm(x, x_batches, M, w, scales, biases, w_batches, N, K, lhs_indices, rhs_indices,
+                   batches, transpose, group_size, bits, sorted_indices, y, y_dtype, stream=None):
+    _check(lib().qmm_gather_qmm(_ptr(x), x_batches, M, _ptr(w), _ptr(scales), _ptr(biases),
+                                w_batches, N, K, _ptr(lhs_indices), _ptr(rhs_indices), batches,
+                                int(transpose), group_size, bits, int(sorted_indices), _ptr(y),
+                                y_dtype, _stream(stream)))
 
 
 def qmm_rows(w, scales, biases, table_rows, cols, idx, n, group_size, bits, out, out_dtype,
