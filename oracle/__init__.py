@@ -178,6 +178,33 @@ def gather_qmm(x, x_batches, M, packed, scales, biases, w_batches, N, K, lhs, rh
     return y, a
 
 
+def silu_gate_qmm(gate, up, M, packed, scales, biases, N, K, group_size, bits, resid=None):
+    """(y, scale): fp64 [M, N] each.  y = dequant(W) (silu(gate) * up), plus
+    resid when given (spark_runtime weights/mlx_int8.rs, `gemv_silu_gate` and
+    `gemv_silu_gate_resid` docs: y[n] = x_resid[n] + sum_k W[n, k] *
+    (silu(gate[k]) * up[k])), for each of the M rows; silu(g) = g / (1 + e^-g).
+    Everything in fp64 from the bf16 inputs (W transposed: [N, K]).  scale =
+    sum_k |x w| + |resid|, the tolerance scale."""
+    g = _bf16_f64(gate).reshape(M, K)
+    u = _bf16_f64(up).reshape(M, K)
+    with np.errstate(over="ignore"):
+        x = g / (1.0 + np.exp(-g)) * u
+    codes = unpack(packed, K, bits).astype(np.float64)
+    rep = np.repeat(np.arange(K // group_size), group_size)
+    w = _bf16_f64(scales)[:, rep] * codes + _bf16_f64(biases)[:, rep]
+    y = x @ w.T
+    a = np.abs(x) @ np.abs(w).T
+    if resid is not None:
+        r = _bf16_f64(resid).reshape(M, N)
+        y = y + r
+        a = a + np.abs(r)
+    return y, a
+
+
+def _bf16_f64(h):
+    return (np.asarray(h, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
 def qmm_sampled(x, M, packed, scales, biases, N, K, transpose, group_size, bits,
                 ms, ns, nthreads=None):
     """(y, absy) at the sampled positions (ms[i], ns[i])."""

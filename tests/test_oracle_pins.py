@@ -314,3 +314,32 @@ def test_gather_qmm_out_of_range_index_gives_zero_batch():
     y, a = oracle.gather_qmm(x, 2, 1, w.packed, w.scales, w.biases, E, N, K, None,
                              np.array([1, 7], dtype=np.uint32), True, 64, 4)
     assert (y[1] == 0).all() and (a[1] == 0).all() and (y[0] != 0).any()
+
+
+# -- fused decode GEMVs ------------------------------------------------------------
+
+def test_silu_gate_zero_gate_gives_resid_exactly():
+    N, K, M = 16, 128, 2
+    w = synth.quant_weight(920, N, K, 4, 64)
+    gate = np.zeros((M, K), dtype=np.uint16)
+    up = synth.x_bf16(921, M, K)
+    resid = synth.x_bf16(922, M, N)
+    y, a = oracle.silu_gate_qmm(gate, up, M, w.packed, w.scales, w.biases, N, K, 64, 4, resid)
+    assert (y == bf16_f64(resid)).all() and (a == np.abs(bf16_f64(resid))).all()
+
+
+@pytest.mark.parametrize("bits", (3, 4, 8))
+def test_silu_gate_matches_scipy_expit_route(bits):
+    # Independent route: scipy's logistic function for silu(g) = g * expit(g),
+    # numpy's unpacker for the dense weight, numpy matmul.
+    special = pytest.importorskip("scipy.special")
+    N, K, M, gs = 24, 256, 3, 32
+    w = synth.quant_weight(930 + bits, N, K, bits, gs)
+    gate = synth.x_bf16(931, M, K)
+    up = synth.x_bf16(932, M, K)
+    resid = synth.x_bf16(933, M, N)
+    y, _ = oracle.silu_gate_qmm(gate, up, M, w.packed, w.scales, w.biases, N, K, gs, bits, resid)
+    g = bf16_f64(gate)
+    x = g * special.expit(g) * bf16_f64(up)
+    want = x @ np_dense_f64(w).T + bf16_f64(resid)
+    np.testing.assert_allclose(y, want, rtol=1e-12, atol=1e-12)
