@@ -153,6 +153,54 @@ qmm_status qmm_gather_qmm(const uint16_t *x, int64_t x_batches, int64_t M, const
                           qmm_dtype y_dtype, qmm_stream_t stream);
 
 /*
+ * qmm_gemv_gate_up -- the two projections of a gated feed-forward block from
+ * one x in one launch: y_gate = x . dequant(W_gate)^T, y_up = x . dequant(W_up)^T.
+ * (spark_runtime weights/mlx_int8.rs, `gemv_gate_up`: both weights share
+ *  out and in features and group size, and x is read for both.)
+ *
+ *   x                 bf16 [M, K], 1 <= M <= 16
+ *   w_gate, w_up      uint32 [N, K*bits/32] each (transposed layout)
+ *   scales_gate, biases_gate, scales_up, biases_up  bf16 [N, K/group_size]
+ *   y_gate, y_up      [M, N] of y_dtype
+ *
+ * Rules: as qmm_quantized_matmul with transpose = 1, and K a multiple of 128.
+ * Same tolerance.  Launched like the decode kernel (programmatic dependent
+ * launch when QMM_LAUNCH_PDL is set).
+ */
+qmm_status qmm_gemv_gate_up(const uint16_t *x, int64_t M, const uint32_t *w_gate,
+                            const uint16_t *scales_gate, const uint16_t *biases_gate,
+                            const uint32_t *w_up, const uint16_t *scales_up,
+                            const uint16_t *biases_up, int64_t N, int64_t K, int group_size,
+                            int bits, void *y_gate, void *y_up, qmm_dtype y_dtype,
+                            qmm_stream_t stream);
+
+/*
+ * qmm_gemv_silu_gate -- y = dequant(W) . (silu(gate) * up) (+ resid), the
+ * down projection of a gated feed-forward block with its input formed inside
+ * the kernel: no intermediate [M, K] buffer and no separate launch.
+ * (spark_runtime weights/mlx_int8.rs, `gemv_silu_gate` and
+ *  `gemv_silu_gate_resid`: y[n] = x_resid[n] + sum_k W[n, k] *
+ *  (silu(gate[k]) * up[k]).)
+ *
+ *   gate, up  bf16 [M, K], 1 <= M <= 8
+ *   w         uint32 [N, K*bits/32], scales/biases bf16 [N, K/group_size]
+ *   resid     bf16 [M, N] added to y before its rounding, or NULL
+ *   y         [M, N] of y_dtype
+ *
+ * silu(g) = g / (1 + exp(-g)) and its product with up are formed in fp32 and
+ * rounded once to bf16 before the contraction (fp32 accumulation, as
+ * qmm_quantized_matmul).  Every output is within
+ * 8e-3 * (sum_k |x[m,k] * w[n,k]| + |resid[m,n]|) + 1e-6 of the exact value,
+ * x being the exact silu(gate) * up.  Rules: as qmm_gemv_gate_up for the
+ * weight; K a multiple of 128.
+ */
+qmm_status qmm_gemv_silu_gate(const uint16_t *gate, const uint16_t *up, int64_t M,
+                              const uint32_t *w, const uint16_t *scales, const uint16_t *biases,
+                              int64_t N, int64_t K, int group_size, int bits,
+                              const uint16_t *resid, void *y, qmm_dtype y_dtype,
+                              qmm_stream_t stream);
+
+/*
  * qmm_quantized_matmul_noalloc -- qmm_quantized_matmul for callers that cannot
  * allocate device memory while they run: code that owns every byte of the
  * device through its own allocator, or that records work where no allocation

@@ -211,6 +211,71 @@ qmm_status qmm_gather_qmm(const uint16_t *x, int64_t x_batches, int64_t M, const
   return cuda_status(e, op);
 }
 
+// Checks shared by the fused decode GEMVs: a transposed weight [N, K] with K
+// a multiple of 128, 1 <= M <= max_m.
+static qmm_status check_fused(const char *op, int64_t M, int64_t max_m, const uint32_t *w,
+                              const uint16_t *scales, const uint16_t *biases, int64_t N,
+                              int64_t K, int group_size, int bits, qmm_dtype y_dtype) {
+  qmm_status st;
+  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
+  if ((st = check_dtype(op, y_dtype)) != QMM_OK) return st;
+  if (M < 0 || N < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative M or N", op);
+  if (M > max_m)
+    return fail(QMM_ERR_INVALID_ARG, "%s: M is at most %lld, got %lld", op, (long long)max_m,
+                (long long)M);
+  if (K <= 0 || K % 128 != 0 || K >= (int64_t(1) << 31))
+    return fail(QMM_ERR_INVALID_ARG, "%s: K must be a positive multiple of 128, got %lld", op,
+                (long long)K);
+  if (N >= (int64_t(1) << 31)) return fail(QMM_ERR_INVALID_ARG, "%s: N must be below 2^31", op);
+  return check_weight(op, w, scales, biases, N, K, group_size);
+}
+
+qmm_status qmm_gemv_gate_up(const uint16_t *x, int64_t M, const uint32_t *w_gate,
+                            const uint16_t *scales_gate, const uint16_t *biases_gate,
+                            const uint32_t *w_up, const uint16_t *scales_up,
+                            const uint16_t *biases_up, int64_t N, int64_t K, int group_size,
+                            int bits, void *y_gate, void *y_up, qmm_dtype y_dtype,
+                            qmm_stream_t stream) {
+  const char *op = "qmm_gemv_gate_up";
+  qmm_status st;
+  if ((st = check_fused(op, M, 16, w_gate, scales_gate, biases_gate, N, K, group_size, bits,
+                        y_dtype)) != QMM_OK)
+    return st;
+  if ((st = check_weight(op, w_up, scales_up, biases_up, N, K, group_size)) != QMM_OK) return st;
+  if (M == 0 || N == 0) return QMM_OK;
+  if (!x || !aligned16(x))
+    return fail(QMM_ERR_INVALID_ARG, "%s: x must be a non-null 16-byte aligned pointer", op);
+  if (!y_gate || !aligned16(y_gate) || !y_up || !aligned16(y_up))
+    return fail(QMM_ERR_INVALID_ARG, "%s: y_gate and y_up must be non-null 16-byte aligned pointers", op);
+  qmm::PackedWeight g{w_gate, scales_gate, biases_gate, N, K, group_size, bits};
+  qmm::PackedWeight u{w_up, scales_up, biases_up, N, K, group_size, bits};
+  return cuda_status(qmm::launch_gate_up(x, M, g, u, y_gate, y_up, y_dtype == QMM_BF16,
+                                         reinterpret_cast<cudaStream_t>(stream)),
+                     op);
+}
+
+qmm_status qmm_gemv_silu_gate(const uint16_t *gate, const uint16_t *up, int64_t M,
+                              const uint32_t *w, const uint16_t *scales, const uint16_t *biases,
+                              int64_t N, int64_t K, int group_size, int bits,
+                              const uint16_t *resid, void *y, qmm_dtype y_dtype,
+                              qmm_stream_t stream) {
+  const char *op = "qmm_gemv_silu_gate";
+  qmm_status st;
+  if ((st = check_fused(op, M, 8, w, scales, biases, N, K, group_size, bits, y_dtype)) != QMM_OK)
+    return st;
+  if (M == 0 || N == 0) return QMM_OK;
+  if (!gate || !aligned16(gate) || !up || !aligned16(up))
+    return fail(QMM_ERR_INVALID_ARG, "%s: gate and up must be non-null 16-byte aligned pointers", op);
+  if (resid && !aligned16(resid))
+    return fail(QMM_ERR_INVALID_ARG, "%s: resid must be 16-byte aligned", op);
+  if (!y || !aligned16(y))
+    return fail(QMM_ERR_INVALID_ARG, "%s: y must be a non-null 16-byte aligned pointer", op);
+  qmm::PackedWeight pw{w, scales, biases, N, K, group_size, bits};
+  return cuda_status(qmm::launch_silu_gate(gate, up, M, pw, resid, y, y_dtype == QMM_BF16,
+                                           reinterpret_cast<cudaStream_t>(stream)),
+                     op);
+}
+
 // For callers that cannot allocate device memory: the checks and kernels of
 // qmm_quantized_matmul, with split-K partials in the library's static scratch.
 qmm_status qmm_quantized_matmul_noalloc(const uint16_t *x, int64_t M, const uint32_t *w,

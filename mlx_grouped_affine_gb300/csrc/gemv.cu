@@ -49,6 +49,20 @@ struct GemvArgs {
   int M, N, K;
   int group_shift;
   int parts;  // K parts = cluster size * warps per block
+  const uint16_t *resid;  // bf16 [M, N] added to y before it is stored, or null
+};
+
+// Fused decode GEMVs (spark_runtime weights/mlx_int8.rs, `gemv_gate_up`,
+// `gemv_silu_gate`, `gemv_silu_gate_resid`).
+//   kFuseDual: blockIdx.z = 1 computes a second weight (scales2, biases2,
+//     through the second tensor map) on the same x into y2.
+//   kFuseSilu: x[m, k] = RN_bf16(silu(gate[m, k]) * up[m, k]) in fp32,
+//     formed by each block in shared memory for its K range.
+constexpr int kFuseNone = 0, kFuseDual = 1, kFuseSilu = 2;
+struct FuseArgs {
+  const uint16_t *scales2, *biases2;
+  void *y2;
+  const uint16_t *gate, *up;   // bf16 [M, K]
 };
 
 // gather_qmm (nuvec_core quantized.rs, `gather_qmm`): output batch b is
@@ -166,8 +180,9 @@ __device__ __forceinline__ void reduce_and_store(float (&acc)[ACC], float *red, 
     map(lane, i, m, n);
     if (m < a.M && n < a.N) {
       const int64_t o = static_cast<int64_t>(m) * a.N + n;
-      if (out_bf16) static_cast<uint16_t *>(a.y)[o] = f32_to_bf16_bits(sum[i]);
-      else static_cast<float *>(a.y)[o] = sum[i];
+      const float v = a.resid ? sum[i] + bf16_bits_to_f32(a.resid[o]) : sum[i];
+      if (out_bf16) static_cast<uint16_t *>(a.y)[o] = f32_to_bf16_bits(v);
+      else static_cast<float *>(a.y)[o] = v;
     }
   }
 }
@@ -454,11 +469,13 @@ __host__ __device__ constexpr int tma_warps() { return NT == 1 ? 16 : 8; }
 constexpr int kTmaMaxChunksPerWarp = 4;
 
 // (A minimum of 0 blocks leaves the register budget to the compiler, as with
-// no minimum given; the gather instantiations are held to two blocks per SM.)
-template <int BITS, int NT, bool OUT_BF16, bool GATHER>
-__global__ void __launch_bounds__(32 * tma_warps<NT>(), GATHER ? 2 : 0)
+// no minimum given; the gather and fused instantiations are held to two
+// blocks per SM.)
+template <int BITS, int NT, bool OUT_BF16, bool GATHER, int FUSE>
+__global__ void __launch_bounds__(32 * tma_warps<NT>(), GATHER || FUSE ? 2 : 0)
 gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayout L,
-                  unsigned *err, GatherArgs ga) {
+                  unsigned *err, GatherArgs ga, const __grid_constant__ CUtensorMap wmap2,
+                  FuseArgs fa) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -475,6 +492,15 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
   const int nchunks = ncodes >> 7;
   // The block's weight rows start at wrow0 (its weight batch's first row in
   // the tensor map); it computes `rows` rows of x from xbase into ybase.
+  const CUtensorMap *map = &wmap;
+  if constexpr (FUSE == kFuseDual) {
+    if (blockIdx.z == 1) {
+      map = &wmap2;
+      a.scales = fa.scales2;
+      a.biases = fa.biases2;
+      a.y = fa.y2;
+    }
+  }
   int wrow0 = 0, rows = a.M;
   const uint16_t *xbase = a.x;
   char *ybase = static_cast<char *>(a.y);
@@ -525,7 +551,7 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
       asm volatile(
           "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
           " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem + c * L.box_bytes)),
-          "l"(&wmap), "r"(xw), "r"(wrow0 + n0), "r"(smem_u32(&bars[c]))
+          "l"(map), "r"(xw), "r"(wrow0 + n0), "r"(smem_u32(&bars[c]))
           : "memory");
     }
   }
@@ -557,6 +583,33 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
   // its own 32 x values per chunk (L2-resident: every block reads the same x),
   // natural pairs like the weights.
   griddep_wait();
+  if constexpr (FUSE == kFuseSilu) {
+    // x = silu(gate) * up for this block's K range, rounded once to bf16, into
+    // shared memory (rows of L.xpitch bytes); the lanes read it from there.
+    // gate and up may be written by the previous kernel: after the wait.
+    const int per_row = ncodes >> 3;  // 8 values per step
+    for (int i = threadIdx.x; i < a.M * per_row; i += blockDim.x) {
+      const int m = i / per_row, q = i - m * per_row;
+      const int64_t gofs = static_cast<int64_t>(m) * a.K + k0 + 8 * q;
+      const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(fa.gate + gofs));
+      const uint4 uv = __ldg(reinterpret_cast<const uint4 *>(fa.up + gofs));
+      const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float r[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float gf = bf16_bits_to_f32((gw[j] >> (16 * h)) & 0xFFFFu);
+          const float uf = bf16_bits_to_f32((uw[j] >> (16 * h)) & 0xFFFFu);
+          r[h] = __fdividef(gf, 1.0f + __expf(-gf)) * uf;
+        }
+        o[j] = pack_bf16x2(r[0], r[1]);
+      }
+      *reinterpret_cast<uint4 *>(smem + L.x_off + m * L.xpitch + 16 * q) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    __syncthreads();
+  }
   bool ok = true;
   // One pass computes mrows <= 8 * NT rows of x, from xc, into yc.
   auto pass = [&](const uint16_t *xc, void *yc, int mrows) {
@@ -570,11 +623,13 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
       for (int nt = 0; nt < NT; ++nt) {
         const int m = g + 8 * nt;
         if (m < ac.M) {
-          const uint4 *xp = reinterpret_cast<const uint4 *>(
-              ac.x + static_cast<int64_t>(m) * a.K + k0 + (c << 7) + 32 * t);
+          const uint4 *xp =
+              FUSE == kFuseSilu
+                  ? reinterpret_cast<const uint4 *>(smem + L.x_off + m * L.xpitch + ((c << 7) + 32 * t) * 2)
+                  : reinterpret_cast<const uint4 *>(ac.x + static_cast<int64_t>(m) * a.K + k0 + (c << 7) + 32 * t);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const uint4 u = __ldg(xp + i);
+            const uint4 u = FUSE == kFuseSilu ? xp[i] : __ldg(xp + i);
             xv[nt][4 * i] = u.x; xv[nt][4 * i + 1] = u.y; xv[nt][4 * i + 2] = u.z; xv[nt][4 * i + 3] = u.w;
           }
         }
@@ -761,8 +816,9 @@ cudaError_t launch_t(const GemvArgs &a0, const Batches &b, cudaStream_t stream) 
   });
 }
 
-template <int BITS, int NT, bool OUT_BF16, bool GATHER>
-cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, const Batches &b, cudaStream_t stream) {
+template <int BITS, int NT, bool OUT_BF16, bool GATHER, int FUSE = kFuseNone>
+cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, const Batches &b, cudaStream_t stream,
+                         const FuseArgs &f = FuseArgs{}, const uint32_t *w2 = nullptr) {
   const int64_t tiles = (a.N + 15) / 16;
   const int box_bytes = 16 * 16 * BITS;
   auto kr_of = [&](int c) { return ((a.K / c + 127) / 128) * 128; };
@@ -782,11 +838,14 @@ cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, const Batches &b, cudaStre
   L.kr = kr_of(C);
   L.box_bytes = box_bytes;
   const int nch = L.kr / 128;
-  L.x_off = nch * box_bytes;  // x is read from global memory by each lane
-  L.xpitch = 0;
-  L.red_off = L.x_off;
+  // x is read from global memory by each lane, or (silu) from the rows the
+  // block forms in shared memory.
+  L.x_off = nch * box_bytes;
+  L.xpitch = FUSE == kFuseSilu ? L.kr * 2 + 16 : 0;
+  L.red_off = L.x_off + a.M * L.xpitch;
   L.bar_off = L.red_off + tma_warps<NT>() * NT * 4 * 32 * 4;
   const size_t smem = L.bar_off + 8 * (nch + 1) + 1024;  // + slack for the 1024-byte base
+  if (smem > 220 * 1024) return cudaErrorNotSupported;
   // The tensor map spans every weight batch: batch e's row n is row e*N + n.
   const uint64_t map_rows = static_cast<uint64_t>(a.N) * (GATHER ? b.g.w_batches : 1);
   if (map_rows >= (uint64_t(1) << 31)) return cudaErrorNotSupported;
@@ -796,16 +855,23 @@ cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, const Batches &b, cudaStre
                                 static_cast<uint64_t>(a.K) * BITS / 8, 4 * BITS, 16,
                                 BITS == 8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
+  CUtensorMap wmap2 = wmap;
+  if (FUSE == kFuseDual) {
+    e = encode_map_2d(&wmap2, CU_TENSOR_MAP_DATA_TYPE_UINT32, w2, static_cast<uint64_t>(a.K) * BITS / 32,
+                      map_rows, static_cast<uint64_t>(a.K) * BITS / 8, 4 * BITS, 16,
+                      BITS == 8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+  }
   unsigned *err = device_error_word();
   if (!err) return cudaErrorInvalidSymbol;
-  auto kern = gemv_t_tma_kernel<BITS, NT, OUT_BF16, GATHER>;
+  auto kern = gemv_t_tma_kernel<BITS, NT, OUT_BF16, GATHER, FUSE>;
   if (smem > 48 * 1024) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
   return over_z(b, [&](const GatherArgs &g, unsigned nz) {
     return launch_ex(kern, dim3(static_cast<unsigned>(tiles), C, nz), dim3(32 * tma_warps<NT>()),
-                     smem, C, pdl, stream, wmap, a, L, err, g);
+                     smem, C, pdl, stream, wmap, a, L, err, g, wmap2, f);
   });
 }
 
@@ -896,7 +962,76 @@ cudaError_t launch_gather_bits(const GemvArgs &a0, const Batches &b0, bool trans
   return cudaSuccess;
 }
 
+// The fused decode GEMVs: transposed W, K a multiple of 128; dual for
+// M <= 16, silu for M <= 8.
+template <int BITS>
+cudaError_t launch_fused_bits(const GemvArgs &a, int fuse, const FuseArgs &f, const uint32_t *w2,
+                              bool y_bf16, bool pdl, cudaStream_t stream) {
+  if (fuse == kFuseDual) {
+    Batches two;
+    two.count = 2;
+    if (a.M <= 8)
+      return y_bf16 ? launch_t_tma<BITS, 1, true, false, kFuseDual>(a, pdl, two, stream, f, w2)
+                    : launch_t_tma<BITS, 1, false, false, kFuseDual>(a, pdl, two, stream, f, w2);
+    return y_bf16 ? launch_t_tma<BITS, 2, true, false, kFuseDual>(a, pdl, two, stream, f, w2)
+                  : launch_t_tma<BITS, 2, false, false, kFuseDual>(a, pdl, two, stream, f, w2);
+  }
+  const Batches one;
+  return y_bf16 ? launch_t_tma<BITS, 1, true, false, kFuseSilu>(a, pdl, one, stream, f)
+                : launch_t_tma<BITS, 1, false, false, kFuseSilu>(a, pdl, one, stream, f);
+}
+
+cudaError_t launch_fused(const GemvArgs &a, int bits, int fuse, const FuseArgs &f,
+                         const uint32_t *w2, bool y_bf16, cudaStream_t stream) {
+  const bool pdl = (launch_flags() & kLaunchPdl) != 0;
+  switch (bits) {
+    case 1: return launch_fused_bits<1>(a, fuse, f, w2, y_bf16, pdl, stream);
+    case 2: return launch_fused_bits<2>(a, fuse, f, w2, y_bf16, pdl, stream);
+    case 3: return launch_fused_bits<3>(a, fuse, f, w2, y_bf16, pdl, stream);
+    case 4: return launch_fused_bits<4>(a, fuse, f, w2, y_bf16, pdl, stream);
+    case 5: return launch_fused_bits<5>(a, fuse, f, w2, y_bf16, pdl, stream);
+    case 6: return launch_fused_bits<6>(a, fuse, f, w2, y_bf16, pdl, stream);
+    case 8: return launch_fused_bits<8>(a, fuse, f, w2, y_bf16, pdl, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+GemvArgs transposed_args(const uint16_t *x, int64_t M, const PackedWeight &w, void *y) {
+  GemvArgs a;
+  a.x = x;
+  a.w = w.w;
+  a.scales = w.scales;
+  a.biases = w.biases;
+  a.y = y;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(w.rows);
+  a.K = static_cast<int>(w.cols);
+  a.group_shift = w.group == 32 ? 5 : w.group == 64 ? 6 : 7;
+  a.parts = 1;
+  a.resid = nullptr;
+  return a;
+}
+
 }  // namespace
+
+cudaError_t launch_gate_up(const uint16_t *x, int64_t M, const PackedWeight &gate,
+                           const PackedWeight &up, void *y_gate, void *y_up, bool y_bf16,
+                           cudaStream_t stream) {
+  if (gate.cols % 128 != 0 || M > 16) return cudaErrorNotSupported;
+  GemvArgs a = transposed_args(x, M, gate, y_gate);
+  FuseArgs f{up.scales, up.biases, y_up, nullptr, nullptr};
+  return launch_fused(a, gate.bits, kFuseDual, f, up.w, y_bf16, stream);
+}
+
+cudaError_t launch_silu_gate(const uint16_t *gate, const uint16_t *up, int64_t M,
+                             const PackedWeight &w, const uint16_t *resid, void *y, bool y_bf16,
+                             cudaStream_t stream) {
+  if (w.cols % 128 != 0 || M > 8) return cudaErrorNotSupported;
+  GemvArgs a = transposed_args(nullptr, M, w, y);
+  a.resid = resid;
+  FuseArgs f{nullptr, nullptr, nullptr, gate, up};
+  return launch_fused(a, w.bits, kFuseSilu, f, nullptr, y_bf16, stream);
+}
 
 cudaError_t launch_gemv(const uint16_t *x, int64_t M, const PackedWeight &w, bool transpose,
                         void *y, bool y_bf16, cudaStream_t stream) {
@@ -911,6 +1046,7 @@ cudaError_t launch_gemv(const uint16_t *x, int64_t M, const PackedWeight &w, boo
   a.K = static_cast<int>(transpose ? w.cols : w.rows);
   a.group_shift = w.group == 32 ? 5 : w.group == 64 ? 6 : 7;
   a.parts = 1;
+  a.resid = nullptr;
   const bool pdl = (launch_flags() & kLaunchPdl) != 0;
   switch (w.bits) {
     case 1: return launch_bits<1>(a, transpose, y_bf16, pdl, stream);
@@ -939,6 +1075,7 @@ cudaError_t launch_gather(const uint16_t *x, int64_t x_batches, int64_t M, const
   a.K = static_cast<int>(transpose ? w.cols : w.rows);
   a.group_shift = w.group == 32 ? 5 : w.group == 64 ? 6 : 7;
   a.parts = 1;
+  a.resid = nullptr;
   Batches b;
   b.g.lhs = lhs;
   b.g.rhs = rhs;

@@ -62,6 +62,17 @@ cudaError_t launch_gather(const uint16_t *x, int64_t x_batches, int64_t M, const
                           int64_t batches, bool transpose, bool sorted, void *y, bool y_bf16,
                           cudaStream_t stream);
 
+// Fused decode GEMVs on a transposed W ([N, K], K a multiple of 128):
+// y_gate = x . gate^T and y_up = x . up^T in one launch (M <= 16; the two
+// weights share N, K, bits and group size); y = silu(gate) * up . w^T (+ resid,
+// bf16 [M, N], when not null) with M <= 8.  cudaErrorNotSupported otherwise.
+cudaError_t launch_gate_up(const uint16_t *x, int64_t M, const PackedWeight &gate,
+                           const PackedWeight &up, void *y_gate, void *y_up, bool y_bf16,
+                           cudaStream_t stream);
+cudaError_t launch_silu_gate(const uint16_t *gate, const uint16_t *up, int64_t M,
+                             const PackedWeight &w, const uint16_t *resid, void *y, bool y_bf16,
+                             cudaStream_t stream);
+
 // The variant of launch_gemm whose split-K partials go to `scratch` (the
 // library's static array, see static_scratch) instead of a stream-ordered
 // allocation.  *needed gets the partials' bytes; cudaErrorInvalidValue, with

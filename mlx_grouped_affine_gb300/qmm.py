@@ -15,8 +15,8 @@ STATUS_NAMES = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED",
                 3: "QMM_ERR_CUDA", 4: "QMM_ERR_INDEX", 5: "QMM_ERR_TIMEOUT"}
 QMM_LAUNCH_PDL = 1
 EXPORTS = ("qmm_dequantize", "qmm_quantized_matmul", "qmm_quantized_matmul_noalloc",
-           "qmm_gather_qmm", "qmm_rows", "qmm_last_error", "qmm_get_device_error",
-           "qmm_set_launch_flags")
+           "qmm_gather_qmm", "qmm_gemv_gate_up", "qmm_gemv_silu_gate", "qmm_rows",
+           "qmm_last_error", "qmm_get_device_error", "qmm_set_launch_flags")
 
 _lib = None
 
@@ -38,10 +38,13 @@ def lib():
         L.qmm_quantized_matmul.argtypes = [P, I64, P, P, P, I64, I64, I, I, I, P, I, P]
         L.qmm_quantized_matmul_noalloc.argtypes = [P, I64, P, P, P, I64, I64, I, I, I, P, I, P]
         L.qmm_gather_qmm.argtypes = [P, I64, I64, P, P, P, I64, I64, I64, P, P, I64, I, I, I, I, P, I, P]
+        L.qmm_gemv_gate_up.argtypes = [P, I64, P, P, P, P, P, P, I64, I64, I, I, P, P, I, P]
+        L.qmm_gemv_silu_gate.argtypes = [P, P, I64, P, P, P, I64, I64, I, I, P, P, I, P]
         L.qmm_rows.argtypes = [P, P, P, I64, I64, P, I64, I, I, P, I, P]
         L.qmm_get_device_error.argtypes = [P]
         for f in ("qmm_dequantize", "qmm_quantized_matmul", "qmm_quantized_matmul_noalloc",
-                  "qmm_gather_qmm", "qmm_rows", "qmm_get_device_error"):
+                  "qmm_gather_qmm", "qmm_gemv_gate_up", "qmm_gemv_silu_gate", "qmm_rows",
+                  "qmm_get_device_error"):
             getattr(L, f).restype = I
         L.qmm_set_launch_flags.argtypes = [ctypes.c_uint]
         L.qmm_set_launch_flags.restype = ctypes.c_uint
@@ -106,6 +109,20 @@ def qmm_gather_qmm(x, x_batches, M, w, scales, biases, w_batches, N, K, lhs_indi
                                 w_batches, N, K, _ptr(lhs_indices), _ptr(rhs_indices), batches,
                                 int(transpose), group_size, bits, int(sorted_indices), _ptr(y),
                                 y_dtype, _stream(stream)))
+
+
+def qmm_gemv_gate_up(x, M, w_gate, scales_gate, biases_gate, w_up, scales_up, biases_up, N, K,
+                     group_size, bits, y_gate, y_up, y_dtype, stream=None):
+    _check(lib().qmm_gemv_gate_up(_ptr(x), M, _ptr(w_gate), _ptr(scales_gate), _ptr(biases_gate),
+                                  _ptr(w_up), _ptr(scales_up), _ptr(biases_up), N, K, group_size,
+                                  bits, _ptr(y_gate), _ptr(y_up), y_dtype, _stream(stream)))
+
+
+def qmm_gemv_silu_gate(gate, up, M, w, scales, biases, N, K, group_size, bits, resid, y, y_dtype,
+                       stream=None):
+    _check(lib().qmm_gemv_silu_gate(_ptr(gate), _ptr(up), M, _ptr(w), _ptr(scales), _ptr(biases),
+                                    N, K, group_size, bits, _ptr(resid), _ptr(y), y_dtype,
+                                    _stream(stream)))
 
 
 def qmm_rows(w, scales, biases, table_rows, cols, idx, n, group_size, bits, out, out_dtype,
