@@ -302,6 +302,63 @@ def gather_detail(torch, qmm, synth, peaks, warmup):
     return out
 
 
+def fused_detail(torch, qmm, synth, peaks, warmup):
+    """The fused decode GEMVs of an 8B-class gated feed-forward block at M=1,
+    4-bit g64, each against the unfused calls it replaces: gate_up (two
+    [14336, 4096] weights, one x) and silu_gate with the residual (down
+    projection [4096, 14336]).  GB/s counts weights + inputs + outputs; rotating
+    weight copies keep every launch on HBM; programmatic dependent launch on."""
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(
+        {np.dtype(np.uint32): np.int32, np.dtype(np.uint16): np.int16}[a.dtype])).cuda()
+    out = {}
+    flags = qmm.qmm_set_launch_flags(qmm.QMM_LAUNCH_PDL)
+    N, K = 14336, 4096
+    base_g, base_u = synth.quant_weight(130, N, K, 4, 64), synth.quant_weight(131, N, K, 4, 64)
+    R = max(2, -(-3 * L2_BYTES // (2 * base_g.nbytes)))
+    ws = [tuple(dev(np.roll(a, r, 0)) for w in (base_g, base_u) for a in (w.packed, w.scales, w.biases))
+          for r in range(R)]
+    x = dev(synth.x_bf16(132, 1, K))
+    yg = torch.empty((R, 1, N), dtype=torch.int16, device="cuda")
+    yu = torch.empty_like(yg)
+    nbytes = 2 * base_g.nbytes + 2 * K + 4 * N
+
+    def fused():
+        for r in range(R):
+            qmm.qmm_gemv_gate_up(x, 1, *ws[r], N, K, 64, 4, yg[r], yu[r], qmm.QMM_BF16)
+
+    def unfused():
+        for r in range(R):
+            pg, sg, bg, pu, su, bu = ws[r]
+            qmm.qmm_quantized_matmul(x, 1, pg, sg, bg, N, K, 1, 64, 4, yg[r], qmm.QMM_BF16)
+            qmm.qmm_quantized_matmul(x, 1, pu, su, bu, N, K, 1, 64, 4, yu[r], qmm.QMM_BF16)
+    for name, fn in (("gemv_gate_up_2x%dx%d_b4_M1" % (N, K), fused),
+                     ("gemv_gate_up_unfused_2x%dx%d_b4_M1" % (N, K), unfused)):
+        t = time_graph(torch, graph_of(torch, fn), 200, warmup) / R
+        out[name] = {"us": round(t * 1e3, 2), "GB/s": round(nbytes / (t * 1e-3) / 1e9, 1),
+                     "frac_hbm": round(nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
+    del ws, yg, yu
+    N, K = 4096, 14336
+    base = synth.quant_weight(133, N, K, 4, 64)
+    R = max(2, -(-3 * L2_BYTES // base.nbytes))
+    ws = [tuple(dev(np.roll(a, r, 0)) for a in (base.packed, base.scales, base.biases)) for r in range(R)]
+    gate, up = dev(synth.x_bf16(134, 1, K)), dev(synth.x_bf16(135, 1, K))
+    resid = dev(synth.x_bf16(136, 1, N))
+    y = torch.empty((R, 1, N), dtype=torch.int16, device="cuda")
+    nbytes = base.nbytes + 4 * K + 4 * N
+
+    def fused_silu():
+        for r in range(R):
+            qmm.qmm_gemv_silu_gate(gate, up, 1, *ws[r], N, K, 64, 4, resid, y[r], qmm.QMM_BF16)
+    t = time_graph(torch, graph_of(torch, fused_silu), 200, warmup) / R
+    out["gemv_silu_gate_resid_%dx%d_b4_M1" % (N, K)] = {
+        "us": round(t * 1e3, 2), "GB/s": round(nbytes / (t * 1e-3) / 1e9, 1),
+        "frac_hbm": round(nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
+    qmm.qmm_set_launch_flags(flags)
+    del ws, y
+    torch.cuda.empty_cache()
+    return out
+
+
 def measured_traffic():
     """DRAM bytes per launch of the decode kernel from the committed ncu capture,
     or None if the kernel source changed since it was taken."""
@@ -434,6 +491,7 @@ def run_gpu(args):
                 torch.cuda.empty_cache()
         detail.update(sweep_detail(torch, qmm, synth, peaks, args.warmup))
         detail.update(gather_detail(torch, qmm, synth, peaks, args.warmup))
+        detail.update(fused_detail(torch, qmm, synth, peaks, args.warmup))
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
