@@ -57,6 +57,7 @@ def _load():
         lib.oracle_qmm.argtypes = [P, I64, P, P, P, I64, I64, I, I, I, P, P, I]
         lib.oracle_qmm_sampled.argtypes = [P, I64, P, P, P, I64, I64, I, I, I,
                                            P, P, I64, P, P, I]
+        lib.oracle_quantize.argtypes = [P, I64, I64, I, I, P, P, P, I]
         _lib = lib
     return _lib
 
@@ -203,6 +204,20 @@ def silu_gate_qmm(gate, up, M, packed, scales, biases, N, K, group_size, bits, r
 
 def _bf16_f64(h):
     return (np.asarray(h, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def quantize(w, rows, cols, group_size, bits, nthreads=None):
+    """(packed, scales, biases) of bf16 w [rows, cols]; see oracle_quantize in
+    qmm_oracle.c for the rule and its readings."""
+    w, pw = _c(w, np.uint16)
+    packed = np.empty((rows, cols * bits // 32), dtype=np.uint32)
+    scales = np.empty((rows, cols // group_size), dtype=np.uint16)
+    biases = np.empty((rows, cols // group_size), dtype=np.uint16)
+    _load().oracle_quantize(pw, rows, cols, group_size, bits,
+                            packed.ctypes.data_as(ctypes.c_void_p),
+                            scales.ctypes.data_as(ctypes.c_void_p),
+                            biases.ctypes.data_as(ctypes.c_void_p), nthreads or default_threads())
+    return packed, scales, biases
 
 
 def qmm_sampled(x, M, packed, scales, biases, N, K, transpose, group_size, bits,

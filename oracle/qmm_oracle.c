@@ -338,3 +338,76 @@ int oracle_qmm_sampled(const uint16_t *x, int64_t M, const uint32_t *packed,
     parallel_for(count, nthreads, qmm_samples_range, &c);
     return 0;
 }
+
+/* ------------------------------------------------------------ quantize --- */
+/*
+ * quantize (nuvec_core quantized.rs, module doc: a value w is stored as
+ * round((w - bias) / scale), clamped to [0, 2^bits - 1]; `dequantize` doc:
+ * bias = the group minimum).  The pages do not give the scale; the reading
+ * taken here is the plain min-max one: scale = (max - min) / (2^bits - 1),
+ * in fp32, stored as its round-to-nearest-even bf16, and the codes come from
+ * the stored (bf16) scale and bias, each step one IEEE fp32 operation, the
+ * round half to even (rintf).  A zero scale (a constant group) gives every
+ * code 0, so that the group dequantizes to its value exactly.
+ * Input w: bf16 [rows, cols]; outputs as the packed format above.
+ */
+typedef struct {
+    const uint16_t *w;
+    int64_t rows, cols;
+    int group_size, bits;
+    uint32_t *packed;
+    uint16_t *scales, *biases;
+} quant_ctx;
+
+static void quant_rows_range(void *arg, int64_t begin, int64_t end)
+{
+    quant_ctx *c = (quant_ctx *)arg;
+    int64_t groups = c->cols / c->group_size;
+    uint32_t top = (1u << c->bits) - 1u;
+    uint8_t *codes = (uint8_t *)malloc((size_t)c->cols);
+    for (int64_t r = begin; r < end; ++r) {
+        const uint16_t *row = c->w + r * c->cols;
+        for (int64_t g = 0; g < groups; ++g) {
+            const uint16_t *v = row + g * c->group_size;
+            float lo = oracle_bf16_to_f32(v[0]), hi = lo;
+            for (int i = 1; i < c->group_size; ++i) {
+                float f = oracle_bf16_to_f32(v[i]);
+                if (f < lo)
+                    lo = f;
+                if (f > hi)
+                    hi = f;
+            }
+            float range = hi - lo;
+            float scale_f32 = range / (float)top;
+            uint16_t sb = oracle_f32_to_bf16(scale_f32);
+            uint16_t bb = oracle_f32_to_bf16(lo); /* exact: lo is a bf16 value */
+            c->scales[r * groups + g] = sb;
+            c->biases[r * groups + g] = bb;
+            float s = oracle_bf16_to_f32(sb), b = oracle_bf16_to_f32(bb);
+            for (int i = 0; i < c->group_size; ++i) {
+                uint32_t code = 0;
+                if (s != 0.0f) {
+                    float d = oracle_bf16_to_f32(v[i]) - b;
+                    float q = rintf(d / s);
+                    if (q < 0.0f)
+                        q = 0.0f;
+                    if (q > (float)top)
+                        q = (float)top;
+                    code = (uint32_t)q;
+                }
+                codes[g * c->group_size + i] = (uint8_t)code;
+            }
+        }
+        oracle_pack(codes, 1, c->cols, c->bits,
+                    c->packed + r * oracle_words_per_row(c->cols, c->bits));
+    }
+    free(codes);
+}
+
+void oracle_quantize(const uint16_t *w, int64_t rows, int64_t cols, int group_size,
+                     int bits, uint32_t *packed, uint16_t *scales, uint16_t *biases,
+                     int nthreads)
+{
+    quant_ctx c = {w, rows, cols, group_size, bits, packed, scales, biases};
+    parallel_for(rows, nthreads, quant_rows_range, &c);
+}

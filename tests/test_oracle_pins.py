@@ -343,3 +343,72 @@ def test_silu_gate_matches_scipy_expit_route(bits):
     x = g * special.expit(g) * bf16_f64(up)
     want = x @ np_dense_f64(w).T + bf16_f64(resid)
     np.testing.assert_allclose(y, want, rtol=1e-12, atol=1e-12)
+
+
+# -- quantize -------------------------------------------------------------------
+
+def _doctest_weight():
+    # the module doctest's weight: w[r, c] = (64 r + c) / 64, [4, 64]
+    rows, cols = 4, 64
+    f = (np.arange(rows * cols, dtype=np.float32) / 64.0).reshape(rows, cols)
+    return (f.view(np.uint32) >> 16).astype(np.uint16), rows, cols
+
+
+def test_quantize_doctest_shapes():
+    g = load_golden("pack_shape.txt")
+    w, rows, cols = _doctest_weight()
+    assert [rows, cols] == ints(g["weight_shape"])
+    bits = int(g["bits"][0])
+    packed, s, b = oracle.quantize(w, rows, cols, 64, bits)
+    assert list(packed.shape) == ints(g["packed_shape"])
+    assert s.shape == b.shape == (rows, 1)
+
+
+@pytest.mark.parametrize("bits", ALL_BITS)
+@pytest.mark.parametrize("gs", (32, 128))
+def test_quantize_codes_follow_the_stated_rule(bits, gs):
+    # round((w - bias) / scale) clamped to [0, 2^bits - 1], with the oracle's
+    # scales and biases, recomputed with numpy float32 and numpy's unpacker;
+    # the bias is the group minimum, the group minimum gets code 0 and the
+    # group maximum code 2^bits - 1.
+    rows, cols = 6, 256
+    w = synth.x_bf16(940 + bits, rows, cols)
+    packed, s, b = oracle.quantize(w, rows, cols, gs, bits)
+    wf = bf16_f64(w).astype(np.float32).reshape(rows, cols // gs, gs)
+    sf = bf16_f64(s).astype(np.float32)[:, :, None]
+    bf = bf16_f64(b).astype(np.float32)[:, :, None]
+    assert (bf[:, :, 0] == wf.min(axis=2)).all()
+    top = (1 << bits) - 1
+    want = np.clip(np.rint((wf - bf) / sf), 0, top).astype(np.uint32).reshape(rows, cols)
+    got = np_codes(packed, cols, bits)
+    assert (got == want).all()
+    g3 = got.reshape(rows, cols // gs, gs)
+    assert (g3[wf == wf.min(axis=2, keepdims=True)] == 0).all()
+    # The bf16 scale is within 2^-9 of (max - min) / top, so the maximum lands
+    # within top * 2^-9 of top: exactly top below 8 bits, top or top - 1 at 8.
+    slack = 1 if bits == 8 else 0
+    assert (g3[wf == wf.max(axis=2, keepdims=True)] >= top - slack).all()
+
+
+@pytest.mark.parametrize("bits", ALL_BITS)
+def test_quantize_round_trip_within_half_a_step(bits):
+    rows, cols, gs = 5, 128, 64
+    w = synth.x_bf16(950 + bits, rows, cols)
+    packed, s, b = oracle.quantize(w, rows, cols, gs, bits)
+    back = oracle.dequantize(packed, s, b, rows, cols, gs, bits).astype(np.float64)
+    step = np.repeat(bf16_f64(s), gs, axis=1)
+    # half a step, plus the clamp at the top code: the bf16 scale's relative
+    # error 2^-9 over the 2^bits - 1 steps of the range
+    top = (1 << bits) - 1
+    bound = 0.5 * step * (1 + 1e-3) + top * 2.0 ** -9 * step + 1e-6
+    assert (np.abs(back - bf16_f64(w)) <= bound).all()
+
+
+def test_quantize_constant_groups_are_exact():
+    rows, cols, gs = 3, 64, 32
+    vals = np.array([0.0, 1.0, -2.5], dtype=np.float32)
+    w = np.repeat((vals.view(np.uint32) >> 16).astype(np.uint16)[:, None], cols, axis=1)
+    packed, s, b = oracle.quantize(w, rows, cols, gs, 4)
+    assert (s == 0).all() and (packed == 0).all()
+    back = oracle.dequantize(packed, s, b, rows, cols, gs, 4)
+    assert (back == vals[:, None]).all()
