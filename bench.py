@@ -199,6 +199,23 @@ def dequant_rows_detail(torch, qmm, synth, peaks, steps, warmup):
             "us": round(t * 1e3, 2), "GB/s": round(nbytes / (t * 1e-3) / 1e9, 1),
             "frac_hbm": round(nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
         del copies, o
+    # quantize: bf16 [N, K] read, packed codes + bf16 scales and biases written
+    wsrc = [dev(synth.x_bf16(45 + r, N, K)) for r in range(2)]
+    for bits in (4, 8):
+        p = torch.empty((2, N, K * bits // 32), dtype=torch.int32, device="cuda")
+        sc = torch.empty((2, N, K // 64), dtype=torch.int16, device="cuda")
+        bi = torch.empty_like(sc)
+
+        def fn():
+            for r in range(2):
+                qmm.qmm_quantize(wsrc[r], N, K, 64, bits, p[r], sc[r], bi[r])
+        t = time_graph(torch, graph_of(torch, fn), steps, warmup) / 2
+        nbytes = 2 * N * K + N * K * bits // 8 + 4 * N * (K // 64)
+        out["quantize_b%d_%dx%d_bf16" % (bits, N, K)] = {
+            "us": round(t * 1e3, 2), "GB/s": round(nbytes / (t * 1e-3) / 1e9, 1),
+            "frac_hbm": round(nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
+        del p, sc, bi
+    del wsrc
     T, C = synth.ROWS_TABLE
     w = synth.quant_weight(2, T, C, 4, 64)
     pw, ps, pb = dev(w.packed), dev(w.scales), dev(w.biases)

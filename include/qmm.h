@@ -83,6 +83,29 @@ qmm_status qmm_dequantize(const uint32_t *w, const uint16_t *scales,
                           qmm_dtype out_dtype, qmm_stream_t stream);
 
 /*
+ * qmm_quantize -- packed codes, scales and biases of a bf16 weight, in the
+ * format above.  (nuvec_core quantized.rs, module doc: a value w is stored as
+ * round((w - bias) / scale), clamped to [0, 2^bits - 1]; `dequantize` doc:
+ * bias = the group minimum.)
+ *
+ *   w       bf16 [rows, cols]
+ *   packed  uint32 [rows, cols*bits/32]
+ *   scales  bf16   [rows, cols/group_size]
+ *   biases  bf16   [rows, cols/group_size]
+ *
+ * Per group: bias = the minimum (exact); scale = (max - min) / (2^bits - 1)
+ * in fp32, rounded to nearest even bf16 (the pages do not give the scale:
+ * this is the plain min-max reading, not a claim of MLX's exact rounding);
+ * code = round half to even of (w - bias) / scale with the stored bf16 scale
+ * and bias, each step one IEEE fp32 operation, clamped.  A zero scale gives
+ * every code 0.  Rules: bits and group_size as above; cols > 0 and a multiple
+ * of group_size; rows >= 0.
+ */
+qmm_status qmm_quantize(const uint16_t *w, int64_t rows, int64_t cols, int group_size, int bits,
+                        uint32_t *packed, uint16_t *scales, uint16_t *biases,
+                        qmm_stream_t stream);
+
+/*
  * qmm_quantized_matmul -- y = x . dequant(W)^T (transpose = 1) or
  * y = x . dequant(W) (transpose = 0), without materialising dequant(W).
  * (nuvec_core quantized.rs, `quantized_matmul`; maya2_mlx quant.py, `mm`,

@@ -211,6 +211,25 @@ qmm_status qmm_gather_qmm(const uint16_t *x, int64_t x_batches, int64_t M, const
   return cuda_status(e, op);
 }
 
+qmm_status qmm_quantize(const uint16_t *w, int64_t rows, int64_t cols, int group_size, int bits,
+                        uint32_t *packed, uint16_t *scales, uint16_t *biases,
+                        qmm_stream_t stream) {
+  const char *op = "qmm_quantize";
+  qmm_status st;
+  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
+  if (rows < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative row count %lld", op, (long long)rows);
+  if (cols <= 0 || cols % group_size != 0)
+    return fail(QMM_ERR_INVALID_ARG, "%s: cols (%lld) must be a positive multiple of group_size %d",
+                op, (long long)cols, group_size);
+  if (rows == 0) return QMM_OK;
+  if (!w || !aligned16(w) || !packed || !aligned16(packed) || !scales || !aligned16(scales) ||
+      !biases || !aligned16(biases))
+    return fail(QMM_ERR_INVALID_ARG, "%s: every pointer must be non-null and 16-byte aligned", op);
+  return cuda_status(qmm::launch_quantize(w, rows, cols, group_size, bits, packed, scales, biases,
+                                          reinterpret_cast<cudaStream_t>(stream)),
+                     op);
+}
+
 // Checks shared by the fused decode GEMVs: a transposed weight [N, K] with K
 // a multiple of 128, 1 <= M <= max_m.
 static qmm_status check_fused(const char *op, int64_t M, int64_t max_m, const uint32_t *w,

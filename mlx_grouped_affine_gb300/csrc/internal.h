@@ -73,6 +73,12 @@ cudaError_t launch_silu_gate(const uint16_t *gate, const uint16_t *up, int64_t M
                              const PackedWeight &w, const uint16_t *resid, void *y, bool y_bf16,
                              cudaStream_t stream);
 
+// quantize: bf16 w [rows, cols] (cols a multiple of group) -> packed
+// uint32 [rows, cols*bits/32], bf16 scales and biases [rows, cols/group].
+cudaError_t launch_quantize(const uint16_t *w, int64_t rows, int64_t cols, int group, int bits,
+                            uint32_t *packed, uint16_t *scales, uint16_t *biases,
+                            cudaStream_t stream);
+
 // The variant of launch_gemm whose split-K partials go to `scratch` (the
 // library's static array, see static_scratch) instead of a stream-ordered
 // allocation.  *needed gets the partials' bytes; cudaErrorInvalidValue, with

@@ -14,7 +14,7 @@ QMM_F32, QMM_BF16 = 0, 1
 STATUS_NAMES = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED",
                 3: "QMM_ERR_CUDA", 4: "QMM_ERR_INDEX", 5: "QMM_ERR_TIMEOUT"}
 QMM_LAUNCH_PDL = 1
-EXPORTS = ("qmm_dequantize", "qmm_quantized_matmul", "qmm_quantized_matmul_noalloc",
+EXPORTS = ("qmm_quantize", "qmm_dequantize", "qmm_quantized_matmul", "qmm_quantized_matmul_noalloc",
            "qmm_gather_qmm", "qmm_gemv_gate_up", "qmm_gemv_silu_gate", "qmm_rows",
            "qmm_last_error", "qmm_get_device_error", "qmm_set_launch_flags")
 
@@ -35,6 +35,7 @@ def lib():
         L = ctypes.CDLL(path)
         P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         L.qmm_dequantize.argtypes = [P, P, P, I64, I64, I, I, P, I, P]
+        L.qmm_quantize.argtypes = [P, I64, I64, I, I, P, P, P, P]
         L.qmm_quantized_matmul.argtypes = [P, I64, P, P, P, I64, I64, I, I, I, P, I, P]
         L.qmm_quantized_matmul_noalloc.argtypes = [P, I64, P, P, P, I64, I64, I, I, I, P, I, P]
         L.qmm_gather_qmm.argtypes = [P, I64, I64, P, P, P, I64, I64, I64, P, P, I64, I, I, I, I, P, I, P]
@@ -42,7 +43,7 @@ def lib():
         L.qmm_gemv_silu_gate.argtypes = [P, P, I64, P, P, P, I64, I64, I, I, P, P, I, P]
         L.qmm_rows.argtypes = [P, P, P, I64, I64, P, I64, I, I, P, I, P]
         L.qmm_get_device_error.argtypes = [P]
-        for f in ("qmm_dequantize", "qmm_quantized_matmul", "qmm_quantized_matmul_noalloc",
+        for f in ("qmm_quantize", "qmm_dequantize", "qmm_quantized_matmul", "qmm_quantized_matmul_noalloc",
                   "qmm_gather_qmm", "qmm_gemv_gate_up", "qmm_gemv_silu_gate", "qmm_rows",
                   "qmm_get_device_error"):
             getattr(L, f).restype = I
@@ -79,6 +80,11 @@ def _check(status):
 
 def qmm_last_error():
     return lib().qmm_last_error().decode()
+
+
+def qmm_quantize(w, rows, cols, group_size, bits, packed, scales, biases, stream=None):
+    _check(lib().qmm_quantize(_ptr(w), rows, cols, group_size, bits, _ptr(packed), _ptr(scales),
+                              _ptr(biases), _stream(stream)))
 
 
 def qmm_dequantize(w, scales, biases, rows, cols, group_size, bits, out, out_dtype,
