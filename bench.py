@@ -609,7 +609,63 @@ PROFILE_CASES = {
     "decode_m16": (16, 4096, 4096, 4, 64, True),
     "decode_b8": (1, 4096, 4096, 8, 64, True),
     "prefill": (2048, 14336, 4096, 4, 64, True),
+    "splitk_m128": (128, 4096, 4096, 4, 64, True),
 }
+OTHER_PROFILES = ("gather_sorted", "silu_gate", "quantize", "dequantize", "rows")
+
+
+def run_other_profile(case, launches):
+    """Eager launches of the non-matmul entry points for ncu (inputs > L2)."""
+    import torch
+    from mlx_grouped_affine_gb300 import qmm, synth
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(
+        {np.dtype(np.uint32): np.int32, np.dtype(np.uint16): np.int16}[a.dtype])).cuda()
+    if case == "gather_sorted":
+        E, N, K, B = 8, 14336, 4096, 32
+        ws = [synth.quant_weight(120 + e, N, K, 4, 64) for e in range(E)]
+        packed = dev(np.stack([w.packed for w in ws]))
+        sc, bi = dev(np.stack([w.scales for w in ws])), dev(np.stack([w.biases for w in ws]))
+        rhs = dev(np.sort(synth.indices(121, B, E)).astype(np.uint32))
+        x = dev(synth.x_bf16(122, B, K))
+        y = torch.empty((B, 1, N), dtype=torch.int16, device="cuda")
+        for _ in range(launches):
+            qmm.qmm_gather_qmm(x, B, 1, packed, sc, bi, E, N, K, None, rhs, B, 1, 64, 4, 1, y,
+                               qmm.QMM_BF16)
+    elif case == "silu_gate":
+        N, K, R = 4096, 14336, 6
+        base = synth.quant_weight(133, N, K, 4, 64)
+        ws = [tuple(dev(np.roll(a, r, 0)) for a in (base.packed, base.scales, base.biases))
+              for r in range(R)]
+        gate, up = dev(synth.x_bf16(134, 1, K)), dev(synth.x_bf16(135, 1, K))
+        resid = dev(synth.x_bf16(136, 1, N))
+        y = torch.empty((1, N), dtype=torch.int16, device="cuda")
+        for i in range(launches):
+            qmm.qmm_gemv_silu_gate(gate, up, 1, *ws[i % R], N, K, 64, 4, resid, y, qmm.QMM_BF16)
+    elif case == "quantize":
+        N, K, R = 14336, 4096, 2
+        src = [dev(synth.x_bf16(45 + r, N, K)) for r in range(R)]
+        p = torch.empty((N, K // 8), dtype=torch.int32, device="cuda")
+        sc = torch.empty((N, K // 64), dtype=torch.int16, device="cuda")
+        bi = torch.empty_like(sc)
+        for i in range(launches):
+            qmm.qmm_quantize(src[i % R], N, K, 64, 4, p, sc, bi)
+    elif case == "dequantize":
+        N, K, R = 14336, 4096, 2
+        w = synth.quant_weight(44, N, K, 4, 64)
+        cs = [tuple(dev(np.roll(a, r, 0)) for a in (w.packed, w.scales, w.biases)) for r in range(R)]
+        o = torch.empty((N, K), dtype=torch.int16, device="cuda")
+        for i in range(launches):
+            qmm.qmm_dequantize(*cs[i % R], N, K, 64, 4, o, qmm.QMM_BF16)
+    elif case == "rows":
+        T, C = synth.ROWS_TABLE
+        w = synth.quant_weight(2, T, C, 4, 64)
+        pw, ps, pb = dev(w.packed), dev(w.scales), dev(w.biases)
+        idx = dev(synth.indices(3, synth.ROWS_GATHER, T))
+        o = torch.empty((synth.ROWS_GATHER, C), dtype=torch.int16, device="cuda")
+        for _ in range(launches):
+            qmm.qmm_rows(pw, ps, pb, T, C, idx, synth.ROWS_GATHER, 64, 4, o, qmm.QMM_BF16)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": case, "launches": launches}))
 
 
 def run_profile(case, launches):
@@ -631,7 +687,7 @@ def run_profile(case, launches):
 
 def main():
     p = argparse.ArgumentParser()
-    p.add_argument("--profile", choices=sorted(PROFILE_CASES),
+    p.add_argument("--profile", choices=sorted(PROFILE_CASES) + sorted(OTHER_PROFILES),
                    help="run a few eager launches of one case (for ncu) and exit")
     p.add_argument("--launches", type=int, default=6)
     p.add_argument("--gpus", type=int, default=1)
@@ -646,7 +702,10 @@ def main():
                    help="total CPU time budget of the reference arm")
     args = p.parse_args()
     if args.profile:
-        run_profile(args.profile, args.launches)
+        if args.profile in OTHER_PROFILES:
+            run_other_profile(args.profile, args.launches)
+        else:
+            run_profile(args.profile, args.launches)
         return
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
