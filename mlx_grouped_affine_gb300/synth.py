@@ -7,7 +7,8 @@ path and the CPU oracle may use it.
 * Codes uniform on [0, 2^bits - 1] packed LSB-first into uint32 words are
   drawn as uniformly random words: every bit of the packed stream is an
   independent fair bit, which is exactly a row of independent uniform codes.
-* bf16 values are drawn in fp32 and keep their top 16 bits.
+* bf16 values are drawn in fp32 and keep their top 16 bits; fp16 values are
+  numpy's float16 conversion of the fp32 draws; fp32 values are the draws.
 * Scales are uniform on [lo, hi]; biases are -scale * 2^(bits-1) plus
   N(0, sigma) noise, so that dequantized weights are centred on zero.
 * x is N(0, 1) in bf16; row indices are uniform on [0, table_rows).
@@ -29,16 +30,30 @@ def _top16(values):
     return (v.view(np.uint32) >> 16).astype(np.uint16)
 
 
+def as_dtype(values, dtype):
+    """fp32 draws stored as dtype: "f32" float32 values, "bf16" the top 16
+    bits, "f16" the bit patterns of numpy's float16 conversion."""
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    if dtype == "f32":
+        return v
+    if dtype == "bf16":
+        return _top16(v)
+    if dtype == "f16":
+        return v.astype(np.float16).view(np.uint16)
+    raise ValueError(dtype)
+
+
 @dataclass
 class QuantWeight:
     """A packed weight: the packed codes, scales and biases, host arrays."""
     packed: np.ndarray   # uint32 [rows, cols*bits/32]
-    scales: np.ndarray   # uint16 bf16 bit patterns [rows, cols/group_size]
-    biases: np.ndarray   # uint16 bf16 bit patterns [rows, cols/group_size]
+    scales: np.ndarray   # [rows, cols/group_size]: bf16 bit patterns (uint16) by default
+    biases: np.ndarray   # same dtype as scales
     rows: int
     cols: int
     bits: int
     group_size: int
+    sb_dtype: str = "bf16"   # "bf16", "f16" (uint16 patterns) or "f32" (float32)
 
     @property
     def nbytes(self):
@@ -60,6 +75,26 @@ def quant_weight(seed, rows, cols, bits, group_size, scale_lo=0.002, scale_hi=0.
     b = (-s * np.float32(2 ** (bits - 1))
          + g.normal(0.0, bias_sigma, size=(rows, groups)).astype(np.float32))
     return QuantWeight(packed, _top16(s), _top16(b), rows, cols, bits, group_size)
+
+
+def quant_weight_typed(seed, rows, cols, bits, group_size, sb_dtype, scale_lo=0.002,
+                       scale_hi=0.02, bias_sigma=1e-3):
+    """quant_weight's law with the scales and biases stored as sb_dtype (the
+    same draws: for "bf16" this is quant_weight itself)."""
+    g = rng(seed)
+    packed = random_words(g, rows, cols, bits)
+    groups = cols // group_size
+    s = g.uniform(scale_lo, scale_hi, size=(rows, groups)).astype(np.float32)
+    b = (-s * np.float32(2 ** (bits - 1))
+         + g.normal(0.0, bias_sigma, size=(rows, groups)).astype(np.float32))
+    return QuantWeight(packed, as_dtype(s, sb_dtype), as_dtype(b, sb_dtype), rows, cols, bits,
+                       group_size, sb_dtype)
+
+
+def x_typed(seed, M, K, dtype):
+    """x [M, K] N(0, 1) stored as dtype (x_bf16's draws)."""
+    g = rng(seed)
+    return as_dtype(g.standard_normal(size=(M, K)).astype(np.float32), dtype)
 
 
 def x_bf16(seed, M, K):

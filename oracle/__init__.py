@@ -10,6 +10,8 @@ the pages it restates, at the top of that file.
 All arrays are numpy arrays on the host:
   packed  uint32 [rows, cols*bits/32]   scales/biases uint16 (bf16 bits) [rows, cols/G]
   x       uint16 (bf16 bits) [M, K]     idx uint32 [n]
+The typed variants take a dtype name per buffer: "bf16" and "f16" buffers
+hold 16-bit patterns (uint16), "f32" buffers float32 values.
 """
 import ctypes
 import os
@@ -58,8 +60,40 @@ def _load():
         lib.oracle_qmm_sampled.argtypes = [P, I64, P, P, P, I64, I64, I, I, I,
                                            P, P, I64, P, P, I]
         lib.oracle_quantize.argtypes = [P, I64, I64, I, I, P, P, P, I]
+        lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_f16_to_f64.restype = ctypes.c_double
+        lib.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+        lib.oracle_f32_to_f16.restype = ctypes.c_uint16
+        lib.oracle_dequantize_typed.argtypes = [P, P, P, I, I64, I64, I, I, I, P, I]
+        lib.oracle_rows_typed.argtypes = [P, P, P, I, I64, I64, P, I64, I, I, I, P, I]
+        lib.oracle_rows_typed.restype = I64
+        lib.oracle_qmm_typed.argtypes = [P, I, I64, P, P, P, I, I64, I64, I, I, I, P, P, I]
+        lib.oracle_qmm_sampled_typed.argtypes = [P, I, I64, P, P, P, I, I64, I64, I, I, I,
+                                                 P, P, I64, P, P, I]
+        lib.oracle_quantize_typed.argtypes = [P, I, I64, I64, I, I, P, P, P, I]
         _lib = lib
     return _lib
+
+
+# The oracle's own numbering of element types (qmm_oracle.c, ORACLE_*).
+_TYPE = {"f32": 0, "bf16": 1, "f16": 2}
+# numpy storage of each type: 16-bit types as their bit patterns.
+_STORE = {"f32": np.float32, "bf16": np.uint16, "f16": np.uint16}
+
+# (exponent bits, fraction bits) of each floating-point format.
+_FORMAT = {"bf16": (8, 7), "f16": (5, 10), "f32": (8, 23)}
+
+
+def promote_types(a, b):
+    """The type x, scales and biases are promoted to (nuvec_core quantized.rs,
+    `quantized_matmul`: promote_types over the three, floating point only):
+    the narrowest of bf16, f16 and f32 whose exponent and fraction fields are
+    both at least as wide as each operand's, so that it holds every value of
+    both exactly.  bf16 with f16 has no 16-bit answer: f32."""
+    ea, fa = _FORMAT[a]
+    eb, fb = _FORMAT[b]
+    fits = [t for t, (e, f) in _FORMAT.items() if e >= max(ea, eb) and f >= max(fa, fb)]
+    return min(fits, key=lambda t: sum(_FORMAT[t]))
 
 
 def default_threads():
@@ -94,6 +128,14 @@ def pack(codes, bits):
     return out
 
 
+def f16_to_f64(h):
+    return float(_load().oracle_f16_to_f64(int(h)))
+
+
+def f32_to_f16(f):
+    return int(_load().oracle_f32_to_f16(float(f)))
+
+
 def bf16_to_f32(h):
     return float(_load().oracle_bf16_to_f32(int(h)))
 
@@ -110,45 +152,47 @@ def f32_to_bf16_array(a):
 
 
 def dequantize(packed, scales, biases, rows, cols, group_size, bits,
-               out_dtype="f32", nthreads=None):
-    """dequant(W) as float32 [rows, cols], or bf16 bits (uint16) if out_dtype='bf16'."""
+               out_dtype="f32", nthreads=None, sb_dtype="bf16"):
+    """dequant(W) [rows, cols] in out_dtype: float32 values for "f32", 16-bit
+    patterns (uint16) for "bf16" and "f16"; scales and biases of sb_dtype."""
     packed, pp = _c(packed, np.uint32)
-    scales, ps = _c(scales, np.uint16)
-    biases, pb = _c(biases, np.uint16)
-    bf16 = out_dtype == "bf16"
-    out = np.empty((rows, cols), dtype=np.uint16 if bf16 else np.float32)
-    _load().oracle_dequantize(pp, ps, pb, rows, cols, group_size, bits, int(bf16),
-                              out.ctypes.data_as(ctypes.c_void_p),
-                              nthreads or default_threads())
+    scales, ps = _c(scales, _STORE[sb_dtype])
+    biases, pb = _c(biases, _STORE[sb_dtype])
+    out = np.empty((rows, cols), dtype=_STORE[out_dtype])
+    _load().oracle_dequantize_typed(pp, ps, pb, _TYPE[sb_dtype], rows, cols, group_size, bits,
+                                    _TYPE[out_dtype], out.ctypes.data_as(ctypes.c_void_p),
+                                    nthreads or default_threads())
     return out
 
 
 def rows(packed, scales, biases, table_rows, cols, idx, group_size, bits,
-         out_dtype="bf16", nthreads=None):
+         out_dtype="bf16", nthreads=None, sb_dtype="bf16"):
     """(out [n, cols], number of out-of-table indices)."""
     packed, pp = _c(packed, np.uint32)
-    scales, ps = _c(scales, np.uint16)
-    biases, pb = _c(biases, np.uint16)
+    scales, ps = _c(scales, _STORE[sb_dtype])
+    biases, pb = _c(biases, _STORE[sb_dtype])
     idx, pi = _c(idx, np.uint32)
-    bf16 = out_dtype == "bf16"
-    out = np.empty((idx.size, cols), dtype=np.uint16 if bf16 else np.float32)
-    bad = _load().oracle_rows(pp, ps, pb, table_rows, cols, pi, idx.size, group_size,
-                              bits, int(bf16), out.ctypes.data_as(ctypes.c_void_p),
-                              nthreads or default_threads())
+    out = np.empty((idx.size, cols), dtype=_STORE[out_dtype])
+    bad = _load().oracle_rows_typed(pp, ps, pb, _TYPE[sb_dtype], table_rows, cols, pi,
+                                    idx.size, group_size, bits, _TYPE[out_dtype],
+                                    out.ctypes.data_as(ctypes.c_void_p),
+                                    nthreads or default_threads())
     return out, int(bad)
 
 
-def qmm(x, M, packed, scales, biases, N, K, transpose, group_size, bits, nthreads=None):
+def qmm(x, M, packed, scales, biases, N, K, transpose, group_size, bits, nthreads=None,
+        x_dtype="bf16", sb_dtype="bf16"):
     """(y, absy): fp64 [M, N] each; absy = sum_k |x*w|, the tolerance scale."""
-    x, px = _c(x, np.uint16)
+    x, px = _c(x, _STORE[x_dtype])
     packed, pp = _c(packed, np.uint32)
-    scales, ps = _c(scales, np.uint16)
-    biases, pb = _c(biases, np.uint16)
+    scales, ps = _c(scales, _STORE[sb_dtype])
+    biases, pb = _c(biases, _STORE[sb_dtype])
     y = np.empty((M, N), dtype=np.float64)
     a = np.empty((M, N), dtype=np.float64)
-    _load().oracle_qmm(px, M, pp, ps, pb, N, K, int(bool(transpose)), group_size, bits,
-                       y.ctypes.data_as(ctypes.c_void_p), a.ctypes.data_as(ctypes.c_void_p),
-                       nthreads or default_threads())
+    _load().oracle_qmm_typed(px, _TYPE[x_dtype], M, pp, ps, pb, _TYPE[sb_dtype], N, K,
+                             int(bool(transpose)), group_size, bits,
+                             y.ctypes.data_as(ctypes.c_void_p), a.ctypes.data_as(ctypes.c_void_p),
+                             nthreads or default_threads())
     return y, a
 
 
@@ -206,33 +250,36 @@ def _bf16_f64(h):
     return (np.asarray(h, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def quantize(w, rows, cols, group_size, bits, nthreads=None):
-    """(packed, scales, biases) of bf16 w [rows, cols]; see oracle_quantize in
-    qmm_oracle.c for the rule and its readings."""
-    w, pw = _c(w, np.uint16)
+def quantize(w, rows, cols, group_size, bits, nthreads=None, w_dtype="bf16"):
+    """(packed, scales, biases) of w [rows, cols] of w_dtype, the scales and
+    biases in w_dtype; see oracle_quantize_typed in qmm_oracle.c for the rule
+    and its readings."""
+    w, pw = _c(w, _STORE[w_dtype])
     packed = np.empty((rows, cols * bits // 32), dtype=np.uint32)
-    scales = np.empty((rows, cols // group_size), dtype=np.uint16)
-    biases = np.empty((rows, cols // group_size), dtype=np.uint16)
-    _load().oracle_quantize(pw, rows, cols, group_size, bits,
-                            packed.ctypes.data_as(ctypes.c_void_p),
-                            scales.ctypes.data_as(ctypes.c_void_p),
-                            biases.ctypes.data_as(ctypes.c_void_p), nthreads or default_threads())
+    scales = np.empty((rows, cols // group_size), dtype=_STORE[w_dtype])
+    biases = np.empty((rows, cols // group_size), dtype=_STORE[w_dtype])
+    _load().oracle_quantize_typed(pw, _TYPE[w_dtype], rows, cols, group_size, bits,
+                                  packed.ctypes.data_as(ctypes.c_void_p),
+                                  scales.ctypes.data_as(ctypes.c_void_p),
+                                  biases.ctypes.data_as(ctypes.c_void_p),
+                                  nthreads or default_threads())
     return packed, scales, biases
 
 
 def qmm_sampled(x, M, packed, scales, biases, N, K, transpose, group_size, bits,
-                ms, ns, nthreads=None):
+                ms, ns, nthreads=None, x_dtype="bf16", sb_dtype="bf16"):
     """(y, absy) at the sampled positions (ms[i], ns[i])."""
-    x, px = _c(x, np.uint16)
+    x, px = _c(x, _STORE[x_dtype])
     packed, pp = _c(packed, np.uint32)
-    scales, ps = _c(scales, np.uint16)
-    biases, pb = _c(biases, np.uint16)
+    scales, ps = _c(scales, _STORE[sb_dtype])
+    biases, pb = _c(biases, _STORE[sb_dtype])
     ms, pm = _c(ms, np.int64)
     ns, pn = _c(ns, np.int64)
     y = np.empty(ms.size, dtype=np.float64)
     a = np.empty(ms.size, dtype=np.float64)
-    _load().oracle_qmm_sampled(px, M, pp, ps, pb, N, K, int(bool(transpose)), group_size,
-                               bits, pm, pn, ms.size, y.ctypes.data_as(ctypes.c_void_p),
-                               a.ctypes.data_as(ctypes.c_void_p),
-                               nthreads or default_threads())
+    _load().oracle_qmm_sampled_typed(px, _TYPE[x_dtype], M, pp, ps, pb, _TYPE[sb_dtype], N, K,
+                                     int(bool(transpose)), group_size, bits, pm, pn, ms.size,
+                                     y.ctypes.data_as(ctypes.c_void_p),
+                                     a.ctypes.data_as(ctypes.c_void_p),
+                                     nthreads or default_threads())
     return y, a

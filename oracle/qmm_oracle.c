@@ -41,6 +41,16 @@
  *    nothing about it; the library reports such an index through its device
  *    error word, and the oracle counts them).
  *
+ *  - Other dtypes (nuvec_core quantized.rs, `quantize` doc: w may be
+ *    float16, bfloat16 or float32 and the scales and biases keep w's dtype;
+ *    `dequantize` doc: the result is in the scales' dtype; `quantized_matmul`:
+ *    x, scales and biases are promoted to one floating-point type).  The
+ *    typed functions take each buffer's type: ORACLE_F32, ORACLE_BF16 or
+ *    ORACLE_F16 (IEEE binary16).  A dequantized element is scale * code +
+ *    bias rounded once to fp32 (fmaf); for 16-bit scales the product is exact
+ *    in fp32, so this is the same value as the multiply-then-add above.  A
+ *    16-bit output is the round-to-nearest-even of that fp32 value.
+ *
  * Threading: rows (or output elements) are independent, so they are split
  * across plain pthreads, the way rlx-moshi's `dequantize_affine` splits rows
  * across rayon workers.  Results do not depend on the thread count.
@@ -125,12 +135,79 @@ uint16_t oracle_f32_to_bf16(float f)
     return (uint16_t)(u >> 16);
 }
 
-/* One weight in fp32: p = s*c exactly, then one rounding at the add. */
+/* ---------------------------------------------------------------- fp16 --- */
+
+/* IEEE 754 binary16: sign in bit 15, a 5-bit exponent field (bias 15) in
+ * bits 10..14, a 10-bit fraction.  Field 0 holds zero and the subnormals
+ * fraction * 2^-24; field 31 the infinities (fraction 0) and NaNs. */
+double oracle_f16_to_f64(uint16_t h)
+{
+    int e = (h >> 10) & 31, f = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25);
+    return (h & 0x8000u) ? -v : v;
+}
+
+/* Round-to-nearest-even from fp32 to binary16, from the definition: q is the
+ * spacing of binary16 numbers at |v| (2^(e-10) for |v| in [2^e, 2^(e+1)),
+ * 2^-24 below 2^-14), |v|/q (exact: q is a power of two) goes to the nearest
+ * integer with ties to even, and the result is encoded.  Results of 2^16 or
+ * more are past the largest finite value (65504) and become infinity. */
+uint16_t oracle_f32_to_f16(float f)
+{
+    double v = (double)f, a = fabs(v);
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    if (isnan(v))
+        return sign | 0x7E00u;
+    if (isinf(v))
+        return sign | 0x7C00u;
+    int e;
+    frexp(a, &e); /* a in [2^(e-1), 2^e) */
+    int ex = e - 1 < -14 ? -14 : e - 1;
+    double q = ldexp(1.0, ex - 10);
+    double r = nearbyint(a / q) * q;
+    if (r >= 65536.0)
+        return sign | 0x7C00u;
+    if (r < ldexp(1.0, -14))
+        return sign | (uint16_t)(r / ldexp(1.0, -24));
+    int e2;
+    double m = frexp(r, &e2); /* r = m * 2^e2, m in [0.5, 1) */
+    return sign | (uint16_t)((e2 - 1 + 15) << 10) | (uint16_t)((m * 2.0 - 1.0) * 1024.0);
+}
+
+/* Element types of the typed functions. */
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2 };
+
+/* Element i of a buffer of the given type, exactly. */
+static double load_elem(const void *p, int type, int64_t i)
+{
+    if (type == ORACLE_BF16)
+        return (double)oracle_bf16_to_f32(((const uint16_t *)p)[i]);
+    if (type == ORACLE_F16)
+        return oracle_f16_to_f64(((const uint16_t *)p)[i]);
+    return (double)((const float *)p)[i];
+}
+
+/* Store the fp32 value v as element i: as is, or rounded to nearest even. */
+static void store_elem(void *p, int type, int64_t i, float v)
+{
+    if (type == ORACLE_BF16)
+        ((uint16_t *)p)[i] = oracle_f32_to_bf16(v);
+    else if (type == ORACLE_F16)
+        ((uint16_t *)p)[i] = oracle_f32_to_f16(v);
+    else
+        ((float *)p)[i] = v;
+}
+
+/* One weight in fp32: scale * code + bias, rounded once (C99 fmaf). */
 static inline float dequant_f32(float s, uint32_t code, float b)
 {
-    float p = s * (float)code;
-    float r = p + b;
-    return r;
+    return fmaf(s, (float)code, b);
 }
 
 /* ------------------------------------------------------------- threads --- */
@@ -180,10 +257,11 @@ static void parallel_for(int64_t count, int nthreads, range_fn fn, void *ctx)
 
 typedef struct {
     const uint32_t *packed;
-    const uint16_t *scales, *biases;
+    const void *scales, *biases;
+    int sb_type;
     const uint32_t *idx; /* NULL: row r of the output is row r of the table */
     int64_t table_rows, cols;
-    int group_size, bits, out_bf16;
+    int group_size, bits, out_type;
     void *out;
     int64_t bad_index; /* rows gathered from outside the table */
 } dequant_ctx;
@@ -202,15 +280,12 @@ static void dequant_range(void *arg, int64_t begin, int64_t end)
             float v = 0.0f;
             if (in_table) {
                 int64_t g = j / c->group_size;
-                float s = oracle_bf16_to_f32(c->scales[src * groups + g]);
-                float b = oracle_bf16_to_f32(c->biases[src * groups + g]);
+                float s = (float)load_elem(c->scales, c->sb_type, src * groups + g);
+                float b = (float)load_elem(c->biases, c->sb_type, src * groups + g);
                 uint32_t code = oracle_code(c->packed + src * wpr, j, c->bits);
                 v = dequant_f32(s, code, b);
             }
-            if (c->out_bf16)
-                ((uint16_t *)c->out)[r * c->cols + j] = oracle_f32_to_bf16(v);
-            else
-                ((float *)c->out)[r * c->cols + j] = v;
+            store_elem(c->out, c->out_type, r * c->cols + j, v);
         }
     }
 }
@@ -218,35 +293,59 @@ static void dequant_range(void *arg, int64_t begin, int64_t end)
 /* out[rows, cols] = dequant(W).  Returns 0.  The oracle does not enforce the
  * library's parameter rules: any group size that divides cols and any bit
  * width 1..8 with cols*bits a multiple of 32 is computed as written. */
+int oracle_dequantize_typed(const uint32_t *packed, const void *scales,
+                            const void *biases, int sb_type, int64_t rows,
+                            int64_t cols, int group_size, int bits, int out_type,
+                            void *out, int nthreads)
+{
+    dequant_ctx c = {packed, scales, biases, sb_type, NULL, rows, cols,
+                     group_size, bits, out_type, out, 0};
+    parallel_for(rows, nthreads, dequant_range, &c);
+    return 0;
+}
+
+/* bf16 scales and biases; fp32 output, or bf16 if out_bf16. */
 int oracle_dequantize(const uint32_t *packed, const uint16_t *scales,
                       const uint16_t *biases, int64_t rows, int64_t cols,
                       int group_size, int bits, int out_bf16, void *out,
                       int nthreads)
 {
-    dequant_ctx c = {packed, scales, biases, NULL, rows, cols,
-                     group_size, bits, out_bf16, out, 0};
-    parallel_for(rows, nthreads, dequant_range, &c);
-    return 0;
+    return oracle_dequantize_typed(packed, scales, biases, ORACLE_BF16, rows, cols,
+                                   group_size, bits,
+                                   out_bf16 ? ORACLE_BF16 : ORACLE_F32, out, nthreads);
 }
 
 /* out[n, cols] = dequant(W[idx[i]]).  Returns the number of indices outside
  * [0, table_rows); their output rows are zero. */
+int64_t oracle_rows_typed(const uint32_t *packed, const void *scales,
+                          const void *biases, int sb_type, int64_t table_rows,
+                          int64_t cols, const uint32_t *idx, int64_t n,
+                          int group_size, int bits, int out_type, void *out,
+                          int nthreads)
+{
+    dequant_ctx c = {packed, scales, biases, sb_type, idx, table_rows, cols,
+                     group_size, bits, out_type, out, 0};
+    parallel_for(n, nthreads, dequant_range, &c);
+    return c.bad_index;
+}
+
 int64_t oracle_rows(const uint32_t *packed, const uint16_t *scales,
                     const uint16_t *biases, int64_t table_rows, int64_t cols,
                     const uint32_t *idx, int64_t n, int group_size, int bits,
                     int out_bf16, void *out, int nthreads)
 {
-    dequant_ctx c = {packed, scales, biases, idx, table_rows, cols,
-                     group_size, bits, out_bf16, out, 0};
-    parallel_for(n, nthreads, dequant_range, &c);
-    return c.bad_index;
+    return oracle_rows_typed(packed, scales, biases, ORACLE_BF16, table_rows, cols,
+                             idx, n, group_size, bits,
+                             out_bf16 ? ORACLE_BF16 : ORACLE_F32, out, nthreads);
 }
 
 /* ------------------------------------------------------- quantized matmul --- */
 
-/* The exact weight at logical position (k, n) of the [K, N] right operand. */
-static double weight_kn(const uint32_t *packed, const uint16_t *scales,
-                        const uint16_t *biases, int64_t N, int64_t K,
+/* The exact weight at logical position (k, n) of the [K, N] right operand
+ * (s*c + b in fp64 is exact for 16-bit scales and biases; for fp32 ones it is
+ * the fp64 rounding of the exact value, far inside any matmul tolerance). */
+static double weight_kn(const uint32_t *packed, const void *scales,
+                        const void *biases, int sb_type, int64_t N, int64_t K,
                         int transpose, int group_size, int bits, int64_t k,
                         int64_t n)
 {
@@ -256,17 +355,19 @@ static double weight_kn(const uint32_t *packed, const uint16_t *scales,
     int64_t cols = transpose ? K : N;
     int64_t wpr = oracle_words_per_row(cols, bits);
     int64_t groups = cols / group_size;
-    double s = (double)oracle_bf16_to_f32(scales[row * groups + col / group_size]);
-    double b = (double)oracle_bf16_to_f32(biases[row * groups + col / group_size]);
+    double s = load_elem(scales, sb_type, row * groups + col / group_size);
+    double b = load_elem(biases, sb_type, row * groups + col / group_size);
     uint32_t code = oracle_code(packed + row * wpr, col, bits);
     return s * (double)code + b;
 }
 
 typedef struct {
-    const uint16_t *x;
+    const void *x;
+    int x_type;
     int64_t M;
     const uint32_t *packed;
-    const uint16_t *scales, *biases;
+    const void *scales, *biases;
+    int sb_type;
     int64_t N, K;
     int transpose, group_size, bits;
     const int64_t *ms, *ns; /* sampled outputs, or NULL for all of them */
@@ -280,12 +381,12 @@ static void qmm_cols_range(void *arg, int64_t begin, int64_t end)
     double *w = (double *)malloc(sizeof(double) * (size_t)c->K);
     for (int64_t n = begin; n < end; ++n) {
         for (int64_t k = 0; k < c->K; ++k)
-            w[k] = weight_kn(c->packed, c->scales, c->biases, c->N, c->K,
+            w[k] = weight_kn(c->packed, c->scales, c->biases, c->sb_type, c->N, c->K,
                              c->transpose, c->group_size, c->bits, k, n);
         for (int64_t m = 0; m < c->M; ++m) {
             double acc = 0.0, mag = 0.0;
             for (int64_t k = 0; k < c->K; ++k) {
-                double t = (double)oracle_bf16_to_f32(c->x[m * c->K + k]) * w[k];
+                double t = load_elem(c->x, c->x_type, m * c->K + k) * w[k];
                 acc += t;
                 mag += fabs(t);
             }
@@ -303,9 +404,9 @@ static void qmm_samples_range(void *arg, int64_t begin, int64_t end)
         int64_t m = c->ms[i], n = c->ns[i];
         double acc = 0.0, mag = 0.0;
         for (int64_t k = 0; k < c->K; ++k) {
-            double t = (double)oracle_bf16_to_f32(c->x[m * c->K + k]) *
-                       weight_kn(c->packed, c->scales, c->biases, c->N, c->K,
-                                 c->transpose, c->group_size, c->bits, k, n);
+            double t = load_elem(c->x, c->x_type, m * c->K + k) *
+                       weight_kn(c->packed, c->scales, c->biases, c->sb_type, c->N,
+                                 c->K, c->transpose, c->group_size, c->bits, k, n);
             acc += t;
             mag += fabs(t);
         }
@@ -314,29 +415,53 @@ static void qmm_samples_range(void *arg, int64_t begin, int64_t end)
     }
 }
 
-/* y[M, N] and absy[M, N] (fp64) for x bf16 [M, K]. */
-int oracle_qmm(const uint16_t *x, int64_t M, const uint32_t *packed,
-               const uint16_t *scales, const uint16_t *biases, int64_t N,
-               int64_t K, int transpose, int group_size, int bits, double *y,
-               double *absy, int nthreads)
+/* y[M, N] and absy[M, N] (fp64) for x [M, K] of x_type and scales/biases of
+ * sb_type.  The promoted type changes nothing here: every operand value is
+ * exact in fp64, and the result is the exact product up to fp64 rounding. */
+int oracle_qmm_typed(const void *x, int x_type, int64_t M, const uint32_t *packed,
+                     const void *scales, const void *biases, int sb_type, int64_t N,
+                     int64_t K, int transpose, int group_size, int bits, double *y,
+                     double *absy, int nthreads)
 {
-    qmm_ctx c = {x, M, packed, scales, biases, N, K, transpose, group_size,
-                 bits, NULL, NULL, y, absy};
+    qmm_ctx c = {x, x_type, M, packed, scales, biases, sb_type, N, K, transpose,
+                 group_size, bits, NULL, NULL, y, absy};
     parallel_for(N, nthreads, qmm_cols_range, &c);
     return 0;
 }
 
 /* The same, at count sampled output positions (ms[i], ns[i]) only. */
+int oracle_qmm_sampled_typed(const void *x, int x_type, int64_t M,
+                             const uint32_t *packed, const void *scales,
+                             const void *biases, int sb_type, int64_t N, int64_t K,
+                             int transpose, int group_size, int bits,
+                             const int64_t *ms, const int64_t *ns, int64_t count,
+                             double *y, double *absy, int nthreads)
+{
+    qmm_ctx c = {x, x_type, M, packed, scales, biases, sb_type, N, K, transpose,
+                 group_size, bits, ms, ns, y, absy};
+    parallel_for(count, nthreads, qmm_samples_range, &c);
+    return 0;
+}
+
+/* bf16 x, scales and biases. */
+int oracle_qmm(const uint16_t *x, int64_t M, const uint32_t *packed,
+               const uint16_t *scales, const uint16_t *biases, int64_t N,
+               int64_t K, int transpose, int group_size, int bits, double *y,
+               double *absy, int nthreads)
+{
+    return oracle_qmm_typed(x, ORACLE_BF16, M, packed, scales, biases, ORACLE_BF16, N, K,
+                            transpose, group_size, bits, y, absy, nthreads);
+}
+
 int oracle_qmm_sampled(const uint16_t *x, int64_t M, const uint32_t *packed,
                        const uint16_t *scales, const uint16_t *biases,
                        int64_t N, int64_t K, int transpose, int group_size,
                        int bits, const int64_t *ms, const int64_t *ns,
                        int64_t count, double *y, double *absy, int nthreads)
 {
-    qmm_ctx c = {x, M, packed, scales, biases, N, K, transpose, group_size,
-                 bits, ms, ns, y, absy};
-    parallel_for(count, nthreads, qmm_samples_range, &c);
-    return 0;
+    return oracle_qmm_sampled_typed(x, ORACLE_BF16, M, packed, scales, biases, ORACLE_BF16,
+                                    N, K, transpose, group_size, bits, ms, ns, count, y,
+                                    absy, nthreads);
 }
 
 /* ------------------------------------------------------------ quantize --- */
@@ -349,14 +474,17 @@ int oracle_qmm_sampled(const uint16_t *x, int64_t M, const uint32_t *packed,
  * the stored (bf16) scale and bias, each step one IEEE fp32 operation, the
  * round half to even (rintf).  A zero scale (a constant group) gives every
  * code 0, so that the group dequantizes to its value exactly.
- * Input w: bf16 [rows, cols]; outputs as the packed format above.
+ * Input w [rows, cols] of w_type (fp32, bf16 or fp16); the scales and biases
+ * are stored in w's type (nuvec_core `quantize` doc), the scale rounded to
+ * nearest even from its fp32 value, the bias (a value of w) exactly.
  */
 typedef struct {
-    const uint16_t *w;
+    const void *w;
+    int w_type;
     int64_t rows, cols;
     int group_size, bits;
     uint32_t *packed;
-    uint16_t *scales, *biases;
+    void *scales, *biases;
 } quant_ctx;
 
 static void quant_rows_range(void *arg, int64_t begin, int64_t end)
@@ -366,12 +494,11 @@ static void quant_rows_range(void *arg, int64_t begin, int64_t end)
     uint32_t top = (1u << c->bits) - 1u;
     uint8_t *codes = (uint8_t *)malloc((size_t)c->cols);
     for (int64_t r = begin; r < end; ++r) {
-        const uint16_t *row = c->w + r * c->cols;
         for (int64_t g = 0; g < groups; ++g) {
-            const uint16_t *v = row + g * c->group_size;
-            float lo = oracle_bf16_to_f32(v[0]), hi = lo;
+            int64_t v0 = r * c->cols + g * c->group_size; /* first element of the group */
+            float lo = (float)load_elem(c->w, c->w_type, v0), hi = lo;
             for (int i = 1; i < c->group_size; ++i) {
-                float f = oracle_bf16_to_f32(v[i]);
+                float f = (float)load_elem(c->w, c->w_type, v0 + i);
                 if (f < lo)
                     lo = f;
                 if (f > hi)
@@ -379,15 +506,14 @@ static void quant_rows_range(void *arg, int64_t begin, int64_t end)
             }
             float range = hi - lo;
             float scale_f32 = range / (float)top;
-            uint16_t sb = oracle_f32_to_bf16(scale_f32);
-            uint16_t bb = oracle_f32_to_bf16(lo); /* exact: lo is a bf16 value */
-            c->scales[r * groups + g] = sb;
-            c->biases[r * groups + g] = bb;
-            float s = oracle_bf16_to_f32(sb), b = oracle_bf16_to_f32(bb);
+            store_elem(c->scales, c->w_type, r * groups + g, scale_f32);
+            store_elem(c->biases, c->w_type, r * groups + g, lo); /* exact: lo is a value of w */
+            float s = (float)load_elem(c->scales, c->w_type, r * groups + g);
+            float b = (float)load_elem(c->biases, c->w_type, r * groups + g);
             for (int i = 0; i < c->group_size; ++i) {
                 uint32_t code = 0;
                 if (s != 0.0f) {
-                    float d = oracle_bf16_to_f32(v[i]) - b;
+                    float d = (float)load_elem(c->w, c->w_type, v0 + i) - b;
                     float q = rintf(d / s);
                     if (q < 0.0f)
                         q = 0.0f;
@@ -404,10 +530,18 @@ static void quant_rows_range(void *arg, int64_t begin, int64_t end)
     free(codes);
 }
 
+void oracle_quantize_typed(const void *w, int w_type, int64_t rows, int64_t cols,
+                           int group_size, int bits, uint32_t *packed, void *scales,
+                           void *biases, int nthreads)
+{
+    quant_ctx c = {w, w_type, rows, cols, group_size, bits, packed, scales, biases};
+    parallel_for(rows, nthreads, quant_rows_range, &c);
+}
+
 void oracle_quantize(const uint16_t *w, int64_t rows, int64_t cols, int group_size,
                      int bits, uint32_t *packed, uint16_t *scales, uint16_t *biases,
                      int nthreads)
 {
-    quant_ctx c = {w, rows, cols, group_size, bits, packed, scales, biases};
-    parallel_for(rows, nthreads, quant_rows_range, &c);
+    oracle_quantize_typed(w, ORACLE_BF16, rows, cols, group_size, bits, packed, scales,
+                          biases, nthreads);
 }

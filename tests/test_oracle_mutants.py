@@ -12,9 +12,19 @@ import test_oracle_pins as pins
 
 MUTANTS = {
     # bias subtracted instead of added (the bug rlx-moshi's doc comment names)
-    "bias_subtracted": ("float r = p + b;", "float r = p - b;"),
+    "bias_subtracted": ("return fmaf(s, (float)code, b);", "return fmaf(s, (float)code, -b);"),
     # bias dropped
-    "bias_dropped": ("float r = p + b;", "float r = p;"),
+    "bias_dropped": ("return fmaf(s, (float)code, b);", "return fmaf(s, (float)code, 0.0f);"),
+    # fp16 output truncated instead of rounded to nearest even
+    "f16_truncation": ("double r = nearbyint(a / q) * q;", "double r = floor(a / q) * q;"),
+    # fp16 exponent bias off by one
+    "f16_exponent_bias": ("v = ldexp((double)(1024 + f), e - 25);",
+                          "v = ldexp((double)(1024 + f), e - 24);"),
+    # fp16 subnormals read with the normal numbers' implicit one
+    "f16_subnormal": ("v = ldexp((double)f, -24);", "v = ldexp((double)(1024 + f), -24);"),
+    # typed matmul reads x as bf16 whatever its type
+    "x_type_ignored": ("double t = load_elem(c->x, c->x_type, m * c->K + k) * w[k];",
+                       "double t = load_elem(c->x, ORACLE_BF16, m * c->K + k) * w[k];"),
     # most significant bit first inside a code
     "msb_first": ("code |= stream_bit(row_words, j * (int64_t)bits + t) << t;",
                   "code |= stream_bit(row_words, j * (int64_t)bits + t) << (bits - 1 - t);"),
@@ -43,6 +53,13 @@ PIN_TESTS = [
     (pins.test_qmm_brute_force_tiny, (4, 64, False)),
     (pins.test_transpose_flag_is_not_a_no_op, ()),
     (pins.test_rows_is_a_gather_of_dequantize, ()),
+    (pins.test_f16_to_f64_matches_numpy_every_pattern, ()),
+    (pins.test_f32_to_f16_matches_numpy, ()),
+    (pins.test_typed_dequant_pins, ("f16",)),
+    (pins.test_typed_dequant_pins, ("f32",)),
+    (pins.test_typed_dequant_f16_out_is_rne_of_f32, ("f32",)),
+    (pins.test_typed_qmm_brute_force_tiny, ("f16", "f16", True)),
+    (pins.test_typed_qmm_brute_force_tiny, ("f32", "bf16", False)),
 ]
 
 
@@ -64,7 +81,9 @@ def test_pins_catch_mutant(name, tmp_path, monkeypatch):
     # Give the mutant the same prototypes as the real library.
     for sym in ("oracle_code", "oracle_unpack", "oracle_pack", "oracle_bf16_to_f32",
                 "oracle_f32_to_bf16", "oracle_dequantize", "oracle_rows", "oracle_qmm",
-                "oracle_qmm_sampled"):
+                "oracle_qmm_sampled", "oracle_quantize", "oracle_f16_to_f64",
+                "oracle_f32_to_f16", "oracle_dequantize_typed", "oracle_rows_typed",
+                "oracle_qmm_typed", "oracle_qmm_sampled_typed", "oracle_quantize_typed"):
         f, g = getattr(real, sym), getattr(mutant, sym)
         g.argtypes, g.restype = f.argtypes, f.restype
     monkeypatch.setattr(oracle, "_lib", mutant)

@@ -412,3 +412,224 @@ def test_quantize_constant_groups_are_exact():
     assert (s == 0).all() and (packed == 0).all()
     back = oracle.dequantize(packed, s, b, rows, cols, gs, 4)
     assert (back == vals[:, None]).all()
+
+
+# -- other dtypes ----------------------------------------------------------------
+# fp16 and fp32 scales, biases and x (nuvec_core quantized.rs: `quantize` keeps
+# w's dtype for the scales and biases, `dequantize` returns the scales' dtype,
+# `quantized_matmul` promotes x, scales and biases to one float type).
+
+DTYPES = ("bf16", "f16", "f32")
+
+
+def np_f64(a, dtype):
+    """Values of a stored buffer via numpy's own conversions."""
+    a = np.asarray(a)
+    if dtype == "f32":
+        return a.astype(np.float32).astype(np.float64)
+    if dtype == "f16":
+        return a.astype(np.uint16).view(np.float16).astype(np.float64)
+    return bf16_f64(a)
+
+
+def np_dense_typed_f64(w):
+    c = np_codes(w.packed, w.cols, w.bits).astype(np.float64)
+    s = np.repeat(np_f64(w.scales, w.sb_dtype), w.group_size, axis=1)
+    b = np.repeat(np_f64(w.biases, w.sb_dtype), w.group_size, axis=1)
+    return s * c + b
+
+
+def np_f16_bits(f32):
+    with np.errstate(over="ignore"):
+        return np.asarray(f32, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def test_f16_to_f64_matches_numpy_every_pattern():
+    pats = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    want = pats.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_to_f64(int(p)) for p in pats])
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all(), pats[~same][:8]
+    # signs of zero
+    assert np.signbit(oracle.f16_to_f64(0x8000)) and not np.signbit(oracle.f16_to_f64(0))
+
+
+def test_f32_to_f16_matches_numpy():
+    g = synth.rng(17)
+    mags = 10.0 ** g.uniform(-9, 5.5, size=6000)
+    vals = (mags * np.where(g.random(6000) < 0.5, -1.0, 1.0)).astype(np.float32)
+    # midpoints between neighbouring fp16 values (ties), normal and subnormal,
+    # both parities of the lower neighbour
+    lo = np.arange(0, 0x7BFF, 37, dtype=np.uint32).astype(np.uint16)
+    mid = ((lo.view(np.float16).astype(np.float64)
+            + (lo + 1).view(np.float16).astype(np.float64)) / 2).astype(np.float32)
+    edge = np.array([0.0, -0.0, 65504.0, 65519.0, 65519.996, 65520.0, 65536.0, 1e9,
+                     2.0 ** -14, 2.0 ** -24, 2.0 ** -25, 2.0 ** -25 * 1.0001, 2.0 ** -26,
+                     6.1e-5, np.inf, -np.inf], dtype=np.float32)
+    allv = np.concatenate([vals, mid, -mid, edge])
+    got = np.array([oracle.f32_to_f16(float(v)) for v in allv], dtype=np.uint16)
+    assert (got == np_f16_bits(allv)).all(), allv[got != np_f16_bits(allv)][:8]
+    nan = oracle.f32_to_f16(float("nan"))
+    assert (nan & 0x7C00) == 0x7C00 and (nan & 0x3FF) != 0
+
+
+def _golden_typed(sb):
+    g = load_golden("lsb_first_plus_bias.txt")
+    words = np.array(ints(g["words"]), dtype=np.uint32)[None, :]
+    bits, cols, gs = int(g["bits"][0]), int(g["cols"][0]), int(g["group_size"][0])
+    scale = float(bf16_f64(int(g["scale_bf16"][0], 0)))
+    bias = float(bf16_f64(int(g["bias_bf16"][0], 0)))
+    s = synth.as_dtype(np.full((1, cols // gs), scale), sb)
+    b = synth.as_dtype(np.full((1, cols // gs), bias), sb)
+    return words, s, b, cols, gs, bits, [float(v) for v in g["expect_f32"]]
+
+
+def _is_correctly_rounded_f32(v32, exact):
+    """v32 is the fp32 nearest to the exact rational value (ties to even)."""
+    from fractions import Fraction
+    v = Fraction(float(v32))
+    up = Fraction(float(np.nextafter(np.float32(v32), np.float32(np.inf))))
+    dn = Fraction(float(np.nextafter(np.float32(v32), np.float32(-np.inf))))
+    d = abs(v - exact)
+    if d > abs(up - exact) or d > abs(dn - exact):
+        return False
+    if d == abs(up - exact) or d == abs(dn - exact):  # a tie: the even one
+        return (np.float32(v32).view(np.uint32) & 1) == 0
+    return True
+
+
+@pytest.mark.parametrize("sb", ("f16", "f32"))
+def test_typed_dequant_pins(sb):
+    from fractions import Fraction
+    # the printed example: codes 0..7 with scale 2, bias -1 -> 2c - 1
+    words, s, b, cols, gs, bits, expected = _golden_typed(sb)
+    out = oracle.dequantize(words, s, b, 1, cols, gs, bits, "f32", sb_dtype=sb)
+    assert out.ravel().astype(np.float64).tolist() == expected
+    # zero codes give the bias exactly
+    w = synth.quant_weight_typed(71, 6, 128, 4, 32, sb)
+    w.packed[:] = 0
+    out = oracle.dequantize(w.packed, w.scales, w.biases, 6, 128, 32, 4, "f32", sb_dtype=sb)
+    assert (out.astype(np.float64) == np.repeat(np_f64(w.biases, sb), 32, axis=1)).all()
+    # every element is s*c + b rounded once to fp32 (exact rational arithmetic)
+    for bits in (3, 4, 8):
+        w = synth.quant_weight_typed(72 + bits, 3, 64, bits, 32, sb)
+        out = oracle.dequantize(w.packed, w.scales, w.biases, 3, 64, 32, bits, "f32",
+                                sb_dtype=sb)
+        codes = np_codes(w.packed, 64, bits)
+        s = np_f64(w.scales, sb)
+        b = np_f64(w.biases, sb)
+        for r in range(3):
+            for j in range(64):
+                exact = Fraction(s[r, j // 32]) * int(codes[r, j]) + Fraction(b[r, j // 32])
+                assert _is_correctly_rounded_f32(out[r, j], exact), (bits, r, j)
+
+
+@pytest.mark.parametrize("sb", DTYPES)
+def test_typed_dequant_f16_out_is_rne_of_f32(sb):
+    w = synth.quant_weight_typed(81, 9, 512, 5, 64, sb)
+    f = oracle.dequantize(w.packed, w.scales, w.biases, 9, 512, 64, 5, "f32", sb_dtype=sb)
+    h = oracle.dequantize(w.packed, w.scales, w.biases, 9, 512, 64, 5, "f16", sb_dtype=sb)
+    assert (h == np_f16_bits(f)).all()
+    bb = oracle.dequantize(w.packed, w.scales, w.biases, 9, 512, 64, 5, "bf16", sb_dtype=sb)
+    assert (bb == torch_bf16_bits(f)).all()
+    # and the fp32 value is the exact fp64 one rounded once (16-bit scales:
+    # s*c + b is exact in fp64)
+    if sb != "f32":
+        assert (f == np_dense_typed_f64(w).astype(np.float32)).all()
+
+
+def test_typed_rows_is_a_gather_of_typed_dequantize():
+    w = synth.quant_weight_typed(91, 40, 128, 6, 32, "f16")
+    full = oracle.dequantize(w.packed, w.scales, w.biases, 40, 128, 32, 6, "f16", sb_dtype="f16")
+    idx = synth.indices(92, 17, 40)
+    got, bad = oracle.rows(w.packed, w.scales, w.biases, 40, 128, idx, 32, 6, "f16",
+                           sb_dtype="f16")
+    assert bad == 0 and (got == full[idx]).all()
+
+
+@pytest.mark.parametrize("x_dtype,sb_dtype,transpose", [
+    ("f16", "f16", True), ("f16", "f16", False), ("f32", "f32", True), ("f32", "bf16", False),
+    ("bf16", "f16", True), ("f16", "f32", False)])
+def test_typed_qmm_brute_force_tiny(x_dtype, sb_dtype, transpose):
+    M, K, bits, gs = 3, 64, 5, 32
+    N = 8 if transpose else 32
+    x = synth.x_typed(310, M, K, x_dtype)
+    if transpose:
+        w = synth.quant_weight_typed(410, N, K, bits, gs, sb_dtype)
+        dense_kn = np_dense_typed_f64(w).T
+    else:
+        w = synth.quant_weight_typed(510, K, N, bits, gs, sb_dtype)
+        dense_kn = np_dense_typed_f64(w)
+    y, a = oracle.qmm(x, M, w.packed, w.scales, w.biases, N, K, transpose, gs, bits,
+                      x_dtype=x_dtype, sb_dtype=sb_dtype)
+    xf = np_f64(x, x_dtype)
+    want = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):
+                acc += xf[m, k] * dense_kn[k, n]
+            want[m, n] = acc
+    assert np.allclose(y, want, rtol=1e-12, atol=1e-12)
+    assert np.allclose(a, np.abs(xf) @ np.abs(dense_kn), rtol=1e-12, atol=1e-12)
+    ms, ns = np.array([0, 2, 1], np.int64), np.array([N - 1, 0, 3], np.int64)
+    ys, _ = oracle.qmm_sampled(x, M, w.packed, w.scales, w.biases, N, K, transpose, gs, bits,
+                               ms, ns, x_dtype=x_dtype, sb_dtype=sb_dtype)
+    assert (ys == y[ms, ns]).all()
+
+
+def _holds(values, t):
+    """Whether every (finite) value is exactly a value of type t."""
+    v = np.asarray(values, dtype=np.float64)
+    v = v[np.isfinite(v)]
+    if t == "f32":
+        return bool((v.astype(np.float32).astype(np.float64) == v).all())
+    if t == "f16":
+        with np.errstate(over="ignore"):
+            return bool((v.astype(np.float16).astype(np.float64) == v).all())
+    f = v.astype(np.float32)
+    return bool(((f.astype(np.float64) == v) & ((f.view(np.uint32) & 0xFFFF) == 0)).all())
+
+
+def test_promote_types_holds_both_exactly_and_is_narrowest():
+    every = {"bf16": bf16_f64(np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)),
+             "f16": np.arange(1 << 16, dtype=np.uint32).astype(np.uint16).view(np.float16)
+             .astype(np.float64),
+             # fp32 values no 16-bit type holds (fraction and exponent range)
+             "f32": np.array([1.0 + 2.0 ** -23, 2.0 ** -140, 3.0e38, 1.0], np.float32)
+             .astype(np.float64)}
+    width = {"bf16": 16, "f16": 16, "f32": 32}
+    for a in DTYPES:
+        for b in DTYPES:
+            t = oracle.promote_types(a, b)
+            assert t == oracle.promote_types(b, a)
+            both = np.concatenate([every[a], every[b]])
+            assert _holds(both, t), (a, b, t)
+            narrower = [u for u in DTYPES if width[u] < width[t]]
+            assert not any(_holds(both, u) for u in narrower), (a, b, t)
+    assert oracle.promote_types("bf16", "f16") == "f32"
+
+
+@pytest.mark.parametrize("w_dtype", ("f16", "f32"))
+@pytest.mark.parametrize("bits", (2, 4, 8))
+def test_typed_quantize_codes_follow_the_stated_rule(w_dtype, bits):
+    rows, cols, gs = 6, 256, 64
+    w = synth.x_typed(960 + bits, rows, cols, w_dtype)
+    packed, s, b = oracle.quantize(w, rows, cols, gs, bits, w_dtype=w_dtype)
+    assert s.dtype == b.dtype == np.asarray(w).dtype
+    wf = np_f64(w, w_dtype).astype(np.float32).reshape(rows, cols // gs, gs)
+    sf = np_f64(s, w_dtype).astype(np.float32)[:, :, None]
+    bf = np_f64(b, w_dtype).astype(np.float32)[:, :, None]
+    assert (bf[:, :, 0] == wf.min(axis=2)).all()
+    top = (1 << bits) - 1
+    # the stored scale is (max - min) / top in fp32, then in w's dtype
+    sc = (wf.max(axis=2) - wf.min(axis=2)) / np.float32(top)
+    want_s = sc if w_dtype == "f32" else sc.astype(np.float16).astype(np.float32)
+    assert (sf[:, :, 0] == want_s).all()
+    want = np.clip(np.rint((wf - bf) / sf), 0, top).astype(np.uint32).reshape(rows, cols)
+    assert (np_codes(packed, cols, bits) == want).all()
+    back = oracle.dequantize(packed, s, b, rows, cols, gs, bits, sb_dtype=w_dtype)
+    step = np.repeat(sf[:, :, 0].astype(np.float64), gs, axis=1)
+    rel = 2.0 ** -11 if w_dtype == "f16" else 2.0 ** -23
+    bound = 0.5 * step * (1 + 1e-3) + top * rel * step + 1e-6
+    assert (np.abs(back.astype(np.float64) - np_f64(w, w_dtype)) <= bound).all()
