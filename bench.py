@@ -376,6 +376,50 @@ def fused_detail(torch, qmm, synth, peaks, warmup):
     return out
 
 
+def dtype_detail(torch, qmm, synth, peaks, warmup):
+    """quantized_matmul in the other compute types at 4 bits, group 64: fp16
+    (fp16 x, scales and biases: the tensor-core kernels in fp16) and fp32 (fp32
+    x, scales and biases: the CUDA-core path), at the decode shapes (W [4096,
+    4096], M = 1 and 16) and the prefill shape (x [2048, 4096], W [14336,
+    4096]).  GB/s counts codes, scales, biases, x and y in their own types;
+    TFLOP/s is 2 M N K.  Decode lines rotate weight copies above L2."""
+    out = {}
+    flags = qmm.qmm_set_launch_flags(qmm.QMM_LAUNCH_PDL)
+    Q = {"f16": qmm.QMM_F16, "f32": qmm.QMM_F32}
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(
+        {np.dtype(np.uint32): np.int32, np.dtype(np.uint16): np.int16,
+         np.dtype(np.float32): np.float32}[a.dtype])).cuda()
+    for d in ("f16", "f32"):
+        esz = 2 if d == "f16" else 4
+        for (M, N, K) in ((1, 4096, 4096), (16, 4096, 4096), (2048, 14336, 4096)):
+            w = synth.quant_weight_typed(140 + M, N, K, 4, 64, d)
+            nw = w.packed.nbytes + w.scales.nbytes + w.biases.nbytes
+            R = max(2, -(-3 * L2_BYTES // nw)) if M <= 16 else 2
+            ws = [tuple(dev(np.roll(a, r, 0)) for a in (w.packed, w.scales, w.biases))
+                  for r in range(R)]
+            x = dev(synth.x_typed(141 + M, M, K, d))
+            y = torch.empty((R, M, N), dtype=torch.float32 if d == "f32" else torch.int16,
+                            device="cuda")
+
+            def fn():
+                for r in range(R):
+                    pw, ps, pb = ws[r]
+                    qmm.qmm_quantized_matmul_typed(x, Q[d], M, pw, ps, pb, Q[d], N, K, 1, 64, 4,
+                                                   y[r], Q[d])
+            steps = 200 if M <= 16 else (6 if d == "f16" else 2)
+            t = time_graph(torch, graph_of(torch, fn), steps, min(warmup, 3)) / R
+            nbytes = nw + esz * (M * K + M * N)
+            gbs = nbytes / (t * 1e-3) / 1e9
+            tf = 2.0 * M * N * K / (t * 1e-3) / 1e12
+            out["%s_b4_%dx%d_M%d" % (d, N, K, M)] = {
+                "us": round(t * 1e3, 2), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 3),
+                "TFLOP/s": round(tf, 2), "frac_bf16": round(tf / peaks["bf16_tflops"], 4)}
+            del ws, y
+            torch.cuda.empty_cache()
+    qmm.qmm_set_launch_flags(flags)
+    return out
+
+
 def measured_traffic():
     """DRAM bytes per launch of the decode kernel from the committed ncu capture,
     or None if the kernel source changed since it was taken."""
@@ -389,11 +433,11 @@ def measured_traffic():
 
 
 def decode_sources_sha():
-    """sha256 over the decode kernel's sources (the kernel file, then the
-    device helpers it includes)."""
+    """sha256 over the decode kernel's sources (the kernels, the file that
+    instantiates them, then the device helpers they include)."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("gemv.cu", "common.cuh"):
+    for name in ("gemv_impl.cuh", "gemv.cu", "common.cuh"):
         with open(os.path.join(ROOT, "mlx_grouped_affine_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -509,6 +553,7 @@ def run_gpu(args):
         detail.update(sweep_detail(torch, qmm, synth, peaks, args.warmup))
         detail.update(gather_detail(torch, qmm, synth, peaks, args.warmup))
         detail.update(fused_detail(torch, qmm, synth, peaks, args.warmup))
+        detail.update(dtype_detail(torch, qmm, synth, peaks, args.warmup))
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -611,11 +656,13 @@ PROFILE_CASES = {
     "prefill": (2048, 14336, 4096, 4, 64, True),
     "splitk_m128": (128, 4096, 4096, 4, 64, True),
 }
-OTHER_PROFILES = ("gather_sorted", "silu_gate", "quantize", "dequantize", "rows")
+OTHER_PROFILES = ("gather_sorted", "silu_gate", "quantize", "dequantize", "rows", "f16_prefill",
+                  "f16_decode", "f32_decode", "f32_prefill")
 
 
 def run_other_profile(case, launches):
-    """Eager launches of the non-matmul entry points for ncu (inputs > L2)."""
+    """Eager launches, for ncu, of the entry points and dtypes the matmul cases
+    above do not cover (inputs larger than L2)."""
     import torch
     from mlx_grouped_affine_gb300 import qmm, synth
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(
@@ -656,6 +703,21 @@ def run_other_profile(case, launches):
         o = torch.empty((N, K), dtype=torch.int16, device="cuda")
         for i in range(launches):
             qmm.qmm_dequantize(*cs[i % R], N, K, 64, 4, o, qmm.QMM_BF16)
+    elif case in ("f16_prefill", "f16_decode", "f32_decode", "f32_prefill"):
+        d = case[:3]
+        Q = {"f16": qmm.QMM_F16, "f32": qmm.QMM_F32}[d]
+        M, N, K = (2048, 14336, 4096) if case.endswith("prefill") else (1, 4096, 4096)
+        w = synth.quant_weight_typed(150, N, K, 4, 64, d)
+        nw = w.packed.nbytes + w.scales.nbytes + w.biases.nbytes
+        R = max(2, -(-3 * L2_BYTES // nw)) if M == 1 else 2
+        tdev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(
+            {np.dtype(np.uint32): np.int32, np.dtype(np.uint16): np.int16,
+             np.dtype(np.float32): np.float32}[a.dtype])).cuda()
+        ws = [tuple(tdev(np.roll(a, r, 0)) for a in (w.packed, w.scales, w.biases)) for r in range(R)]
+        x = tdev(synth.x_typed(151, M, K, d))
+        y = torch.empty((M, N), dtype=torch.float32 if d == "f32" else torch.int16, device="cuda")
+        for i in range(launches):
+            qmm.qmm_quantized_matmul_typed(x, Q, M, *ws[i % R], Q, N, K, 1, 64, 4, y, Q)
     elif case == "rows":
         T, C = synth.ROWS_TABLE
         w = synth.quant_weight(2, T, C, 4, 64)

@@ -34,6 +34,10 @@
  *     QMM_ERR_CUDA.  qmm_last_error() then describes the failure.
  *   - An empty output (zero rows, M == 0, N == 0 or n == 0) is a valid no-op.
  *   - Outputs: QMM_F32 or QMM_BF16 (round to nearest even).
+ *   - Other dtypes: the calls above take bf16 x, scales and biases (the
+ *     pages' checkpoint format).  The *_typed calls at the end of this file
+ *     take fp16 and fp32 as well, with MLX's promotion of x, scales and
+ *     biases to one type (see qmm_promote_types).
  *
  * Thread safety: calls may come from several host threads; the last-error
  * message is per host thread.
@@ -59,7 +63,8 @@ typedef enum {
     QMM_ERR_TIMEOUT = 5      /* a bounded wait inside a kernel ran out */
 } qmm_status;
 
-typedef enum { QMM_F32 = 0, QMM_BF16 = 1 } qmm_dtype;
+/* Element types.  bf16 and fp16 values are passed as their 16-bit patterns. */
+typedef enum { QMM_F32 = 0, QMM_BF16 = 1, QMM_F16 = 2 } qmm_dtype;
 
 /*
  * qmm_dequantize -- out = dequant(W), contiguous [rows, cols].
@@ -302,6 +307,71 @@ const char *qmm_last_error(void);
  * synchronization itself failed, else QMM_OK.
  */
 qmm_status qmm_get_device_error(qmm_stream_t stream);
+
+/* ------------------------------------------------------------- dtypes ----
+ * (nuvec_core quantized.rs: `quantize` takes float16, bfloat16 or float32
+ * weights and returns scales and biases in the weights' dtype; `dequantize`
+ * returns the scales' dtype; `quantized_matmul` promotes x, scales and biases
+ * to one floating-point type and computes in it.)  These calls take the same
+ * pointers as the bf16 calls above, typed by a qmm_dtype argument; an fp32
+ * buffer holds 4-byte values, the others 16-bit patterns.  Scales and biases
+ * share one dtype. */
+
+/*
+ * qmm_promote_types -- *out = the type that a and b promote to: the
+ * narrowest of bf16, f16 and f32 that holds every value of both exactly
+ * (a itself when a == b; f32 otherwise, since bf16 and f16 each hold values
+ * the other lacks).  QMM_ERR_UNSUPPORTED for an unknown dtype.
+ */
+qmm_status qmm_promote_types(qmm_dtype a, qmm_dtype b, qmm_dtype *out);
+
+/*
+ * qmm_dequantize_typed / qmm_rows_typed -- qmm_dequantize and qmm_rows with
+ * scales and biases of sb_dtype.  Each element is scale * code + bias
+ * rounded once to fp32 (for 16-bit scales the product is exact), stored as
+ * is (out_dtype QMM_F32) or rounded to nearest even in the scales' dtype
+ * (out_dtype == sb_dtype); other output dtypes give QMM_ERR_UNSUPPORTED.
+ * Rules, ownership and errors as qmm_dequantize / qmm_rows.
+ */
+qmm_status qmm_dequantize_typed(const uint32_t *w, const void *scales, const void *biases,
+                                qmm_dtype sb_dtype, int64_t rows, int64_t cols, int group_size,
+                                int bits, void *out, qmm_dtype out_dtype, qmm_stream_t stream);
+
+qmm_status qmm_rows_typed(const uint32_t *w, const void *scales, const void *biases,
+                          qmm_dtype sb_dtype, int64_t table_rows, int64_t cols,
+                          const uint32_t *idx, int64_t n, int group_size, int bits, void *out,
+                          qmm_dtype out_dtype, qmm_stream_t stream);
+
+/*
+ * qmm_quantize_typed -- qmm_quantize of a weight of w_dtype; scales and
+ * biases [rows, cols/group_size] are written in w_dtype: the bias (the group
+ * minimum) exactly, the scale (max - min) / (2^bits - 1) computed in fp32 and
+ * rounded to nearest even for the 16-bit types.  Codes, rules and errors as
+ * qmm_quantize.
+ */
+qmm_status qmm_quantize_typed(const void *w, qmm_dtype w_dtype, int64_t rows, int64_t cols,
+                              int group_size, int bits, uint32_t *packed, void *scales,
+                              void *biases, qmm_stream_t stream);
+
+/*
+ * qmm_quantized_matmul_typed -- qmm_quantized_matmul with x of x_dtype and
+ * scales and biases of sb_dtype, computed in D = the promotion of the two:
+ *   D = bf16: the bf16 kernels of qmm_quantized_matmul;
+ *   D = f16:  the same kernels in fp16 (weights rounded once to fp16, fp16
+ *             tensor-core products, fp32 accumulation);
+ *   D = f32:  fp32 on the CUDA cores (weights fp32 fma(scale, code, bias),
+ *             x widened exactly, fp32 products and sums), for any mix that
+ *             promotes to f32; x rows at most 65535 * 128.
+ * y_dtype is QMM_F32 or D.  Every output is within 8e-3 * sum_k |x w| + 1e-6
+ * of the exact product (D = f32 is far inside it: the sums' own rounding).
+ * Shapes, rules and errors as qmm_quantized_matmul; the D = f32 path splits K
+ * over blocks with a stream-ordered workspace the same way.
+ */
+qmm_status qmm_quantized_matmul_typed(const void *x, qmm_dtype x_dtype, int64_t M,
+                                      const uint32_t *w, const void *scales, const void *biases,
+                                      qmm_dtype sb_dtype, int64_t N, int64_t K, int transpose,
+                                      int group_size, int bits, void *y, qmm_dtype y_dtype,
+                                      qmm_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -51,6 +51,27 @@ qmm_status check_dtype(const char *op, qmm_dtype d) {
   return QMM_OK;
 }
 
+bool known_dtype(qmm_dtype d) { return d == QMM_F32 || d == QMM_BF16 || d == QMM_F16; }
+
+const char *dtype_name(qmm_dtype d) {
+  return d == QMM_F32 ? "f32" : d == QMM_BF16 ? "bf16" : d == QMM_F16 ? "f16" : "unknown";
+}
+
+// An output of a typed call: fp32, or the type the call computes in.
+qmm_status check_out_dtype(const char *op, qmm_dtype out, qmm_dtype compute) {
+  if (!known_dtype(out) || (out != QMM_F32 && out != compute))
+    return fail(QMM_ERR_UNSUPPORTED, "%s: output dtype %d is not supported here (QMM_F32 or %s)",
+                op, static_cast<int>(out), dtype_name(compute));
+  return QMM_OK;
+}
+
+// The narrowest of bf16, f16 and f32 that holds every value of a and of b
+// (bf16 and f16 each hold values the other lacks, so together they need f32).
+qmm_dtype promote(qmm_dtype a, qmm_dtype b) {
+  if (a == b) return a;
+  return QMM_F32;
+}
+
 // The packed weight [rows, cols]: grouped axis, pointers, alignment.
 qmm_status check_weight(const char *op, const uint32_t *w, const uint16_t *scales,
                         const uint16_t *biases, int64_t rows, int64_t cols, int group_size) {
@@ -102,7 +123,7 @@ qmm_status qmm_dequantize(const uint32_t *w, const uint16_t *scales, const uint1
   if (!out || !aligned16(out))
     return fail(QMM_ERR_INVALID_ARG, "%s: output must be a non-null 16-byte aligned pointer", op);
   qmm::PackedWeight pw{w, scales, biases, rows, cols, group_size, bits};
-  return cuda_status(qmm::launch_dequantize(pw, nullptr, rows, out, out_dtype == QMM_BF16,
+  return cuda_status(qmm::launch_dequantize(pw, nullptr, rows, out, static_cast<int>(out_dtype),
                                             reinterpret_cast<cudaStream_t>(stream)),
                      op);
 }
@@ -123,7 +144,7 @@ qmm_status qmm_rows(const uint32_t *w, const uint16_t *scales, const uint16_t *b
   if (!out || !aligned16(out))
     return fail(QMM_ERR_INVALID_ARG, "%s: output must be a non-null 16-byte aligned pointer", op);
   qmm::PackedWeight pw{w, scales, biases, table_rows, cols, group_size, bits};
-  return cuda_status(qmm::launch_dequantize(pw, idx, n, out, out_dtype == QMM_BF16,
+  return cuda_status(qmm::launch_dequantize(pw, idx, n, out, static_cast<int>(out_dtype),
                                             reinterpret_cast<cudaStream_t>(stream)),
                      op);
 }
@@ -225,8 +246,8 @@ qmm_status qmm_quantize(const uint16_t *w, int64_t rows, int64_t cols, int group
   if (!w || !aligned16(w) || !packed || !aligned16(packed) || !scales || !aligned16(scales) ||
       !biases || !aligned16(biases))
     return fail(QMM_ERR_INVALID_ARG, "%s: every pointer must be non-null and 16-byte aligned", op);
-  return cuda_status(qmm::launch_quantize(w, rows, cols, group_size, bits, packed, scales, biases,
-                                          reinterpret_cast<cudaStream_t>(stream)),
+  return cuda_status(qmm::launch_quantize(w, qmm::kTypeBF16, rows, cols, group_size, bits, packed,
+                                          scales, biases, reinterpret_cast<cudaStream_t>(stream)),
                      op);
 }
 
@@ -337,6 +358,135 @@ qmm_status qmm_quantized_matmul_noalloc(const uint16_t *x, int64_t M, const uint
                 "%s: M=%lld N=%lld K=%lld needs %zu bytes of split-K scratch, more than the "
                 "%zu this entry point holds (qmm_quantized_matmul has no such limit)",
                 op, (long long)M, (long long)N, (long long)K, needed, qmm::static_scratch_bytes());
+  return cuda_status(e, op);
+}
+
+// ------------------------------------------------------------- dtypes ----
+
+qmm_status qmm_promote_types(qmm_dtype a, qmm_dtype b, qmm_dtype *out) {
+  if (!out) return fail(QMM_ERR_INVALID_ARG, "qmm_promote_types: null output pointer");
+  if (!known_dtype(a) || !known_dtype(b))
+    return fail(QMM_ERR_UNSUPPORTED, "qmm_promote_types: unknown dtype %d or %d",
+                static_cast<int>(a), static_cast<int>(b));
+  *out = promote(a, b);
+  return QMM_OK;
+}
+
+qmm_status qmm_dequantize_typed(const uint32_t *w, const void *scales, const void *biases,
+                                qmm_dtype sb_dtype, int64_t rows, int64_t cols, int group_size,
+                                int bits, void *out, qmm_dtype out_dtype, qmm_stream_t stream) {
+  const char *op = "qmm_dequantize_typed";
+  qmm_status st;
+  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
+  if (!known_dtype(sb_dtype))
+    return fail(QMM_ERR_UNSUPPORTED, "%s: unknown scale dtype %d", op, static_cast<int>(sb_dtype));
+  if ((st = check_out_dtype(op, out_dtype, sb_dtype)) != QMM_OK) return st;
+  const uint16_t *s16 = static_cast<const uint16_t *>(scales);
+  const uint16_t *b16 = static_cast<const uint16_t *>(biases);
+  if ((st = check_weight(op, w, s16, b16, rows, cols, group_size)) != QMM_OK) return st;
+  if (rows == 0) return QMM_OK;
+  if (!out || !aligned16(out))
+    return fail(QMM_ERR_INVALID_ARG, "%s: output must be a non-null 16-byte aligned pointer", op);
+  qmm::PackedWeight pw{w, s16, b16, rows, cols, group_size, bits, static_cast<int>(sb_dtype)};
+  return cuda_status(qmm::launch_dequantize(pw, nullptr, rows, out, static_cast<int>(out_dtype),
+                                            reinterpret_cast<cudaStream_t>(stream)),
+                     op);
+}
+
+qmm_status qmm_rows_typed(const uint32_t *w, const void *scales, const void *biases,
+                          qmm_dtype sb_dtype, int64_t table_rows, int64_t cols,
+                          const uint32_t *idx, int64_t n, int group_size, int bits, void *out,
+                          qmm_dtype out_dtype, qmm_stream_t stream) {
+  const char *op = "qmm_rows_typed";
+  qmm_status st;
+  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
+  if (!known_dtype(sb_dtype))
+    return fail(QMM_ERR_UNSUPPORTED, "%s: unknown scale dtype %d", op, static_cast<int>(sb_dtype));
+  if ((st = check_out_dtype(op, out_dtype, sb_dtype)) != QMM_OK) return st;
+  const uint16_t *s16 = static_cast<const uint16_t *>(scales);
+  const uint16_t *b16 = static_cast<const uint16_t *>(biases);
+  if ((st = check_weight(op, w, s16, b16, table_rows, cols, group_size)) != QMM_OK) return st;
+  if (n < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative index count %lld", op, (long long)n);
+  if (n == 0) return QMM_OK;
+  if (!idx || !aligned16(idx))
+    return fail(QMM_ERR_INVALID_ARG, "%s: indices must be a non-null 16-byte aligned pointer", op);
+  if (!out || !aligned16(out))
+    return fail(QMM_ERR_INVALID_ARG, "%s: output must be a non-null 16-byte aligned pointer", op);
+  qmm::PackedWeight pw{w, s16, b16, table_rows, cols, group_size, bits, static_cast<int>(sb_dtype)};
+  return cuda_status(qmm::launch_dequantize(pw, idx, n, out, static_cast<int>(out_dtype),
+                                            reinterpret_cast<cudaStream_t>(stream)),
+                     op);
+}
+
+qmm_status qmm_quantize_typed(const void *w, qmm_dtype w_dtype, int64_t rows, int64_t cols,
+                              int group_size, int bits, uint32_t *packed, void *scales,
+                              void *biases, qmm_stream_t stream) {
+  const char *op = "qmm_quantize_typed";
+  qmm_status st;
+  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
+  if (!known_dtype(w_dtype))
+    return fail(QMM_ERR_UNSUPPORTED, "%s: unknown weight dtype %d", op, static_cast<int>(w_dtype));
+  if (rows < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative row count %lld", op, (long long)rows);
+  if (cols <= 0 || cols % group_size != 0)
+    return fail(QMM_ERR_INVALID_ARG, "%s: cols (%lld) must be a positive multiple of group_size %d",
+                op, (long long)cols, group_size);
+  if (rows == 0) return QMM_OK;
+  if (!w || !aligned16(w) || !packed || !aligned16(packed) || !scales || !aligned16(scales) ||
+      !biases || !aligned16(biases))
+    return fail(QMM_ERR_INVALID_ARG, "%s: every pointer must be non-null and 16-byte aligned", op);
+  return cuda_status(qmm::launch_quantize(w, static_cast<int>(w_dtype), rows, cols, group_size,
+                                          bits, packed, scales, biases,
+                                          reinterpret_cast<cudaStream_t>(stream)),
+                     op);
+}
+
+qmm_status qmm_quantized_matmul_typed(const void *x, qmm_dtype x_dtype, int64_t M,
+                                      const uint32_t *w, const void *scales, const void *biases,
+                                      qmm_dtype sb_dtype, int64_t N, int64_t K, int transpose,
+                                      int group_size, int bits, void *y, qmm_dtype y_dtype,
+                                      qmm_stream_t stream) {
+  const char *op = "qmm_quantized_matmul_typed";
+  qmm_status st;
+  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
+  if (!known_dtype(x_dtype) || !known_dtype(sb_dtype))
+    return fail(QMM_ERR_UNSUPPORTED, "%s: unknown x or scale dtype (%d, %d)", op,
+                static_cast<int>(x_dtype), static_cast<int>(sb_dtype));
+  const qmm_dtype d = promote(x_dtype, sb_dtype);
+  if ((st = check_out_dtype(op, y_dtype, d)) != QMM_OK) return st;
+  if (transpose != 0 && transpose != 1)
+    return fail(QMM_ERR_INVALID_ARG, "%s: transpose must be 0 or 1, got %d", op, transpose);
+  if (M < 0 || N < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative M or N", op);
+  if (K <= 0) return fail(QMM_ERR_INVALID_ARG, "%s: K must be positive, got %lld", op, (long long)K);
+  const int64_t rows = transpose ? N : K, cols = transpose ? K : N;
+  const uint16_t *s16 = static_cast<const uint16_t *>(scales);
+  const uint16_t *b16 = static_cast<const uint16_t *>(biases);
+  if (transpose || N > 0) {
+    if ((st = check_weight(op, w, s16, b16, rows, cols, group_size)) != QMM_OK) return st;
+  }
+  if (M == 0 || N == 0) return QMM_OK;
+  if (!x || !aligned16(x))
+    return fail(QMM_ERR_INVALID_ARG, "%s: x must be a non-null 16-byte aligned pointer", op);
+  if (!y || !aligned16(y))
+    return fail(QMM_ERR_INVALID_ARG, "%s: y must be a non-null 16-byte aligned pointer", op);
+  if (M > (int64_t(1) << 31) || K > (int64_t(1) << 31) || N > (int64_t(1) << 31))
+    return fail(QMM_ERR_INVALID_ARG, "%s: M, N and K must each be below 2^31", op);
+  if (d == QMM_F32 && M > int64_t(65535) * 128)
+    return fail(QMM_ERR_INVALID_ARG, "%s: the fp32 path takes at most %lld rows of x", op,
+                (long long)(int64_t(65535) * 128));
+  qmm::PackedWeight pw{w, s16, b16, rows, cols, group_size, bits, static_cast<int>(sb_dtype)};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool y16 = y_dtype != QMM_F32;
+  const uint16_t *x16 = static_cast<const uint16_t *>(x);
+  cudaError_t e;
+  if (d == QMM_BF16)
+    e = M <= 16 ? qmm::launch_gemv(x16, M, pw, transpose != 0, y, y16, s)
+                : qmm::launch_gemm(x16, M, pw, transpose != 0, y, y16, s);
+  else if (d == QMM_F16)
+    e = M <= 16 ? qmm::launch_gemv_f16(x16, M, pw, transpose != 0, y, y16, s)
+                : qmm::launch_gemm_f16(x16, M, pw, transpose != 0, y, y16, s);
+  else
+    e = qmm::launch_mm_f32(x, static_cast<int>(x_dtype), M, pw, transpose != 0,
+                           static_cast<float *>(y), s);
   return cuda_status(e, op);
 }
 

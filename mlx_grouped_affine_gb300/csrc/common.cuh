@@ -5,6 +5,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -106,9 +107,54 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
+// ------------------------------------------------- 16-bit element types ----
+//
+// The tensor-core paths dequantize to, and multiply in, one 16-bit type: bf16
+// (the pages' scales) or IEEE fp16 (fp16 scales with fp16 x).  Values travel
+// as bit patterns; pairs as one 32-bit register (low half first).  kMagic2 is
+// a pair of a power of two P whose mantissa has room for any code: OR-ing a
+// code c into each half gives P + c exactly, and subtracting P leaves c
+// (P = 128 for bf16's 7 fraction bits, codes below 2^7; 1024 for fp16's 10,
+// codes below 2^10, which covers 8-bit codes too).
+struct ElemBF16 {
+  static constexpr bool kF16 = false;
+  static constexpr uint32_t kMagic2 = 0x43004300u;  // (128.0, 128.0)
+  __device__ static __forceinline__ float to_f32(uint32_t h) { return bf16_bits_to_f32(h); }
+  __device__ static __forceinline__ uint16_t from_f32(float f) { return f32_to_bf16_bits(f); }
+  __device__ static __forceinline__ uint32_t pack2(float lo, float hi) { return pack_bf16x2(lo, hi); }
+  __device__ static __forceinline__ uint32_t sub2(uint32_t a, uint32_t b) { return bf16x2_sub(a, b); }
+  __device__ static __forceinline__ uint32_t fma2(uint32_t a, uint32_t b, uint32_t c) {
+    return bf16x2_fma(a, b, c);
+  }
+};
+
+struct ElemF16 {
+  static constexpr bool kF16 = true;
+  static constexpr uint32_t kMagic2 = 0x64006400u;  // (1024.0, 1024.0)
+  __device__ static __forceinline__ float to_f32(uint32_t h) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+  }
+  __device__ static __forceinline__ uint16_t from_f32(float f) {
+    return __half_as_ushort(__float2half_rn(f));  // round to nearest even
+  }
+  __device__ static __forceinline__ uint32_t pack2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+  }
+  __device__ static __forceinline__ uint32_t sub2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+  __device__ static __forceinline__ uint32_t fma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+  }
+};
+
 // ----------------------------------------------------- register dequant ----
 
-constexpr uint32_t kMagic = 0x43004300u;  // bf16x2 (128.0, 128.0)
 
 // Code j (0 <= j < n) of a little-endian bit stream held in words v[].
 template <int BITS>
@@ -119,11 +165,11 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t *v, int j) {
   return __funnelshift_r(v[word], v[word + 1], sh) & mask;
 }
 
-// Dequantize the 2*NP codes held in v[] (bit stream, LSB first) to NP bf16x2
-// natural pairs (code 2i in the low half, 2i+1 in the high half), each
-// RN(s*c + b).  s2, b2 are (s, s) and (b, b) in bf16x2; sf, bf the same in
-// fp32 (for 8-bit codes).
-template <int BITS, int NP>
+// Dequantize the 2*NP codes held in v[] (bit stream, LSB first) to NP
+// natural pairs of E (code 2i in the low half, 2i+1 in the high half), each
+// RN(s*c + b).  s2, b2 are (s, s) and (b, b) as E pairs; sf, bf the same in
+// fp32 (8-bit codes in bf16 go through fp32: 255 does not fit bf16's magic).
+template <int BITS, int NP, typename E = ElemBF16>
 __device__ __forceinline__ void dequant_pairs(const uint32_t *v, uint32_t s2, uint32_t b2,
                                               float sf, float bf, uint32_t *out) {
   if constexpr (BITS == 4) {
@@ -134,8 +180,19 @@ __device__ __forceinline__ void dequant_pairs(const uint32_t *v, uint32_t s2, ui
       for (int i = 0; i < 4; ++i) {
         // byte i of w holds codes 8q+2i (low nibble) and 8q+2i+1 (high nibble)
         const uint32_t t = prmt(w, w4, 0x0400u | (i << 8) | i);
-        const uint32_t c = bf16x2_sub(and_or(t, 0x000F000Fu, kMagic), kMagic);
-        out[4 * q + i] = bf16x2_fma(c, s2, b2);
+        const uint32_t c = E::sub2(and_or(t, 0x000F000Fu, E::kMagic2), E::kMagic2);
+        out[4 * q + i] = E::fma2(c, s2, b2);
+      }
+    }
+  } else if constexpr (BITS == 8 && E::kF16) {
+#pragma unroll
+    for (int q = 0; q < NP / 2; ++q) {
+      const uint32_t w = v[q];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        // bytes 2i, 2i+1 into the low bytes of the halves, over the magic
+        const uint32_t t = prmt(w, 0u, 0x4040u | (2 * i) | ((2 * i + 1) << 8)) | E::kMagic2;
+        out[2 * q + i] = E::fma2(E::sub2(t, E::kMagic2), s2, b2);
       }
     }
   } else if constexpr (BITS == 8) {
@@ -147,14 +204,14 @@ __device__ __forceinline__ void dequant_pairs(const uint32_t *v, uint32_t s2, ui
         // fp32 2^23 + byte, exact; minus 2^23 gives the code exactly.
         const float c0 = __uint_as_float(prmt(w, 0x4B000000u, 0x7650u | (2 * i))) - 8388608.0f;
         const float c1 = __uint_as_float(prmt(w, 0x4B000000u, 0x7650u | (2 * i + 1))) - 8388608.0f;
-        out[2 * q + i] = pack_bf16x2(__fmaf_rn(sf, c0, bf), __fmaf_rn(sf, c1, bf));
+        out[2 * q + i] = E::pack2(__fmaf_rn(sf, c0, bf), __fmaf_rn(sf, c1, bf));
       }
     }
   } else {
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
-      const uint32_t p = code_at<BITS>(v, 2 * i) | (code_at<BITS>(v, 2 * i + 1) << 16) | kMagic;
-      out[i] = bf16x2_fma(bf16x2_sub(p, kMagic), s2, b2);
+      const uint32_t p = code_at<BITS>(v, 2 * i) | (code_at<BITS>(v, 2 * i + 1) << 16) | E::kMagic2;
+      out[i] = E::fma2(E::sub2(p, E::kMagic2), s2, b2);
     }
   }
 }
@@ -229,23 +286,28 @@ __device__ __forceinline__ uint32_t pair_fast(const uint32_t *v, int p,
   }
 }
 
-template <int BITS>
+template <int BITS, typename E = ElemBF16>
 __device__ __forceinline__ uint32_t pair_exact(const uint32_t *v, int p, uint32_t s2, uint32_t b2,
                                                float sf, float bf) {
-  if constexpr (BITS == 8) {
+  if constexpr (BITS == 8 && E::kF16) {
+    // bytes 2i, 2i+1 of word p/2 into the low bytes of the halves
+    const uint32_t i = p & 1;
+    const uint32_t q = prmt(v[p >> 1], 0u, 0x4040u | (2 * i) | ((2 * i + 1) << 8)) | E::kMagic2;
+    return E::fma2(E::sub2(q, E::kMagic2), s2, b2);
+  } else if constexpr (BITS == 8) {
     // fp32 2^23 + byte, exact; minus 2^23 gives the code exactly.
     const uint32_t w = v[p >> 1], i = p & 1;
     const float c0 = __uint_as_float(prmt(w, 0x4B000000u, 0x7650u | (2 * i))) - 8388608.0f;
     const float c1 = __uint_as_float(prmt(w, 0x4B000000u, 0x7650u | (2 * i + 1))) - 8388608.0f;
-    return pack_bf16x2(__fmaf_rn(sf, c0, bf), __fmaf_rn(sf, c1, bf));
+    return E::pack2(__fmaf_rn(sf, c0, bf), __fmaf_rn(sf, c1, bf));
   } else if constexpr (BITS == 4) {
     // byte j of w and of w >> 4 hold codes 2j and 2j+1 in their low nibbles
     const uint32_t w = v[p >> 2], j = p & 3;
-    const uint32_t q = and_or(prmt(w, w >> 4, 0x0400u | j | (j << 8)), 0x000F000Fu, kMagic);
-    return bf16x2_fma(bf16x2_sub(q, kMagic), s2, b2);
+    const uint32_t q = and_or(prmt(w, w >> 4, 0x0400u | j | (j << 8)), 0x000F000Fu, E::kMagic2);
+    return E::fma2(E::sub2(q, E::kMagic2), s2, b2);
   } else {
-    const uint32_t q = code_at<BITS>(v, 2 * p) | (code_at<BITS>(v, 2 * p + 1) << 16) | kMagic;
-    return bf16x2_fma(bf16x2_sub(q, kMagic), s2, b2);
+    const uint32_t q = code_at<BITS>(v, 2 * p) | (code_at<BITS>(v, 2 * p + 1) << 16) | E::kMagic2;
+    return E::fma2(E::sub2(q, E::kMagic2), s2, b2);
   }
 }
 
@@ -271,7 +333,8 @@ __device__ __forceinline__ void load_words(const uint32_t *__restrict__ p, uint3
   }
 }
 
-__device__ __forceinline__ uint32_t bcast_bf16x2(uint16_t h) {
+// (h, h): a 16-bit pattern in both halves of a pair.
+__device__ __forceinline__ uint32_t bcast2(uint16_t h) {
   return static_cast<uint32_t>(h) * 0x00010001u;
 }
 

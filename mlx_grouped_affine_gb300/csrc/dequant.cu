@@ -10,14 +10,17 @@
 // boundary and load with the widest aligned vector loads) and writes 64 (bf16)
 // or 128 (fp32) contiguous bytes; consecutive threads cover consecutive code
 // groups, so a warp streams 2 or 4 KB of output.  Each element is fp32
-// fma(scale, code, bias): the product of a bf16 scale and a code below 2^8 is
-// exact, so this rounds once, at the add (rlx-moshi src/mlx_dequant.rs,
-// `dequantize_affine`: scale * code + bias); bf16 output is its
-// round-to-nearest-even.
+// fma(scale, code, bias), scale * code + bias rounded once (rlx-moshi
+// src/mlx_dequant.rs, `dequantize_affine`: scale * code + bias); for 16-bit
+// scales the product is exact.  Scales and biases are bf16, fp16 or fp32
+// (nuvec_core quantized.rs: they keep the quantized weights' dtype, and
+// `dequantize` returns the scales' dtype); a 16-bit output is the
+// round-to-nearest-even of the fp32 value.
 #include "common.cuh"
 #include "internal.h"
 
 #include <mutex>
+#include <type_traits>
 
 namespace qmm {
 
@@ -28,10 +31,17 @@ namespace {
 
 constexpr int kThreads = 256;
 
-template <int BITS, bool OUT_BF16, bool GATHER>
+// Element i of a scale or bias array of type t, in fp32 (exact).
+__device__ __forceinline__ float load_sb(const uint16_t *p, int t, int64_t i) {
+  if (t == kTypeF32) return __ldg(reinterpret_cast<const float *>(p) + i);
+  const uint32_t h = __ldg(p + i);
+  return t == kTypeF16 ? ElemF16::to_f32(h) : ElemBF16::to_f32(h);
+}
+
+template <int BITS, int OUT, bool GATHER>
 __global__ void __launch_bounds__(kThreads)
 dequant_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ scales,
-               const uint16_t *__restrict__ biases, const uint32_t *__restrict__ idx,
+               const uint16_t *__restrict__ biases, int sb_type, const uint32_t *__restrict__ idx,
                int64_t row0, uint32_t groups_total, uint32_t groups_per_row, int64_t table_rows,
                int64_t cols, int group_shift, void *__restrict__ out, unsigned *err) {
   const int64_t words_per_row = (cols * BITS) >> 5;
@@ -52,8 +62,8 @@ dequant_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ scal
       uint32_t words[BITS];
       load_words<BITS>(w + src * words_per_row + static_cast<int64_t>(j) * BITS, words);
       const int64_t g = (static_cast<int64_t>(j) * 32) >> group_shift;
-      const float s = bf16_bits_to_f32(__ldg(scales + src * sb_per_row + g));
-      const float b = bf16_bits_to_f32(__ldg(biases + src * sb_per_row + g));
+      const float s = load_sb(scales, sb_type, src * sb_per_row + g);
+      const float b = load_sb(biases, sb_type, src * sb_per_row + g);
 #pragma unroll
       for (int i = 0; i < 32; ++i)
         v[i] = __fmaf_rn(s, static_cast<float>(code_at<BITS>(words, i)), b);
@@ -62,12 +72,13 @@ dequant_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ scal
       for (int i = 0; i < 32; ++i) v[i] = 0.0f;
     }
     const int64_t o = r * cols + static_cast<int64_t>(j) * 32;
-    if (OUT_BF16) {
+    if constexpr (OUT != kTypeF32) {
+      using E = typename std::conditional<OUT == kTypeF16, ElemF16, ElemBF16>::type;
       uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + o);
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        dst[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                            pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+        dst[q] = make_uint4(E::pack2(v[8 * q], v[8 * q + 1]), E::pack2(v[8 * q + 2], v[8 * q + 3]),
+                            E::pack2(v[8 * q + 4], v[8 * q + 5]), E::pack2(v[8 * q + 6], v[8 * q + 7]));
     } else {
       float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(out) + o);
 #pragma unroll
@@ -76,7 +87,7 @@ dequant_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ scal
   }
 }
 
-template <int BITS, bool OUT_BF16, bool GATHER>
+template <int BITS, int OUT, bool GATHER>
 cudaError_t launch_t(const PackedWeight &pw, const uint32_t *idx, int64_t out_rows,
                      void *out, cudaStream_t stream) {
   const int group_shift = pw.group == 32 ? 5 : pw.group == 64 ? 6 : 7;
@@ -93,8 +104,8 @@ cudaError_t launch_t(const PackedWeight &pw, const uint32_t *idx, int64_t out_ro
     const uint32_t total = static_cast<uint32_t>(rows * gpr);
     const int64_t blocks = (static_cast<int64_t>(total) + kThreads - 1) / kThreads;
     const unsigned grid = static_cast<unsigned>(blocks < max_blocks ? blocks : max_blocks);
-    dequant_kernel<BITS, OUT_BF16, GATHER><<<grid, kThreads, 0, stream>>>(
-        pw.w, pw.scales, pw.biases, idx, r0, total, static_cast<uint32_t>(gpr), pw.rows,
+    dequant_kernel<BITS, OUT, GATHER><<<grid, kThreads, 0, stream>>>(
+        pw.w, pw.scales, pw.biases, pw.sb_type, idx, r0, total, static_cast<uint32_t>(gpr), pw.rows,
         pw.cols, group_shift, out, err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -102,28 +113,36 @@ cudaError_t launch_t(const PackedWeight &pw, const uint32_t *idx, int64_t out_ro
   return cudaSuccess;
 }
 
+template <int BITS, bool GATHER>
+cudaError_t launch_out(const PackedWeight &pw, const uint32_t *idx, int64_t out_rows, void *out,
+                       int out_type, cudaStream_t stream) {
+  switch (out_type) {
+    case kTypeF32: return launch_t<BITS, kTypeF32, GATHER>(pw, idx, out_rows, out, stream);
+    case kTypeBF16: return launch_t<BITS, kTypeBF16, GATHER>(pw, idx, out_rows, out, stream);
+    case kTypeF16: return launch_t<BITS, kTypeF16, GATHER>(pw, idx, out_rows, out, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 template <int BITS>
 cudaError_t launch_bits(const PackedWeight &pw, const uint32_t *idx, int64_t out_rows,
-                        void *out, bool out_bf16, cudaStream_t stream) {
-  if (idx)
-    return out_bf16 ? launch_t<BITS, true, true>(pw, idx, out_rows, out, stream)
-                    : launch_t<BITS, false, true>(pw, idx, out_rows, out, stream);
-  return out_bf16 ? launch_t<BITS, true, false>(pw, idx, out_rows, out, stream)
-                  : launch_t<BITS, false, false>(pw, idx, out_rows, out, stream);
+                        void *out, int out_type, cudaStream_t stream) {
+  return idx ? launch_out<BITS, true>(pw, idx, out_rows, out, out_type, stream)
+             : launch_out<BITS, false>(pw, idx, out_rows, out, out_type, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_dequantize(const PackedWeight &pw, const uint32_t *idx, int64_t out_rows,
-                              void *out, bool out_bf16, cudaStream_t stream) {
+                              void *out, int out_type, cudaStream_t stream) {
   switch (pw.bits) {
-    case 1: return launch_bits<1>(pw, idx, out_rows, out, out_bf16, stream);
-    case 2: return launch_bits<2>(pw, idx, out_rows, out, out_bf16, stream);
-    case 3: return launch_bits<3>(pw, idx, out_rows, out, out_bf16, stream);
-    case 4: return launch_bits<4>(pw, idx, out_rows, out, out_bf16, stream);
-    case 5: return launch_bits<5>(pw, idx, out_rows, out, out_bf16, stream);
-    case 6: return launch_bits<6>(pw, idx, out_rows, out, out_bf16, stream);
-    case 8: return launch_bits<8>(pw, idx, out_rows, out, out_bf16, stream);
+    case 1: return launch_bits<1>(pw, idx, out_rows, out, out_type, stream);
+    case 2: return launch_bits<2>(pw, idx, out_rows, out, out_type, stream);
+    case 3: return launch_bits<3>(pw, idx, out_rows, out, out_type, stream);
+    case 4: return launch_bits<4>(pw, idx, out_rows, out, out_type, stream);
+    case 5: return launch_bits<5>(pw, idx, out_rows, out, out_type, stream);
+    case 6: return launch_bits<6>(pw, idx, out_rows, out, out_type, stream);
+    case 8: return launch_bits<8>(pw, idx, out_rows, out, out_type, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -148,14 +148,18 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, N = BN, M = UM (each of the tile's two MMAs).
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                            (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(UM >> 4) << 24);
+// Instruction descriptor of kind::f16: fp32 accumulator, A and B both bf16
+// (format 1 in bits 7-9 and 10-12) or both fp16 (format 0), both K-major,
+// N = BN, M = UM (each of the tile's two MMAs).
+template <typename E>
+__host__ __device__ constexpr uint32_t idesc_kmajor() {
+  return (1u << 4) | (E::kF16 ? 0u : (1u << 7) | (1u << 10)) |
+         (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(UM >> 4) << 24);
+}
 
 // The same with B (the dequantized weight) MN-major: bit 16 = transpose B.
-constexpr uint32_t kIdescBmn = kIdesc | (1u << 16);
+template <typename E>
+__host__ __device__ constexpr uint32_t idesc_bmn() { return idesc_kmajor<E>() | (1u << 16); }
 
 // MN-major, 128-byte swizzle: atoms of 64 N-elements x 8 K-rows; LBO = 8192
 // bytes between atoms along N, SBO = 1024 bytes between atoms along K.
@@ -274,7 +278,7 @@ __device__ __forceinline__ void item_place(int dt, int tile_n0, int kb, int &row
   }
 }
 
-template <int BITS, bool TRANS>
+template <typename E, int BITS, bool TRANS>
 __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int nk) {
   const int dt = threadIdx.x - 32 * (2 + kEpiWarps);  // 0 .. 32 * kDeqWarps - 1
   const int num_units = a.m_tiles * a.n_tiles * a.splits;
@@ -324,7 +328,10 @@ __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int
     const uint32_t base = smem_u32(sB + s * B_BYTES);
     const uint32_t hs = cur.sb & 0xFFFFu, hb = cur.sb >> 16;
     const uint32_t b2 = hb * 0x00010001u;
-    if (__all_sync(0xffffffffu, fast_scale(hs))) {
+    // The fast form is bf16's (fp16 has no room for its multipliers).
+    bool fast = false;
+    if constexpr (!E::kF16) fast = __all_sync(0xffffffffu, fast_scale(hs));
+    if (fast) {
       uint32_t m[fast_slots<BITS>()];
       fast_muls<BITS>(hs, m);
 #pragma unroll
@@ -336,12 +343,12 @@ __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int
       }
     } else {
       const uint32_t s2 = hs * 0x00010001u;
-      const float sf = bf16_bits_to_f32(hs), bf = bf16_bits_to_f32(hb);
+      const float sf = E::to_f32(hs), bf = E::to_f32(hb);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         uint32_t v[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = pair_exact<BITS>(cur.v, 4 * j + i, s2, b2, sf, bf);
+        for (int i = 0; i < 4; ++i) v[i] = pair_exact<BITS, E>(cur.v, 4 * j + i, s2, b2, sf, bf);
         st_shared_v4(base + off[j], v);
       }
     }
@@ -397,10 +404,10 @@ __device__ void tma_role(const CUtensorMap *tmap, const GemmArgs &a, uint8_t *sA
   }
 }
 
-template <bool TRANS>
+template <typename E, bool TRANS>
 __device__ void mma_role(const GemmArgs &a, uint8_t *sA, uint8_t *sB, Barriers *bars, int nk,
                          uint32_t tmem) {
-  constexpr uint32_t idesc = TRANS ? kIdesc : kIdescBmn;
+  constexpr uint32_t idesc = TRANS ? idesc_kmajor<E>() : idesc_bmn<E>();
   // Start-address step of one 16-wide K slice: 32 bytes inside a K-major row,
   // two 8-row K atoms (2048 bytes) in the MN-major tile; in units of 16 bytes.
   constexpr uint64_t b_step = TRANS ? 2 : 128;
@@ -453,7 +460,7 @@ __device__ void mma_role(const GemmArgs &a, uint8_t *sA, uint8_t *sB, Barriers *
     if (__all_sync(0xffffffffu, mbar_try_wait(&bars->mma_done, 0))) break;
 }
 
-template <bool OUT_BF16>
+template <typename E, bool OUT_BF16>
 __device__ void epilogue_role(const GemmArgs &a, Barriers *bars, uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -497,16 +504,16 @@ __device__ void epilogue_role(const GemmArgs &a, Barriers *bars, uint32_t tmem) 
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             uint4 p;
-            p.x = pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
-            p.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
-            p.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
-            p.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
+            p.x = E::pack2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
+            p.y = E::pack2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
+            p.z = E::pack2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
+            p.w = E::pack2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
             reinterpret_cast<uint4 *>(yp)[j] = p;
           }
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (n + j < a.N) yp[j] = f32_to_bf16_bits(__uint_as_float(r[j]));
+            if (n + j < a.N) yp[j] = E::from_f32(__uint_as_float(r[j]));
         }
       } else {
         float *yp = static_cast<float *>(a.y) + o;
@@ -528,7 +535,7 @@ __device__ void epilogue_role(const GemmArgs &a, Barriers *bars, uint32_t tmem) 
   }
 }
 
-template <int BITS, bool OUT_BF16, bool TRANS>
+template <typename E, int BITS, bool OUT_BF16, bool TRANS>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -568,9 +575,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, GemmArgs a) {
   const int nk = (a.K + BK - 1) / BK;
 
   if (warp == 0) tma_role(&tmap_x, a, sA, bars, nk);
-  else if (warp == 1) mma_role<TRANS>(a, sA, sB, bars, nk, tmem);
-  else if (warp < 2 + kEpiWarps) epilogue_role<OUT_BF16>(a, bars, tmem);
-  else dequant_role<BITS, TRANS>(a, sB, bars, nk);
+  else if (warp == 1) mma_role<E, TRANS>(a, sA, sB, bars, nk, tmem);
+  else if (warp < 2 + kEpiWarps) epilogue_role<E, OUT_BF16>(a, bars, tmem);
+  else dequant_role<E, BITS, TRANS>(a, sB, bars, nk);
 
   tc_fence_before();
   __syncthreads();
@@ -584,7 +591,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, GemmArgs a) {
 // Split-K: y = the sum of the `splits` fp32 partial slices, added in slice
 // order (deterministic), converted to the output type.  Four outputs a thread
 // with 16-byte loads when the slices are 16-byte aligned.
-template <bool OUT_BF16>
+template <typename E, bool OUT_BF16>
 __global__ void __launch_bounds__(256)
 splitk_finalize(const float *__restrict__ ws, int splits, int64_t mn, void *__restrict__ y) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -598,8 +605,8 @@ splitk_finalize(const float *__restrict__ ws, int splits, int64_t mn, void *__re
       }
       if (OUT_BF16) {
         uint2 o;
-        o.x = pack_bf16x2(acc.x, acc.y);
-        o.y = pack_bf16x2(acc.z, acc.w);
+        o.x = E::pack2(acc.x, acc.y);
+        o.y = E::pack2(acc.z, acc.w);
         *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(y) + i) = o;
       } else {
         *reinterpret_cast<float4 *>(static_cast<float *>(y) + i) = acc;
@@ -609,7 +616,7 @@ splitk_finalize(const float *__restrict__ ws, int splits, int64_t mn, void *__re
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < mn; i += stride) {
       float acc = ws[i];
       for (int sl = 1; sl < splits; ++sl) acc += ws[sl * mn + i];
-      if (OUT_BF16) static_cast<uint16_t *>(y)[i] = f32_to_bf16_bits(acc);
+      if (OUT_BF16) static_cast<uint16_t *>(y)[i] = E::from_f32(acc);
       else static_cast<float *>(y)[i] = acc;
     }
   }
@@ -633,16 +640,17 @@ size_t splitk_bytes(const GemmArgs &a) {
   return static_cast<size_t>(a.splits) * a.M * a.N * sizeof(float);
 }
 
-template <int BITS, bool OUT_BF16, bool TRANS>
+template <typename E, int BITS, bool OUT_BF16, bool TRANS>
 cudaError_t launch_t(const uint16_t *x, const GemmArgs &a, cudaStream_t stream) {
   // TMA rows of x must start on 16-byte boundaries.
   if ((static_cast<int64_t>(a.K) * 2) % 16 != 0) return cudaErrorNotSupported;
   CUtensorMap map;
-  cudaError_t me = encode_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, a.K, a.M,
+  cudaError_t me = encode_map_2d(&map, E::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, a.K, a.M,
                                  static_cast<uint64_t>(a.K) * 2, BK, BM,
                                  CU_TENSOR_MAP_SWIZZLE_128B);
   if (me != cudaSuccess) return me;
-  auto kern = gemm_kernel<BITS, OUT_BF16, TRANS>;
+  auto kern = gemm_kernel<E, BITS, OUT_BF16, TRANS>;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -659,22 +667,53 @@ cudaError_t launch_t(const uint16_t *x, const GemmArgs &a, cudaStream_t stream) 
   int64_t blocks = (mn / 4 + 255) / 256;
   if (blocks > 4 * sm_count()) blocks = 4 * sm_count();
   if (blocks < 1) blocks = 1;
-  splitk_finalize<OUT_BF16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.ws, a.splits, mn, a.y);
+  splitk_finalize<E, OUT_BF16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.ws, a.splits, mn, a.y);
   return cudaGetLastError();
 }
 
-template <int BITS>
-cudaError_t launch_bits(const uint16_t *x, const GemmArgs &a, bool transpose, bool y_bf16,
+template <typename E, int BITS>
+cudaError_t launch_bits(const uint16_t *x, const GemmArgs &a, bool transpose, bool y_16,
                         cudaStream_t stream) {
   if (transpose)
-    return y_bf16 ? launch_t<BITS, true, true>(x, a, stream) : launch_t<BITS, false, true>(x, a, stream);
-  return y_bf16 ? launch_t<BITS, true, false>(x, a, stream) : launch_t<BITS, false, false>(x, a, stream);
+    return y_16 ? launch_t<E, BITS, true, true>(x, a, stream) : launch_t<E, BITS, false, true>(x, a, stream);
+  return y_16 ? launch_t<E, BITS, true, false>(x, a, stream) : launch_t<E, BITS, false, false>(x, a, stream);
 }
 
-}  // namespace
+template <typename E>
+cudaError_t launch_any_bits(const uint16_t *x, const GemmArgs &a, int bits, bool transpose,
+                            bool y_16, cudaStream_t stream) {
+  switch (bits) {
+    case 1: return launch_bits<E, 1>(x, a, transpose, y_16, stream);
+    case 2: return launch_bits<E, 2>(x, a, transpose, y_16, stream);
+    case 3: return launch_bits<E, 3>(x, a, transpose, y_16, stream);
+    case 4: return launch_bits<E, 4>(x, a, transpose, y_16, stream);
+    case 5: return launch_bits<E, 5>(x, a, transpose, y_16, stream);
+    case 6: return launch_bits<E, 6>(x, a, transpose, y_16, stream);
+    case 8: return launch_bits<E, 8>(x, a, transpose, y_16, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
-cudaError_t launch_gemm(const uint16_t *x, int64_t M, const PackedWeight &w, bool transpose,
-                        void *y, bool y_bf16, cudaStream_t stream) {
+// x rows that TMA cannot address (K not a multiple of 8, possible when W is
+// stored [K, N]): the decode kernel over 16-row slices of x instead.
+template <typename E>
+cudaError_t gemv_slices(const uint16_t *x, int64_t M, const PackedWeight &w, bool transpose,
+                        int64_t N, int64_t K, void *y, bool y_16, cudaStream_t stream) {
+  const size_t ysz = y_16 ? 2 : 4;
+  for (int64_t m0 = 0; m0 < M; m0 += 16) {
+    const int64_t rows = M - m0 < 16 ? M - m0 : 16;
+    const uint16_t *xs = x + m0 * K;
+    void *ys = static_cast<char *>(y) + m0 * N * static_cast<int64_t>(ysz);
+    const cudaError_t e = E::kF16 ? launch_gemv_f16(xs, rows, w, transpose, ys, y_16, stream)
+                                  : launch_gemv(xs, rows, w, transpose, ys, y_16, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template <typename E>
+cudaError_t gemm_entry(const uint16_t *x, int64_t M, const PackedWeight &w, bool transpose,
+                       void *y, bool y_bf16, cudaStream_t stream) {
   GemmArgs a;
   a.w = w.w;
   a.scales = w.scales;
@@ -702,32 +741,25 @@ cudaError_t launch_gemm(const uint16_t *x, int64_t M, const PackedWeight &w, boo
       a.splits = 1;
     }
   }
-  cudaError_t e;
-  switch (w.bits) {
-    case 1: e = launch_bits<1>(x, a, transpose, y_bf16, stream); break;
-    case 2: e = launch_bits<2>(x, a, transpose, y_bf16, stream); break;
-    case 3: e = launch_bits<3>(x, a, transpose, y_bf16, stream); break;
-    case 4: e = launch_bits<4>(x, a, transpose, y_bf16, stream); break;
-    case 5: e = launch_bits<5>(x, a, transpose, y_bf16, stream); break;
-    case 6: e = launch_bits<6>(x, a, transpose, y_bf16, stream); break;
-    case 8: e = launch_bits<8>(x, a, transpose, y_bf16, stream); break;
-    default: e = cudaErrorInvalidValue;
-  }
+  cudaError_t e = launch_any_bits<E>(x, a, w.bits, transpose, y_bf16, stream);
   if (a.ws) {
     const cudaError_t fe = cudaFreeAsync(a.ws, stream);
     if (e == cudaSuccess) e = fe;
   }
   if (e != cudaErrorNotSupported) return e;
-  // x rows that TMA cannot address (K not a multiple of 8, possible when W is
-  // stored [K, N]): run the decode kernel over 16-row slices of x instead.
-  const size_t ysz = y_bf16 ? 2 : 4;
-  for (int64_t m0 = 0; m0 < M; m0 += 16) {
-    const int64_t rows = M - m0 < 16 ? M - m0 : 16;
-    e = launch_gemv(x + m0 * a.K, rows, w, transpose,
-                    static_cast<char *>(y) + m0 * static_cast<int64_t>(a.N) * ysz, y_bf16, stream);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  return gemv_slices<E>(x, M, w, transpose, a.N, a.K, y, y_bf16, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const uint16_t *x, int64_t M, const PackedWeight &w, bool transpose,
+                        void *y, bool y_bf16, cudaStream_t stream) {
+  return gemm_entry<ElemBF16>(x, M, w, transpose, y, y_bf16, stream);
+}
+
+cudaError_t launch_gemm_f16(const uint16_t *x, int64_t M, const PackedWeight &w, bool transpose,
+                            void *y, bool y_f16, cudaStream_t stream) {
+  return gemm_entry<ElemF16>(x, M, w, transpose, y, y_f16, stream);
 }
 
 // ------------------------------------------- static-scratch variant ----
@@ -783,26 +815,9 @@ cudaError_t launch_gemm_static_scratch(const uint16_t *x, int64_t M, const Packe
   *needed = a.splits > 1 ? splitk_bytes(a) : 0;
   if (*needed > static_scratch_bytes()) return cudaErrorInvalidValue;
   a.ws = a.splits > 1 ? scratch : nullptr;
-  cudaError_t e;
-  switch (w.bits) {
-    case 1: e = launch_bits<1>(x, a, transpose, y_bf16, stream); break;
-    case 2: e = launch_bits<2>(x, a, transpose, y_bf16, stream); break;
-    case 3: e = launch_bits<3>(x, a, transpose, y_bf16, stream); break;
-    case 4: e = launch_bits<4>(x, a, transpose, y_bf16, stream); break;
-    case 5: e = launch_bits<5>(x, a, transpose, y_bf16, stream); break;
-    case 6: e = launch_bits<6>(x, a, transpose, y_bf16, stream); break;
-    case 8: e = launch_bits<8>(x, a, transpose, y_bf16, stream); break;
-    default: e = cudaErrorInvalidValue;
-  }
+  const cudaError_t e = launch_any_bits<ElemBF16>(x, a, w.bits, transpose, y_bf16, stream);
   if (e != cudaErrorNotSupported) return e;
-  const size_t ysz = y_bf16 ? 2 : 4;
-  for (int64_t m0 = 0; m0 < M; m0 += 16) {
-    const int64_t rows = M - m0 < 16 ? M - m0 : 16;
-    e = launch_gemv(x + m0 * a.K, rows, w, transpose,
-                    static_cast<char *>(y) + m0 * static_cast<int64_t>(a.N) * ysz, y_bf16, stream);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  return gemv_slices<ElemBF16>(x, M, w, transpose, a.N, a.K, y, y_bf16, stream);
 }
 
 }  // namespace qmm

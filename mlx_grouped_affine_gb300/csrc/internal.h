@@ -15,12 +15,16 @@ constexpr unsigned kErrTimeoutBit = 2u;  // a bounded wait inside a kernel ran o
 constexpr unsigned kLaunchPdl = 1u;
 unsigned launch_flags();
 
+// Element types, numbered as the C ABI's qmm_dtype.
+constexpr int kTypeF32 = 0, kTypeBF16 = 1, kTypeF16 = 2;
+
 struct PackedWeight {
   const uint32_t *w;       // [rows, cols*bits/32]
-  const uint16_t *scales;  // bf16 [rows, cols/group]
-  const uint16_t *biases;  // bf16 [rows, cols/group]
+  const uint16_t *scales;  // [rows, cols/group] of sb_type (fp32 values when kTypeF32)
+  const uint16_t *biases;  // [rows, cols/group] of sb_type
   int64_t rows, cols;
   int group, bits;
+  int sb_type = kTypeBF16;
 };
 
 // The current device's error word (a static __device__ variable); its device
@@ -38,9 +42,9 @@ cudaError_t encode_map_2d(CUtensorMap *map, CUtensorMapDataType type, const void
 int sm_count();
 
 // dequant.cu: out[r, :] = dequant(W[src(r), :]) for r < out_rows, where
-// src(r) = idx[r] if idx is given (a rows gather) else r.
+// src(r) = idx[r] if idx is given (a rows gather) else r; out of out_type.
 cudaError_t launch_dequantize(const PackedWeight &w, const uint32_t *idx,
-                              int64_t out_rows, void *out, bool out_bf16,
+                              int64_t out_rows, void *out, int out_type,
                               cudaStream_t stream);
 
 // gemv.cu: decode path, M <= 16.
@@ -48,10 +52,17 @@ cudaError_t launch_gemv(const uint16_t *x, int64_t M, const PackedWeight &w,
                         bool transpose, void *y, bool y_bf16,
                         cudaStream_t stream);
 
+// gemv_f16.cu: the same for fp16 x, scales and biases (y fp16 if y_f16).
+cudaError_t launch_gemv_f16(const uint16_t *x, int64_t M, const PackedWeight &w,
+                            bool transpose, void *y, bool y_f16, cudaStream_t stream);
+
 // gemm_sm103.cu: tensor-core path for larger M.
 cudaError_t launch_gemm(const uint16_t *x, int64_t M, const PackedWeight &w,
                         bool transpose, void *y, bool y_bf16,
                         cudaStream_t stream);
+
+cudaError_t launch_gemm_f16(const uint16_t *x, int64_t M, const PackedWeight &w,
+                            bool transpose, void *y, bool y_f16, cudaStream_t stream);
 
 // gather_qmm: output batch b (of `batches`) is x[lhs[b]] (M x K, of
 // x_batches) times weight batch rhs[b] (of w_batches, each shaped as w);
@@ -73,11 +84,17 @@ cudaError_t launch_silu_gate(const uint16_t *gate, const uint16_t *up, int64_t M
                              const PackedWeight &w, const uint16_t *resid, void *y, bool y_bf16,
                              cudaStream_t stream);
 
-// quantize: bf16 w [rows, cols] (cols a multiple of group) -> packed
-// uint32 [rows, cols*bits/32], bf16 scales and biases [rows, cols/group].
-cudaError_t launch_quantize(const uint16_t *w, int64_t rows, int64_t cols, int group, int bits,
-                            uint32_t *packed, uint16_t *scales, uint16_t *biases,
+// quantize: w [rows, cols] of w_type (cols a multiple of group) -> packed
+// uint32 [rows, cols*bits/32], scales and biases [rows, cols/group] of w_type.
+cudaError_t launch_quantize(const void *w, int w_type, int64_t rows, int64_t cols, int group,
+                            int bits, uint32_t *packed, void *scales, void *biases,
                             cudaStream_t stream);
+
+// mm_f32.cu: quantized_matmul computed in fp32 on the CUDA cores, for x,
+// scales and biases that promote to fp32: x [M, K] of x_type, scales and
+// biases of w.sb_type, y fp32 [M, N].
+cudaError_t launch_mm_f32(const void *x, int x_type, int64_t M, const PackedWeight &w,
+                          bool transpose, float *y, cudaStream_t stream);
 
 // The variant of launch_gemm whose split-K partials go to `scratch` (the
 // library's static array, see static_scratch) instead of a stream-ordered

@@ -10,13 +10,15 @@ import ctypes
 from . import build as _build
 
 QMM_OK, QMM_ERR_INVALID_ARG, QMM_ERR_UNSUPPORTED, QMM_ERR_CUDA, QMM_ERR_INDEX, QMM_ERR_TIMEOUT = range(6)
-QMM_F32, QMM_BF16 = 0, 1
+QMM_F32, QMM_BF16, QMM_F16 = 0, 1, 2
 STATUS_NAMES = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED",
                 3: "QMM_ERR_CUDA", 4: "QMM_ERR_INDEX", 5: "QMM_ERR_TIMEOUT"}
 QMM_LAUNCH_PDL = 1
 EXPORTS = ("qmm_quantize", "qmm_dequantize", "qmm_quantized_matmul", "qmm_quantized_matmul_noalloc",
            "qmm_gather_qmm", "qmm_gemv_gate_up", "qmm_gemv_silu_gate", "qmm_rows",
-           "qmm_last_error", "qmm_get_device_error", "qmm_set_launch_flags")
+           "qmm_last_error", "qmm_get_device_error", "qmm_set_launch_flags",
+           "qmm_promote_types", "qmm_dequantize_typed", "qmm_rows_typed", "qmm_quantize_typed",
+           "qmm_quantized_matmul_typed")
 
 _lib = None
 
@@ -43,9 +45,15 @@ def lib():
         L.qmm_gemv_silu_gate.argtypes = [P, P, I64, P, P, P, I64, I64, I, I, P, P, I, P]
         L.qmm_rows.argtypes = [P, P, P, I64, I64, P, I64, I, I, P, I, P]
         L.qmm_get_device_error.argtypes = [P]
+        L.qmm_promote_types.argtypes = [I, I, ctypes.POINTER(I)]
+        L.qmm_dequantize_typed.argtypes = [P, P, P, I, I64, I64, I, I, P, I, P]
+        L.qmm_rows_typed.argtypes = [P, P, P, I, I64, I64, P, I64, I, I, P, I, P]
+        L.qmm_quantize_typed.argtypes = [P, I, I64, I64, I, I, P, P, P, P]
+        L.qmm_quantized_matmul_typed.argtypes = [P, I, I64, P, P, P, I, I64, I64, I, I, I, P, I, P]
         for f in ("qmm_quantize", "qmm_dequantize", "qmm_quantized_matmul", "qmm_quantized_matmul_noalloc",
                   "qmm_gather_qmm", "qmm_gemv_gate_up", "qmm_gemv_silu_gate", "qmm_rows",
-                  "qmm_get_device_error"):
+                  "qmm_get_device_error", "qmm_promote_types", "qmm_dequantize_typed",
+                  "qmm_rows_typed", "qmm_quantize_typed", "qmm_quantized_matmul_typed"):
             getattr(L, f).restype = I
         L.qmm_set_launch_flags.argtypes = [ctypes.c_uint]
         L.qmm_set_launch_flags.restype = ctypes.c_uint
@@ -145,3 +153,36 @@ def qmm_get_device_error(stream=None):
 def qmm_set_launch_flags(flags):
     """Set this host thread's launch flags (QMM_LAUNCH_PDL); returns the previous ones."""
     return int(lib().qmm_set_launch_flags(flags))
+
+
+def qmm_promote_types(a, b):
+    """The dtype that a and b promote to (host-only: no GPU needed)."""
+    out = ctypes.c_int(-1)
+    _check(lib().qmm_promote_types(a, b, ctypes.byref(out)))
+    return out.value
+
+
+def qmm_dequantize_typed(w, scales, biases, sb_dtype, rows, cols, group_size, bits, out,
+                         out_dtype, stream=None):
+    _check(lib().qmm_dequantize_typed(_ptr(w), _ptr(scales), _ptr(biases), sb_dtype, rows, cols,
+                                      group_size, bits, _ptr(out), out_dtype, _stream(stream)))
+
+
+def qmm_rows_typed(w, scales, biases, sb_dtype, table_rows, cols, idx, n, group_size, bits, out,
+                   out_dtype, stream=None):
+    _check(lib().qmm_rows_typed(_ptr(w), _ptr(scales), _ptr(biases), sb_dtype, table_rows, cols,
+                                _ptr(idx), n, group_size, bits, _ptr(out), out_dtype,
+                                _stream(stream)))
+
+
+def qmm_quantize_typed(w, w_dtype, rows, cols, group_size, bits, packed, scales, biases,
+                       stream=None):
+    _check(lib().qmm_quantize_typed(_ptr(w), w_dtype, rows, cols, group_size, bits, _ptr(packed),
+                                    _ptr(scales), _ptr(biases), _stream(stream)))
+
+
+def qmm_quantized_matmul_typed(x, x_dtype, M, w, scales, biases, sb_dtype, N, K, transpose,
+                               group_size, bits, y, y_dtype, stream=None):
+    _check(lib().qmm_quantized_matmul_typed(_ptr(x), x_dtype, M, _ptr(w), _ptr(scales),
+                                            _ptr(biases), sb_dtype, N, K, int(transpose),
+                                            group_size, bits, _ptr(y), y_dtype, _stream(stream)))

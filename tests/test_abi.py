@@ -133,3 +133,47 @@ def test_launch_flags_are_per_thread_and_checked():
     assert qmm.qmm_set_launch_flags(0x10 | qmm.QMM_LAUNCH_PDL) == qmm.QMM_LAUNCH_PDL
     assert "unknown flag" in qmm.qmm_last_error()
     assert qmm.qmm_set_launch_flags(0) == qmm.QMM_LAUNCH_PDL   # the unknown bit was dropped
+
+
+# -- typed calls (dtypes) ----------------------------------------------------------
+
+def test_promote_types_matches_the_oracle():
+    import oracle
+    names = {"f32": qmm.QMM_F32, "bf16": qmm.QMM_BF16, "f16": qmm.QMM_F16}
+    for a, qa in names.items():
+        for b, qb in names.items():
+            assert qmm.qmm_promote_types(qa, qb) == names[oracle.promote_types(a, b)], (a, b)
+    with pytest.raises(qmm.QmmError) as e:
+        qmm.qmm_promote_types(qmm.QMM_F16, 9)
+    assert e.value.status == qmm.QMM_ERR_UNSUPPORTED
+
+
+def mm_typed(**kw):
+    args = dict(x=A, xt=qmm.QMM_F16, M=1, w=A, s=A, b=A, st=qmm.QMM_F16, N=64, K=64, tr=1, G=32,
+                bits=4, y=A, dt=qmm.QMM_F16)
+    args.update(kw)
+    return qmm.lib().qmm_quantized_matmul_typed(
+        args["x"], args["xt"], args["M"], args["w"], args["s"], args["b"], args["st"], args["N"],
+        args["K"], args["tr"], args["G"], args["bits"], args["y"], args["dt"], S)
+
+
+def test_typed_calls_check_dtypes_before_launching():
+    U = qmm.QMM_ERR_UNSUPPORTED
+    L = qmm.lib()
+    # output: fp32 or the computed (promoted) type only
+    assert mm_typed(dt=qmm.QMM_BF16) == U
+    assert mm_typed(xt=qmm.QMM_BF16, dt=qmm.QMM_F16) == U          # bf16 x f16 -> f32
+    assert mm_typed(xt=qmm.QMM_BF16, dt=qmm.QMM_BF16) == U
+    assert mm_typed(xt=5) == U and mm_typed(st=-1) == U
+    assert "dtype" in qmm.qmm_last_error()
+    assert mm_typed(M=0, x=0, y=0) == qmm.QMM_OK
+    assert mm_typed(xt=qmm.QMM_BF16, dt=qmm.QMM_F32, M=0, x=0, y=0) == qmm.QMM_OK
+    assert mm_typed(x=A + 2) == BAD and mm_typed(G=48) == BAD
+    assert L.qmm_dequantize_typed(A, A, A, qmm.QMM_F16, 4, 64, 32, 4, A, qmm.QMM_BF16, S) == U
+    assert L.qmm_dequantize_typed(A, A, A, 3, 4, 64, 32, 4, A, qmm.QMM_F32, S) == U
+    assert L.qmm_dequantize_typed(A, A, A, qmm.QMM_F32, 0, 64, 32, 4, 0, qmm.QMM_F32, S) == qmm.QMM_OK
+    assert L.qmm_rows_typed(A, A, A, qmm.QMM_F16, 10, 64, A, 3, 64, 4, A, qmm.QMM_BF16, S) == U
+    assert L.qmm_rows_typed(A, A, A, qmm.QMM_F16, 10, 64, A, 0, 64, 4, A, qmm.QMM_F16, S) == qmm.QMM_OK
+    assert L.qmm_quantize_typed(A, 7, 4, 64, 32, 4, A, A, A, S) == U
+    assert L.qmm_quantize_typed(A, qmm.QMM_F32, 0, 64, 32, 4, A, A, A, S) == qmm.QMM_OK
+    assert L.qmm_quantize_typed(A, qmm.QMM_F32, 4, 48, 32, 4, A, A, A, S) == BAD

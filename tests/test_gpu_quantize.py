@@ -70,3 +70,19 @@ def test_quantize_then_dequantize_round_trip():
     step = np.repeat((s.astype(np.uint32) << 16).view(np.float32).astype(np.float64), gs, axis=1)
     top = (1 << bits) - 1
     assert (np.abs(back - wf) <= 0.5 * step * (1 + 1e-3) + top * 2.0 ** -9 * step + 1e-6).all()
+
+
+@pytest.mark.parametrize("bits", (2, 4, 8))
+def test_quantize_exact_half_way_quotients(bits):
+    """Groups built so that (w - bias) / scale is exactly n + 1/2 for many w:
+    bias 0, maximum 2^bits - 1, so the scale is exactly 1, and the other values
+    are half-integers (exact in bf16 below 128).  Ties go to the even code on
+    both sides; the kernel must take its exact route for them."""
+    rows, cols, gs = 3, 128, 64
+    top = (1 << bits) - 1
+    g = np.random.default_rng(97 + bits)
+    halves = (g.integers(0, min(top, 127), size=(rows, cols)) + 0.5).astype(np.float32)
+    halves[:, ::gs] = 0.0
+    halves[:, 1::gs] = float(min(top, 127)) if bits < 8 else 127.0
+    w = (halves.view(np.uint32) >> 16).astype(np.uint16)
+    check(w, rows, cols, gs, bits, "half-way quotients bits=%d" % bits)
