@@ -657,7 +657,7 @@ PROFILE_CASES = {
     "splitk_m128": (128, 4096, 4096, 4, 64, True),
 }
 OTHER_PROFILES = ("gather_sorted", "silu_gate", "quantize", "dequantize", "rows", "f16_prefill",
-                  "f16_decode", "f32_decode", "f32_prefill")
+                  "f16_decode", "f32_decode", "f32_decode16", "f32_prefill")
 
 
 def run_other_profile(case, launches):
@@ -703,13 +703,14 @@ def run_other_profile(case, launches):
         o = torch.empty((N, K), dtype=torch.int16, device="cuda")
         for i in range(launches):
             qmm.qmm_dequantize(*cs[i % R], N, K, 64, 4, o, qmm.QMM_BF16)
-    elif case in ("f16_prefill", "f16_decode", "f32_decode", "f32_prefill"):
+    elif case in ("f16_prefill", "f16_decode", "f32_decode", "f32_decode16", "f32_prefill"):
         d = case[:3]
         Q = {"f16": qmm.QMM_F16, "f32": qmm.QMM_F32}[d]
-        M, N, K = (2048, 14336, 4096) if case.endswith("prefill") else (1, 4096, 4096)
+        M, N, K = ((2048, 14336, 4096) if case.endswith("prefill") else
+                   (16, 4096, 4096) if case.endswith("16") else (1, 4096, 4096))
         w = synth.quant_weight_typed(150, N, K, 4, 64, d)
         nw = w.packed.nbytes + w.scales.nbytes + w.biases.nbytes
-        R = max(2, -(-3 * L2_BYTES // nw)) if M == 1 else 2
+        R = max(2, -(-3 * L2_BYTES // nw)) if M <= 16 else 2
         tdev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(
             {np.dtype(np.uint32): np.int32, np.dtype(np.uint16): np.int16,
              np.dtype(np.float32): np.float32}[a.dtype])).cuda()

@@ -21,6 +21,8 @@
 // When the tiles are too few to fill the GPU (small M or N), K is split over
 // grid z; each slice writes fp32 partials to a stream-ordered workspace and
 // a second kernel adds them in slice order, so results repeat bit for bit.
+// At M <= 16 with W stored [N, K] a GEMV form (mm_f32_gemv_kernel, below)
+// replaces the tiles.
 #include "common.cuh"
 #include "internal.h"
 
@@ -35,6 +37,18 @@ __device__ __forceinline__ float load_elem(const void *p, int t, int64_t i) {
   if (t == kTypeF32) return __ldg(static_cast<const float *>(p) + i);
   const uint32_t h = __ldg(static_cast<const uint16_t *>(p) + i);
   return t == kTypeF16 ? ElemF16::to_f32(h) : ElemBF16::to_f32(h);
+}
+
+// Elements i .. i+3 of an array of type t (i a multiple of 4, 16-byte
+// aligned rows), in fp32.
+__device__ __forceinline__ float4 load4(const void *p, int t, int64_t i) {
+  if (t == kTypeF32) return __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(p) + i));
+  const uint2 u = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(p) + i));
+  if (t == kTypeF16)
+    return make_float4(ElemF16::to_f32(u.x & 0xFFFFu), ElemF16::to_f32(u.x >> 16),
+                       ElemF16::to_f32(u.y & 0xFFFFu), ElemF16::to_f32(u.y >> 16));
+  return make_float4(ElemBF16::to_f32(u.x & 0xFFFFu), ElemBF16::to_f32(u.x >> 16),
+                     ElemBF16::to_f32(u.y & 0xFFFFu), ElemBF16::to_f32(u.y >> 16));
 }
 
 struct MmArgs {
@@ -210,6 +224,86 @@ __global__ void __launch_bounds__(kThreads) mm_f32_kernel(MmArgs a) {
   }
 }
 
+// Decode form (M <= 16, W stored [N, K]): no shared-memory round trip for the
+// weights.  A block owns 32 rows of W and a K slice of at most kGemvSteps steps
+// of 64 codes; thread (r, q) = (t / 8, t % 8) takes octet q of every step of
+// row r (the 8 threads of a row read its 64 codes of a step as consecutive
+// words), issues all of its octets' loads at once, then dequantizes each
+// octet and multiplies it into MT accumulators against x, which the block
+// stages in shared memory once (MT x slice, fp32).  The 8 partial sums of a
+// row meet by warp shuffles.
+constexpr int kGemvSteps = 8;  // 64-code steps per block at most (512 codes)
+
+template <int BITS, int MT>
+__global__ void __launch_bounds__(kThreads) mm_f32_gemv_kernel(MmArgs a) {
+  constexpr int KS = 64 * kGemvSteps;
+  __shared__ __align__(16) float xs[MT][KS];
+  const int t = threadIdx.x, r = t >> 3, q = t & 7;
+  const int n = blockIdx.x * 32 + r;
+  const int kb0 = blockIdx.z * a.steps_per_split;  // first 64-code step
+  const int nsteps = min(a.steps_per_split, (a.K + 63) / 64 - kb0);
+  Octet oct[kGemvSteps];
+#pragma unroll
+  for (int i = 0; i < kGemvSteps; ++i) {
+    oct[i] = Octet{0u, 0u, 0u, 0.0f, 0.0f};
+    if (i < nsteps) oct[i] = fetch_octet<BITS, true>(a, n, (kb0 + i) * 64 + 8 * q);
+  }
+  // x rows of the slice, widened exactly (zero beyond M and K), four values
+  // a load; every load is issued before the first store.
+  const int k0 = kb0 * 64;
+  constexpr int NV = MT * KS / 4, NJ = (NV + kThreads - 1) / kThreads;
+  float4 xv[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int e = 4 * (t + kThreads * j), m = e / KS, k = e - m * KS;
+    xv[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (e < MT * KS && m < a.M && k < nsteps * 64 && k0 + k < a.K)
+      xv[j] = load4(a.x, a.x_type, static_cast<int64_t>(m) * a.K + k0 + k);
+  }
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int e = 4 * (t + kThreads * j);
+    if (e < MT * KS) *reinterpret_cast<float4 *>(&xs[e / KS][e % KS]) = xv[j];
+  }
+  __syncthreads();
+  float acc[MT];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kGemvSteps; ++i) {
+    if (i < nsteps) {
+      float v[8];
+      dequant_octet<BITS>(oct[i], v);
+      const int kk = 64 * i + 8 * q;
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        const float4 x0 = *reinterpret_cast<const float4 *>(&xs[m][kk]);
+        const float4 x1 = *reinterpret_cast<const float4 *>(&xs[m][kk + 4]);
+        float s = acc[m];
+        s = __fmaf_rn(v[0], x0.x, s); s = __fmaf_rn(v[1], x0.y, s);
+        s = __fmaf_rn(v[2], x0.z, s); s = __fmaf_rn(v[3], x0.w, s);
+        s = __fmaf_rn(v[4], x1.x, s); s = __fmaf_rn(v[5], x1.y, s);
+        s = __fmaf_rn(v[6], x1.z, s); s = __fmaf_rn(v[7], x1.w, s);
+        acc[m] = s;
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    float s = acc[m];
+    s += __shfl_xor_sync(0xffffffffu, s, 4);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    acc[m] = s;
+  }
+  if (q == 0 && n < a.N) {
+    float *out = a.y + static_cast<int64_t>(blockIdx.z) * a.M * a.N;
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+      if (m < a.M) out[static_cast<int64_t>(m) * a.N + n] = acc[m];
+  }
+}
+
 // y = the sum of the `splits` partial slices, in slice order.
 __global__ void __launch_bounds__(256)
 mm_f32_finalize(const float *__restrict__ ws, int splits, int64_t mn, float *__restrict__ y) {
@@ -221,22 +315,11 @@ mm_f32_finalize(const float *__restrict__ ws, int splits, int64_t mn, float *__r
   }
 }
 
-template <int BITS, int BM, int BN, int PF, bool TRANS>
-cudaError_t launch_cfg(MmArgs a, cudaStream_t stream) {
-  const int64_t mt = (a.M + BM - 1) / BM, nt = (a.N + BN - 1) / BN;
-  if (mt > 65535) return cudaErrorInvalidValue;
-  const int nk = (a.K + BK - 1) / BK;
-  // Split K until the blocks cover the SMs four times, keeping at least PF
-  // (and 4) steps a slice.
-  const int64_t want = 4 * static_cast<int64_t>(sm_count());
-  const int min_steps = PF > 4 ? PF : 4;
-  int splits = 1;
-  if (mt * nt < want) {
-    splits = static_cast<int>((want + mt * nt - 1) / (mt * nt));
-    if (splits > nk / min_steps) splits = nk / min_steps;
-    if (splits > 64) splits = 64;
-    if (splits < 1) splits = 1;
-  }
+// Launch kern over grid (gx, gy, splits) with a.steps_per_split steps a
+// slice; partials through a stream-ordered workspace when splits > 1.
+template <typename Kern>
+cudaError_t launch_split(Kern kern, MmArgs a, unsigned gx, unsigned gy, int nk, int splits,
+                         cudaStream_t stream) {
   a.steps_per_split = (nk + splits - 1) / splits;
   splits = (nk + a.steps_per_split - 1) / a.steps_per_split;
   float *y = a.y;
@@ -244,17 +327,14 @@ cudaError_t launch_cfg(MmArgs a, cudaStream_t stream) {
   const int64_t mn = static_cast<int64_t>(a.M) * a.N;
   if (splits > 1) {
     void *p = nullptr;
-    if (cudaMallocAsync(&p, static_cast<size_t>(splits) * mn * sizeof(float), stream) == cudaSuccess) {
-      ws = static_cast<float *>(p);
-      a.y = ws;
-    } else {
+    if (cudaMallocAsync(&p, static_cast<size_t>(splits) * mn * sizeof(float), stream) != cudaSuccess) {
       cudaGetLastError();
-      splits = 1;
-      a.steps_per_split = nk;
+      return cudaErrorMemoryAllocation;
     }
+    ws = static_cast<float *>(p);
+    a.y = ws;
   }
-  mm_f32_kernel<BITS, BM, BN, PF, TRANS>
-      <<<dim3(static_cast<unsigned>(nt), static_cast<unsigned>(mt), splits), kThreads, 0, stream>>>(a);
+  kern<<<dim3(gx, gy, splits), kThreads, 0, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (ws) {
     if (e == cudaSuccess) {
@@ -269,11 +349,49 @@ cudaError_t launch_cfg(MmArgs a, cudaStream_t stream) {
   return e;
 }
 
+template <int BITS, int BM, int BN, int PF, bool TRANS>
+cudaError_t launch_cfg(const MmArgs &a, cudaStream_t stream) {
+  const int64_t mt = (a.M + BM - 1) / BM, nt = (a.N + BN - 1) / BN;
+  if (mt > 65535) return cudaErrorInvalidValue;
+  const int nk = (a.K + BK - 1) / BK;
+  // Split K until the blocks cover the SMs four times, keeping at least PF
+  // (and 4) steps a slice.
+  const int64_t want = 4 * static_cast<int64_t>(sm_count());
+  const int min_steps = PF > 4 ? PF : 4;
+  int splits = 1;
+  if (mt * nt < want) {
+    splits = static_cast<int>((want + mt * nt - 1) / (mt * nt));
+    if (splits > nk / min_steps) splits = nk / min_steps;
+    if (splits > 64) splits = 64;
+    if (splits < 1) splits = 1;
+  }
+  cudaError_t e = launch_split(mm_f32_kernel<BITS, BM, BN, PF, TRANS>, a, static_cast<unsigned>(nt),
+                               static_cast<unsigned>(mt), nk, splits, stream);
+  if (e == cudaErrorMemoryAllocation && splits > 1)  // no workspace: one slice
+    e = launch_split(mm_f32_kernel<BITS, BM, BN, PF, TRANS>, a, static_cast<unsigned>(nt),
+                     static_cast<unsigned>(mt), nk, 1, stream);
+  return e;
+}
+
+// The decode form: slices of at most kGemvSteps 64-code steps, so K is always
+// split when it exceeds 512 (the workspace is then required).
+template <int BITS, int MT>
+cudaError_t launch_gemv_cfg(const MmArgs &a, cudaStream_t stream) {
+  const int nk = (a.K + 63) / 64;
+  const int splits = (nk + kGemvSteps - 1) / kGemvSteps;
+  return launch_split(mm_f32_gemv_kernel<BITS, MT>, a, static_cast<unsigned>((a.N + 31) / 32), 1u,
+                      nk, splits, stream);
+}
+
 template <int BITS>
 cudaError_t launch_bits(const MmArgs &a, bool transpose, cudaStream_t stream) {
-  if (a.M <= 16)
-    return transpose ? launch_cfg<BITS, 16, 128, 6, true>(a, stream)
-                     : launch_cfg<BITS, 16, 128, 6, false>(a, stream);
+  if (a.M <= 16 && transpose) {
+    if (a.M == 1) return launch_gemv_cfg<BITS, 1>(a, stream);
+    if (a.M <= 4) return launch_gemv_cfg<BITS, 4>(a, stream);
+    if (a.M <= 8) return launch_gemv_cfg<BITS, 8>(a, stream);
+    return launch_gemv_cfg<BITS, 16>(a, stream);
+  }
+  if (a.M <= 16) return launch_cfg<BITS, 16, 128, 6, false>(a, stream);
   return transpose ? launch_cfg<BITS, 128, 128, 1, true>(a, stream)
                    : launch_cfg<BITS, 128, 128, 1, false>(a, stream);
 }
