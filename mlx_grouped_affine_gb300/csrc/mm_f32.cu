@@ -231,7 +231,8 @@ __global__ void __launch_bounds__(kThreads) mm_f32_kernel(MmArgs a) {
 // words), issues all of its octets' loads at once, then dequantizes each
 // octet and multiplies it into MT accumulators against x, which the block
 // stages in shared memory once (MT x slice, fp32).  The 8 partial sums of a
-// row meet by warp shuffles.
+// row meet by warp shuffles.  At M = 16 the x reads from shared memory bound
+// the kernel, so x is laid out for conflict-free reads (see the staging).
 constexpr int kGemvSteps = 8;  // 64-code steps per block at most (512 codes)
 
 template <int BITS, int MT>
@@ -260,10 +261,17 @@ __global__ void __launch_bounds__(kThreads) mm_f32_gemv_kernel(MmArgs a) {
     if (e < MT * KS && m < a.M && k < nsteps * 64 && k0 + k < a.K)
       xv[j] = load4(a.x, a.x_type, static_cast<int64_t>(m) * a.K + k0 + k);
   }
+  // Within each 64-value step, value 8q + 4h + j (octet q, half h) sits at
+  // 32h + 4q + j: the 8 threads of a row then read 128 contiguous bytes per
+  // half, one shared-memory wavefront without bank conflicts.
 #pragma unroll
   for (int j = 0; j < NJ; ++j) {
     const int e = 4 * (t + kThreads * j);
-    if (e < MT * KS) *reinterpret_cast<float4 *>(&xs[e / KS][e % KS]) = xv[j];
+    if (e < MT * KS) {
+      const int k = e % KS, rem = k & 63;
+      const int pos = (k & ~63) + 32 * ((rem >> 2) & 1) + 4 * (rem >> 3);
+      *reinterpret_cast<float4 *>(&xs[e / KS][pos]) = xv[j];
+    }
   }
   __syncthreads();
   float acc[MT];
@@ -274,11 +282,11 @@ __global__ void __launch_bounds__(kThreads) mm_f32_gemv_kernel(MmArgs a) {
     if (i < nsteps) {
       float v[8];
       dequant_octet<BITS>(oct[i], v);
-      const int kk = 64 * i + 8 * q;
+      const int kk = 64 * i + 4 * q;  // the octet's two halves, permuted as staged
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
         const float4 x0 = *reinterpret_cast<const float4 *>(&xs[m][kk]);
-        const float4 x1 = *reinterpret_cast<const float4 *>(&xs[m][kk + 4]);
+        const float4 x1 = *reinterpret_cast<const float4 *>(&xs[m][kk + 32]);
         float s = acc[m];
         s = __fmaf_rn(v[0], x0.x, s); s = __fmaf_rn(v[1], x0.y, s);
         s = __fmaf_rn(v[2], x0.z, s); s = __fmaf_rn(v[3], x0.w, s);

@@ -244,3 +244,20 @@ def test_matmul_typed_full_size_sampled(x_dt, sb_dt, M):
     ref, absy = oracle.qmm_sampled(x, M, w.packed, w.scales, w.biases, N, K, True, 64, 4, ms, ns,
                                    x_dtype=x_dt, sb_dtype=sb_dt)
     check_mm(got[ms, ns], ref, absy, d, d, K, "full %s x %s M=%d" % (x_dt, sb_dt, M))
+
+
+@pytest.mark.parametrize("M,transpose", ((1, True), (16, True), (3, False), (200, True)))
+def test_matmul_f32_split_k_repeats_bit_for_bit_and_long_k(M, transpose):
+    """K = 14336 splits the fp32 path's K range over many blocks (28 slices of
+    512 at M <= 16); the slices are added in a fixed order, so two calls give
+    the same bits, and the result meets the fp32 bound for that K."""
+    N, K, gs, bits = 256, 14336, 128, 4
+    w = synth.quant_weight_typed(950 + M, N if transpose else K, K if transpose else N, bits, gs,
+                                 "f32")
+    x = synth.x_typed(951 + M, M, K, "f32")
+    a = run_mm(x, "f32", M, w, N, K, transpose, "f32")
+    b = run_mm(x, "f32", M, w, N, K, transpose, "f32")
+    assert (a.view(np.uint64) == b.view(np.uint64)).all()
+    ref, absy = oracle.qmm(x, M, w.packed, w.scales, w.biases, N, K, transpose, gs, bits,
+                           x_dtype="f32", sb_dtype="f32")
+    check_mm(a, ref, absy, "f32", "f32", K, "f32 long K M=%d T=%s" % (M, transpose))
