@@ -290,7 +290,8 @@ def gather_detail(torch, qmm, synth, peaks, warmup):
     """Mixture-of-experts decode through gather_qmm: 8 experts [14336, 4096]
     4-bit g64, 32 routed token slots (16 tokens x top 2, one x row each),
     indices drawn once (seeded).  GB/s counts the bytes of the experts used
-    (each read once) plus x and y; sorted = the slots grouped by expert."""
+    (each read once) plus x and y; sorted = the slots grouped by expert.  Then
+    the prefill form: 4096 sorted slots on the same experts."""
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(
         {np.dtype(np.uint32): np.int32, np.dtype(np.uint16): np.int16}[a.dtype])).cuda()
     E, N, K, B = 8, 14336, 4096, 32
@@ -314,7 +315,21 @@ def gather_detail(torch, qmm, synth, peaks, warmup):
         out["gather_qmm_moe_8x%dx%d_b4_32slots_%s" % (N, K, name)] = {
             "us": round(t * 1e3, 2), "experts_used": used, "GB/s": round(nbytes / (t * 1e-3) / 1e9, 1),
             "frac_hbm": round(nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
-    del packed, sc, bi
+    # Prefill: 2048 tokens x top 2 = 4096 sorted slots (the grouped tensor-core
+    # path); TFLOP/s = 2 * slots * N * K.
+    B = 4096
+    rhs = dev(np.sort(synth.indices(123, B, E)).astype(np.uint32))
+    x = dev(synth.x_bf16(124, B, K))
+    y = torch.empty((B, 1, N), dtype=torch.int16, device="cuda")
+
+    def prefill():
+        qmm.qmm_gather_qmm(x, B, 1, packed, sc, bi, E, N, K, None, rhs, B, 1, 64, 4, 1, y,
+                           qmm.QMM_BF16)
+    t = time_graph(torch, graph_of(torch, prefill), 10, warmup)
+    tf = 2.0 * B * N * K / (t * 1e-3) / 1e12
+    out["gather_qmm_moe_prefill_8x%dx%d_b4_%dslots_sorted" % (N, K, B)] = {
+        "us": round(t * 1e3, 1), "TFLOP/s": round(tf, 1), "frac_bf16": round(tf / peaks["bf16_tflops"], 4)}
+    del packed, sc, bi, x, y
     torch.cuda.empty_cache()
     return out
 

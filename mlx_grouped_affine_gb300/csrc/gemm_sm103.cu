@@ -79,7 +79,25 @@ struct GemmArgs {
   int splits;   // K ranges per output tile (split-K when > 1)
   float *ws;    // split-K partials: slice s at ws + s * M * N, fp32 [M, N]
   unsigned *err;
+  // Grouped mode (gather_qmm over sorted expert runs) when plan is not null:
+  // plan[0] = the row tiles in use, then per row tile i (expert, first row,
+  // end row) at plan[1 + 3i]; expert e's weights sit w_bstride words and
+  // sb_bstride scale elements after expert e - 1's.  m_tiles is then read
+  // from the plan on the device.
+  const int *plan = nullptr;
+  int64_t w_bstride = 0, sb_bstride = 0;
 };
+
+// The rows [row0, row_end) of x and y one row tile covers, and its weight batch.
+struct RowTile {
+  int row0, row_end, expert;
+};
+
+__device__ __forceinline__ RowTile row_tile(const GemmArgs &a, int mi) {
+  if (!a.plan) return RowTile{mi * BM, min(a.M, mi * BM + BM), 0};
+  const int *p = a.plan + 1 + 3 * mi;
+  return RowTile{__ldg(p + 1), __ldg(p + 2), __ldg(p)};
+}
 
 // A unit of work: one output tile over one K range (k-blocks [kb0, kb1)).
 struct Unit {
@@ -223,7 +241,8 @@ struct ItemLoad {
 // (stored [N, K] when TRANS, else [K, N]; codes and groups run along the
 // stored columns).  Words past the end of the row read as zero.
 template <int BITS, bool TRANS>
-__device__ __forceinline__ void load_item(const GemmArgs &a, int row, int col, ItemLoad<BITS> &it) {
+__device__ __forceinline__ void load_item(const GemmArgs &a, int row, int col, int expert,
+                                          ItemLoad<BITS> &it) {
   const int rows = TRANS ? a.N : a.K, cols = TRANS ? a.K : a.N;
 #pragma unroll
   for (int i = 0; i < BITS; ++i) it.v[i] = 0u;
@@ -231,7 +250,7 @@ __device__ __forceinline__ void load_item(const GemmArgs &a, int row, int col, I
   if (row < rows && col < cols) {
     const int64_t wpr = (static_cast<int64_t>(cols) * BITS) >> 5;
     const int64_t w0 = static_cast<int64_t>(row) * wpr + (col >> 5) * BITS;
-    const uint32_t *rp = a.w + w0;
+    const uint32_t *rp = a.w + expert * a.w_bstride + w0;
     constexpr int kAlign = BITS % 4 == 0 ? 4 : BITS % 2 == 0 ? 2 : 1;  // words
     if ((col >> 5) * BITS + BITS <= wpr && (w0 & (kAlign - 1)) == 0) {
       load_words<BITS>(rp, it.v);
@@ -241,7 +260,8 @@ __device__ __forceinline__ void load_item(const GemmArgs &a, int row, int col, I
       for (int i = 0; i < BITS; ++i)
         if (i < left) it.v[i] = __ldg(rp + i);
     }
-    const int64_t g = static_cast<int64_t>(row) * (cols >> a.group_shift) + (col >> a.group_shift);
+    const int64_t g = expert * a.sb_bstride + static_cast<int64_t>(row) * (cols >> a.group_shift) +
+                      (col >> a.group_shift);
     it.sb = __ldg(a.scales + g) | (static_cast<uint32_t>(__ldg(a.biases + g)) << 16);
   }
 }
@@ -306,7 +326,7 @@ __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int
     int row, col;
     uint32_t off[4];
     item_place<TRANS>(dt, (pu.tile / a.m_tiles) * BN, pkb, row, col, off);
-    load_item<BITS, TRANS>(a, row, col, buf);
+    load_item<BITS, TRANS>(a, row, col, a.plan ? row_tile(a, pu.tile % a.m_tiles).expert : 0, buf);
     advance(punit, pu, pkb);
   };
   ItemLoad<BITS> buf[kLoadAhead];
@@ -382,7 +402,7 @@ __device__ void tma_role(const CUtensorMap *tmap, const GemmArgs &a, uint8_t *sA
   bool ok = true;
   for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
     const Unit un = unit_of(a, u, nk);
-    const int m0 = (un.tile % a.m_tiles) * BM;
+    const int m0 = row_tile(a, un.tile % a.m_tiles).row0;
     for (int kb = un.kb0; kb < un.kb1; ++kb) {
       if (!wait_warp(&bars->empty_a[s], ph ^ 1u, abort, a.err)) { ok = false; break; }
       if (lane == 0) {
@@ -423,7 +443,8 @@ __device__ void mma_role(const GemmArgs &a, uint8_t *sA, uint8_t *sB, Barriers *
     if (!wait_warp(&bars->tmem_empty, (it & 1) ^ 1u, abort, a.err)) break;
     tc_fence_after();
     // The second 128-row half only when this tile has x rows there.
-    const bool two = (un.tile % a.m_tiles) * BM + UM < a.M;
+    const RowTile rt = row_tile(a, un.tile % a.m_tiles);
+    const bool two = rt.row0 + UM < rt.row_end;
     for (int kb = un.kb0; kb < un.kb1; ++kb) {
       if (!wait_warp(&bars->full_a[sa], pha, abort, a.err) ||
           !wait_warp(&bars->full_b[sb], phb, abort, a.err)) {
@@ -474,15 +495,16 @@ __device__ void epilogue_role(const GemmArgs &a, Barriers *bars, uint32_t tmem) 
     tc_fence_after();
     const int tile = u / a.splits, split = u - tile * a.splits;
     const int n0 = (tile / a.m_tiles) * BN;
+    const RowTile rt = row_tile(a, tile % a.m_tiles);
 #pragma unroll 1
     for (int hc = 0; hc < 2 * (BN / 32); ++hc) {
       const int half = hc / (BN / 32), cc = hc % (BN / 32);
-      const int m = (tile % a.m_tiles) * BM + UM * half + 32 * q + lane;
-      if (half == 1 && (tile % a.m_tiles) * BM + UM >= a.M) break;  // no second half
+      const int m = rt.row0 + UM * half + 32 * q + lane;
+      if (half == 1 && rt.row0 + UM >= rt.row_end) break;  // no second half
       uint32_t r[32];
       tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(half * BN + 32 * cc), r);
       const int n = n0 + 32 * cc;
-      if (m >= a.M || n >= a.N) continue;
+      if (m >= rt.row_end || n >= a.N) continue;
       const int64_t o = static_cast<int64_t>(m) * a.N + n;
       if (a.splits > 1) {
         // A partial of a split tile: fp32 into this split's slice.
@@ -538,6 +560,8 @@ __device__ void epilogue_role(const GemmArgs &a, Barriers *bars, uint32_t tmem) 
 template <typename E, int BITS, bool OUT_BF16, bool TRANS>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, GemmArgs a) {
+  // Grouped mode: the row tiles in use, as the plan kernel counted them.
+  if (a.plan) a.m_tiles = __ldg(a.plan);
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -760,6 +784,121 @@ cudaError_t launch_gemm(const uint16_t *x, int64_t M, const PackedWeight &w, boo
 cudaError_t launch_gemm_f16(const uint16_t *x, int64_t M, const PackedWeight &w, bool transpose,
                             void *y, bool y_f16, cudaStream_t stream) {
   return gemm_entry<ElemF16>(x, M, w, transpose, y, y_f16, stream);
+}
+
+// ------------------------------------------------- grouped (MoE) mode ----
+// gather_qmm with sorted weight-batch indices, one x row per batch and no
+// lhs indices (nuvec_core quantized.rs, `gather_qmm` and `sorted_offsets`:
+// sorted indices let each expert's weights be walked once): batch b is x row
+// b times expert rhs[b], so expert e's batches are one run of consecutive x
+// and y rows.  A one-block plan kernel finds the runs (binary search in the
+// sorted indices), cuts them into row tiles of BM and writes the plan; the
+// GEMM then walks (row tile, column tile) units of every expert.  Indices past
+// the last expert zero their y rows and raise the index bit.
+namespace {
+
+__device__ __forceinline__ int lower_bound_rhs(const uint32_t *v, int n, uint32_t key) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(v + mid) < key) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+constexpr int kPlanThreads = 256;
+
+// Dynamic shared memory: 2 * w_batches ints (row tiles of each expert, then
+// its first plan entry).  The entries never exceed cap (1 + 3 * cap ints of
+// plan), whatever the indices hold: unsorted indices give wrong runs, never
+// writes outside the plan.
+__global__ void __launch_bounds__(kPlanThreads)
+group_plan_kernel(const uint32_t *rhs, int batches, int w_batches, int cap, int *plan, void *y,
+                  int N, int ysz, unsigned *err) {
+  extern __shared__ int sp[];
+  int *count = sp, *first = sp + w_batches;
+  const int t = threadIdx.x;
+  for (int e = t; e < w_batches; e += kPlanThreads) {
+    const int l = lower_bound_rhs(rhs, batches, static_cast<uint32_t>(e));
+    const int h = lower_bound_rhs(rhs, batches, static_cast<uint32_t>(e) + 1u);
+    count[e] = h > l ? (h - l + BM - 1) / BM : 0;
+  }
+  __syncthreads();
+  if (t == 0) {
+    int total = 0;
+    for (int e = 0; e < w_batches; ++e) {
+      const int n = min(count[e], cap - total);
+      count[e] = n;
+      first[e] = total;
+      total += n;
+    }
+    plan[0] = total;
+  }
+  __syncthreads();
+  for (int e = t; e < w_batches; e += kPlanThreads) {
+    const int l = lower_bound_rhs(rhs, batches, static_cast<uint32_t>(e));
+    const int h = lower_bound_rhs(rhs, batches, static_cast<uint32_t>(e) + 1u);
+    for (int j = 0; j < count[e]; ++j) {
+      const int i = first[e] + j, r0 = l + j * BM;
+      plan[1 + 3 * i] = e;
+      plan[2 + 3 * i] = r0;
+      plan[3 + 3 * i] = min(h, r0 + BM);
+    }
+  }
+  // Batches whose index is past the last expert: zero rows, index bit.
+  const int tail = lower_bound_rhs(rhs, batches, static_cast<uint32_t>(w_batches));
+  if (tail < batches) {
+    const int64_t n0 = static_cast<int64_t>(tail) * N, n1 = static_cast<int64_t>(batches) * N;
+    for (int64_t i = n0 + t; i < n1; i += kPlanThreads) {
+      if (ysz == 2) static_cast<uint16_t *>(y)[i] = 0;
+      else static_cast<float *>(y)[i] = 0.0f;
+    }
+    if (t == 0) atomicOr(err, kErrIndexBit);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_grouped(const uint16_t *x, int64_t batches, const PackedWeight &w,
+                                int64_t w_batches, const uint32_t *rhs, void *y, bool y_bf16,
+                                cudaStream_t stream) {
+  if (w_batches > 4096 || batches >= (int64_t(1) << 30) || (w.cols * 2) % 16 != 0)
+    return cudaErrorNotSupported;
+  GemmArgs a;
+  a.w = w.w;
+  a.scales = w.scales;
+  a.biases = w.biases;
+  a.y = y;
+  a.M = static_cast<int>(batches);
+  a.N = static_cast<int>(w.rows);
+  a.K = static_cast<int>(w.cols);
+  a.group_shift = w.group == 32 ? 5 : w.group == 64 ? 6 : 7;
+  // An upper bound of the row tiles (the grid's size); the kernel reads the
+  // actual count from the plan.
+  a.m_tiles = static_cast<int>((batches + BM - 1) / BM + w_batches);
+  a.n_tiles = (a.N + BN - 1) / BN;
+  a.splits = 1;
+  a.ws = nullptr;
+  a.err = device_error_word();
+  if (!a.err) return cudaErrorInvalidSymbol;
+  a.w_bstride = w.rows * ((w.cols * w.bits) / 32);
+  a.sb_bstride = w.rows * (w.cols / w.group);
+  void *p = nullptr;
+  cudaError_t e = cudaMallocAsync(&p, sizeof(int) * (1 + 3 * static_cast<size_t>(a.m_tiles)), stream);
+  if (e != cudaSuccess) return e;
+  int *plan = static_cast<int *>(p);
+  const size_t plan_smem = 2 * sizeof(int) * static_cast<size_t>(w_batches);
+  group_plan_kernel<<<1, kPlanThreads, plan_smem, stream>>>(
+      rhs, static_cast<int>(batches), static_cast<int>(w_batches), a.m_tiles, plan, y, a.N,
+      y_bf16 ? 2 : 4, a.err);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) {
+    a.plan = plan;
+    e = launch_any_bits<ElemBF16>(x, a, w.bits, true, y_bf16, stream);
+  }
+  const cudaError_t fe = cudaFreeAsync(plan, stream);
+  return e != cudaSuccess ? e : fe;
 }
 
 // ------------------------------------------- static-scratch variant ----

@@ -162,6 +162,12 @@ cudaError_t launch_gather(const uint16_t *x, int64_t x_batches, int64_t M, const
   // One weight tile streamed per run: batches sorted by weight batch, one x
   // row each, x batches in order.
   const bool by_runs = sorted && M == 1 && !lhs && rhs;
+  // Long runs (prefill-sized: 32 or more batches per weight batch on
+  // average) go to the tensor cores, one GEMM per run.
+  if (by_runs && transpose && batches >= 32 * w_batches) {
+    const cudaError_t e = launch_gemm_grouped(x, batches, w, w_batches, rhs, y, y_bf16, stream);
+    if (e != cudaErrorNotSupported) return e;
+  }
   switch (w.bits) {
     case 1: return launch_gather_bits<1>(a, b, transpose, y_bf16, by_runs, stream);
     case 2: return launch_gather_bits<2>(a, b, transpose, y_bf16, by_runs, stream);

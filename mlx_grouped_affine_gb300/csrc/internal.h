@@ -73,6 +73,13 @@ cudaError_t launch_gather(const uint16_t *x, int64_t x_batches, int64_t M, const
                           int64_t batches, bool transpose, bool sorted, void *y, bool y_bf16,
                           cudaStream_t stream);
 
+// gemm_sm103.cu: gather_qmm on the tensor cores for sorted weight-batch
+// indices with one x row per batch and no lhs indices (W transposed).
+// cudaErrorNotSupported (nothing launched) when the shape does not suit it.
+cudaError_t launch_gemm_grouped(const uint16_t *x, int64_t batches, const PackedWeight &w,
+                                int64_t w_batches, const uint32_t *rhs, void *y, bool y_bf16,
+                                cudaStream_t stream);
+
 // Fused decode GEMVs on a transposed W ([N, K], K a multiple of 128):
 // y_gate = x . gate^T and y_up = x . up^T in one launch (M <= 16; the two
 // weights share N, K, bits and group size); y = silu(gate) * up . w^T (+ resid,

@@ -131,3 +131,29 @@ def test_more_batches_than_one_grid_holds():
     want = np.tile(ref, (B // 4, 1, 1))
     bound = 8e-3 * np.tile(absy, (B // 4, 1, 1)) + 1e-6
     assert (np.abs(y - want) <= bound).all()
+
+
+@pytest.mark.parametrize("bits,y_dtype", ((4, qmm.QMM_BF16), (3, qmm.QMM_F32), (8, qmm.QMM_F32)))
+def test_sorted_long_runs_take_the_tensor_cores(bits, y_dtype):
+    """Prefill-sized mixture of experts: 1100 tokens over 8 experts (at least
+    32 per expert on average), sorted, one x row each -- the grouped tcgen05
+    path.  Runs of 0, 1, 255, 256, 257 and 600 tokens (row tiles of 256, a
+    ragged last tile, an empty expert), N = 384 (a ragged column tile), and
+    tokens whose index is past the last expert (zero rows, index bit)."""
+    E, N, K, gs = 8, 384, 512, 64
+    runs = [255, 0, 256, 1, 257, 600, 17, 40]
+    bad = 12                                   # tokens with index E (past the experts)
+    rhs = np.concatenate([np.full(r, e, dtype=np.uint32) for e, r in enumerate(runs)] +
+                         [np.full(bad, E, dtype=np.uint32)])
+    B = rhs.size
+    assert B >= 32 * E
+    packed, s, b = experts(700 + bits, E, N, K, bits, gs)
+    x = synth.x_bf16(701 + bits, B, K)
+    y = run(x, B, 1, packed, s, b, E, N, K, None, rhs, B, 1, gs, bits, True, y_dtype)
+    assert qmm.qmm_get_device_error() == qmm.QMM_ERR_INDEX
+    ref, absy = oracle.gather_qmm(x, B, 1, packed, s, b, E, N, K, None, rhs, 1, gs, bits)
+    assert_within_tolerance(y, ref, absy, "grouped bits=%d" % bits)
+    assert (host_f64(y)[B - bad:] == 0).all()
+    # the same call again gives the same bits (no accumulation across calls)
+    y2 = run(x, B, 1, packed, s, b, E, N, K, None, rhs, B, 1, gs, bits, True, y_dtype)
+    assert torch.equal(y, y2)
