@@ -672,7 +672,7 @@ PROFILE_CASES = {
     "splitk_m128": (128, 4096, 4096, 4, 64, True),
 }
 OTHER_PROFILES = ("gather_sorted", "silu_gate", "quantize", "dequantize", "rows", "f16_prefill",
-                  "f16_decode", "f32_decode", "f32_decode16", "f32_prefill")
+                  "f16_decode", "f32_decode", "f32_decode16", "f32_prefill", "gather_prefill")
 
 
 def run_other_profile(case, launches):
@@ -689,6 +689,17 @@ def run_other_profile(case, launches):
         sc, bi = dev(np.stack([w.scales for w in ws])), dev(np.stack([w.biases for w in ws]))
         rhs = dev(np.sort(synth.indices(121, B, E)).astype(np.uint32))
         x = dev(synth.x_bf16(122, B, K))
+        y = torch.empty((B, 1, N), dtype=torch.int16, device="cuda")
+        for _ in range(launches):
+            qmm.qmm_gather_qmm(x, B, 1, packed, sc, bi, E, N, K, None, rhs, B, 1, 64, 4, 1, y,
+                               qmm.QMM_BF16)
+    elif case == "gather_prefill":
+        E, N, K, B = 8, 14336, 4096, 4096
+        ws = [synth.quant_weight(120 + e, N, K, 4, 64) for e in range(E)]
+        packed = dev(np.stack([w.packed for w in ws]))
+        sc, bi = dev(np.stack([w.scales for w in ws])), dev(np.stack([w.biases for w in ws]))
+        rhs = dev(np.sort(synth.indices(123, B, E)).astype(np.uint32))
+        x = dev(synth.x_bf16(124, B, K))
         y = torch.empty((B, 1, N), dtype=torch.int16, device="cuda")
         for _ in range(launches):
             qmm.qmm_gather_qmm(x, B, 1, packed, sc, bi, E, N, K, None, rhs, B, 1, 64, 4, 1, y,
