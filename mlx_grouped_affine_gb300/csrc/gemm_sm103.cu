@@ -675,13 +675,8 @@ cudaError_t launch_t(const uint16_t *x, const GemmArgs &a, cudaStream_t stream) 
                                  CU_TENSOR_MAP_SWIZZLE_128B);
   if (me != cudaSuccess) return me;
   auto kern = gemm_kernel<E, BITS, OUT_BF16, TRANS>;
-  static bool attr_set = false;  // per instantiation
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t ae = ensure_smem_limit(kern, kSmemBytes);
+  if (ae != cudaSuccess) return ae;
   const int units = a.m_tiles * a.n_tiles * a.splits;
   const int grid = units < sm_count() ? units : sm_count();
   kern<<<grid, kThreads, kSmemBytes, stream>>>(map, a);

@@ -1,6 +1,7 @@
 // Host-side interface between the C ABI (api.cpp) and the kernel files.
 // Arguments reaching these launchers have already been validated.
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -40,6 +41,29 @@ cudaError_t encode_map_2d(CUtensorMap *map, CUtensorMapDataType type, const void
                           uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                           uint32_t box_outer, CUtensorMapSwizzle swizzle);
 int sm_count();
+
+// Raise kern's dynamic shared memory limit on the current device to at least
+// `bytes`, calling the runtime only when this device's limit (remembered per
+// kernel, per device) is lower.  Safe from several host threads: a race
+// repeats the (idempotent) call.
+template <typename Kern>
+inline cudaError_t ensure_smem_limit(Kern kern, size_t bytes) {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<size_t> limit[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool known = dev >= 0 && dev < kMaxDevices;
+  if (known && limit[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  if (known) {
+    size_t cur = limit[dev].load(std::memory_order_relaxed);
+    while (cur < bytes && !limit[dev].compare_exchange_weak(cur, bytes, std::memory_order_release)) {
+    }
+  }
+  return cudaSuccess;
+}
 
 // dequant.cu: out[r, :] = dequant(W[src(r), :]) for r < out_rows, where
 // src(r) = idx[r] if idx is given (a rows gather) else r; out of out_type.
