@@ -38,6 +38,13 @@ __device__ __forceinline__ float load_sb(const uint16_t *p, int t, int64_t i) {
   return t == kTypeF16 ? ElemF16::to_f32(h) : ElemBF16::to_f32(h);
 }
 
+// 32 bytes to global memory in one instruction (p 32-byte aligned).
+__device__ __forceinline__ void st_global_256(void *p, const uint4 &a, const uint4 &b) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x),
+               "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+
 template <int BITS, int OUT, bool GATHER>
 __global__ void __launch_bounds__(kThreads)
 dequant_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ scales,
@@ -46,6 +53,7 @@ dequant_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ scal
                int64_t cols, int group_shift, void *__restrict__ out, unsigned *err) {
   const int64_t words_per_row = (cols * BITS) >> 5;
   const int64_t sb_per_row = cols >> group_shift;
+  const bool out32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
   for (uint32_t gid = blockIdx.x * kThreads + threadIdx.x; gid < groups_total;
        gid += gridDim.x * kThreads) {
     const uint32_t rl = gid / groups_per_row, j = gid - rl * groups_per_row;
@@ -72,17 +80,37 @@ dequant_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ scal
       for (int i = 0; i < 32; ++i) v[i] = 0.0f;
     }
     const int64_t o = r * cols + static_cast<int64_t>(j) * 32;
+    // The thread's 32 outputs are 64 (16-bit) or 128 (fp32) contiguous bytes:
+    // 32-byte stores when the output is 32-byte aligned, else 16-byte ones.
     if constexpr (OUT != kTypeF32) {
       using E = typename std::conditional<OUT == kTypeF16, ElemF16, ElemBF16>::type;
-      uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + o);
+      uint4 q4[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        dst[q] = make_uint4(E::pack2(v[8 * q], v[8 * q + 1]), E::pack2(v[8 * q + 2], v[8 * q + 3]),
-                            E::pack2(v[8 * q + 4], v[8 * q + 5]), E::pack2(v[8 * q + 6], v[8 * q + 7]));
+        q4[q] = make_uint4(E::pack2(v[8 * q], v[8 * q + 1]), E::pack2(v[8 * q + 2], v[8 * q + 3]),
+                           E::pack2(v[8 * q + 4], v[8 * q + 5]), E::pack2(v[8 * q + 6], v[8 * q + 7]));
+      uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + o);
+      if (out32) {
+        st_global_256(dst, q4[0], q4[1]);
+        st_global_256(dst + 2, q4[2], q4[3]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = q4[q];
+      }
     } else {
       float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(out) + o);
+      if (out32) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        for (int q = 0; q < 4; ++q)
+          st_global_256(dst + 2 * q,
+                        make_uint4(__float_as_uint(v[8 * q]), __float_as_uint(v[8 * q + 1]),
+                                   __float_as_uint(v[8 * q + 2]), __float_as_uint(v[8 * q + 3])),
+                        make_uint4(__float_as_uint(v[8 * q + 4]), __float_as_uint(v[8 * q + 5]),
+                                   __float_as_uint(v[8 * q + 6]), __float_as_uint(v[8 * q + 7])));
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
     }
   }
 }

@@ -675,7 +675,7 @@ cudaError_t launch_t(const uint16_t *x, const GemmArgs &a, cudaStream_t stream) 
                                  CU_TENSOR_MAP_SWIZZLE_128B);
   if (me != cudaSuccess) return me;
   auto kern = gemm_kernel<E, BITS, OUT_BF16, TRANS>;
-  const cudaError_t ae = ensure_smem_limit(kern, kSmemBytes);
+  const cudaError_t ae = ensure_smem_limit<gemm_kernel<E, BITS, OUT_BF16, TRANS>>(kSmemBytes);
   if (ae != cudaSuccess) return ae;
   const int units = a.m_tiles * a.n_tiles * a.splits;
   const int grid = units < sm_count() ? units : sm_count();

@@ -42,12 +42,13 @@ cudaError_t encode_map_2d(CUtensorMap *map, CUtensorMapDataType type, const void
                           uint32_t box_outer, CUtensorMapSwizzle swizzle);
 int sm_count();
 
-// Raise kern's dynamic shared memory limit on the current device to at least
-// `bytes`, calling the runtime only when this device's limit (remembered per
-// kernel, per device) is lower.  Safe from several host threads: a race
-// repeats the (idempotent) call.
-template <typename Kern>
-inline cudaError_t ensure_smem_limit(Kern kern, size_t bytes) {
+// Raise Kern's dynamic shared memory limit on the current device to at least
+// `bytes`, calling the runtime only when this device's limit is lower.  The
+// limit is remembered per kernel (the template argument is the kernel itself,
+// so each kernel has its own record) and per device.  Safe from several host
+// threads: a race repeats the (idempotent) call.
+template <auto Kern>
+inline cudaError_t ensure_smem_limit(size_t bytes) {
   constexpr int kMaxDevices = 64;
   static std::atomic<size_t> limit[kMaxDevices] = {};
   int dev = 0;
@@ -55,7 +56,7 @@ inline cudaError_t ensure_smem_limit(Kern kern, size_t bytes) {
   if (e != cudaSuccess) return e;
   const bool known = dev >= 0 && dev < kMaxDevices;
   if (known && limit[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
   if (known) {
     size_t cur = limit[dev].load(std::memory_order_relaxed);

@@ -110,3 +110,27 @@ def test_rows_full_size_embedding_gather():
     want, bad = oracle.rows(w.packed, w.scales, w.biases, T, C, idx, 64, 4, "bf16")
     assert status == qmm.QMM_OK and bad == 0
     assert (host_bits(out) == oracle_bits(want)).all()
+
+
+@pytest.mark.parametrize("bits", (3, 4, 8))
+@pytest.mark.parametrize("dt", sorted(DTYPES))
+def test_dequantize_and_rows_into_16_byte_aligned_outputs(bits, dt):
+    """Outputs 16 bytes past a 32-byte boundary (the minimum alignment the calls
+    accept) take the kernels' 16-byte stores; the 32-byte-aligned ones their
+    32-byte stores.  Both give the same bits."""
+    w = synth.quant_weight(70 + bits, 21, 640, bits, 64)
+    pw, ps, pb = weight(w)
+    esz = 4 if dt == "f32" else 2
+    want = oracle_bits(oracle.dequantize(w.packed, w.scales, w.biases, 21, 640, 64, bits, dt))
+    big = empty_out((21 * 640 + 64,), DTYPES[dt])
+    assert big.data_ptr() % 32 == 0
+    off = 16 // esz
+    out = big[off:off + 21 * 640]
+    qmm.qmm_dequantize(pw, ps, pb, 21, 640, 64, bits, out.data_ptr(), DTYPES[dt])
+    torch.cuda.synchronize()
+    assert (host_bits(out).reshape(21, 640) == want).all()
+    idx = synth.indices(71, 9, 21)
+    outr = big[off:off + 9 * 640]
+    qmm.qmm_rows(pw, ps, pb, 21, 640, dev(idx), 9, 64, bits, outr.data_ptr(), DTYPES[dt])
+    torch.cuda.synchronize()
+    assert (host_bits(outr).reshape(9, 640) == want[idx]).all()
