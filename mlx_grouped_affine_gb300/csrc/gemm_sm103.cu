@@ -220,6 +220,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// 32 bytes to global memory in one instruction (p 32-byte aligned).
+__device__ __forceinline__ void st_global_256(void *p, const uint4 &a, const uint4 &b) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x),
+               "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint32_t (&v)[4]) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]),
                "r"(v[2]), "r"(v[3])
@@ -489,6 +496,10 @@ __device__ void epilogue_role(const GemmArgs &a, Barriers *bars, uint32_t tmem) 
   volatile int *abort = &bars->abort;
   const bool vec = OUT_BF16 ? (a.N % 8 == 0) : (a.N % 4 == 0);
   const bool vec_ws = a.N % 4 == 0;
+  // 32-byte stores: rows of y (and of the partials) 32-byte aligned.
+  const bool y32 = (OUT_BF16 ? (a.N % 16 == 0) : (a.N % 8 == 0)) &&
+                   (reinterpret_cast<uintptr_t>(a.y) & 31u) == 0;
+  const bool ws32 = a.N % 8 == 0 && (reinterpret_cast<uintptr_t>(a.ws) & 31u) == 0;
   int it = 0;
   for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++it) {
     if (!wait_warp(&bars->tmem_full, it & 1, abort, a.err)) return;
@@ -509,7 +520,12 @@ __device__ void epilogue_role(const GemmArgs &a, Barriers *bars, uint32_t tmem) 
       if (a.splits > 1) {
         // A partial of a split tile: fp32 into this split's slice.
         float *wp = a.ws + static_cast<int64_t>(split) * a.M * a.N + o;
-        if (vec_ws && n + 32 <= a.N) {
+        if (ws32 && n + 32 <= a.N) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            st_global_256(wp + 8 * j, make_uint4(r[8 * j], r[8 * j + 1], r[8 * j + 2], r[8 * j + 3]),
+                          make_uint4(r[8 * j + 4], r[8 * j + 5], r[8 * j + 6], r[8 * j + 7]));
+        } else if (vec_ws && n + 32 <= a.N) {
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             reinterpret_cast<float4 *>(wp)[j] =
@@ -523,14 +539,20 @@ __device__ void epilogue_role(const GemmArgs &a, Barriers *bars, uint32_t tmem) 
       } else if (OUT_BF16) {
         uint16_t *yp = static_cast<uint16_t *>(a.y) + o;
         if (vec && n + 32 <= a.N) {
+          uint4 p[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            uint4 p;
-            p.x = E::pack2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
-            p.y = E::pack2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
-            p.z = E::pack2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
-            p.w = E::pack2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
-            reinterpret_cast<uint4 *>(yp)[j] = p;
+            p[j].x = E::pack2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
+            p[j].y = E::pack2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
+            p[j].z = E::pack2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
+            p[j].w = E::pack2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
+          }
+          if (y32) {
+            st_global_256(yp, p[0], p[1]);
+            st_global_256(yp + 16, p[2], p[3]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) reinterpret_cast<uint4 *>(yp)[j] = p[j];
           }
         } else {
 #pragma unroll
@@ -539,7 +561,12 @@ __device__ void epilogue_role(const GemmArgs &a, Barriers *bars, uint32_t tmem) 
         }
       } else {
         float *yp = static_cast<float *>(a.y) + o;
-        if (vec && n + 32 <= a.N) {
+        if (y32 && n + 32 <= a.N) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            st_global_256(yp + 8 * j, make_uint4(r[8 * j], r[8 * j + 1], r[8 * j + 2], r[8 * j + 3]),
+                          make_uint4(r[8 * j + 4], r[8 * j + 5], r[8 * j + 6], r[8 * j + 7]));
+        } else if (vec && n + 32 <= a.N) {
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             reinterpret_cast<float4 *>(yp)[j] =
