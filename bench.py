@@ -596,6 +596,8 @@ def run_gpu(args):
     }
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+        one = cpu_baseline(budget_s=min(5.0, args.cpu_seconds), threads=1)
+        detail["cpu_oracle_1thread"] = {"GB/s": one["value"], "sample": one["sample"]}
     if dist:
         dist.barrier()
         dist.destroy_process_group()
@@ -604,16 +606,16 @@ def run_gpu(args):
 
 # ------------------------------------------------------------------- CPU ----
 
-def cpu_baseline(budget_s=15.0, steps=None):
-    """The oracle, as it stands, on all host cores: whole problems of the
-    headline workload (x [1, 4096] . W[4096, 4096]^T at 4 bits), repeated
-    until about `budget_s` seconds have passed."""
+def cpu_baseline(budget_s=15.0, steps=None, threads=None):
+    """The oracle, as it stands, on all host cores (or `threads` of them):
+    whole problems of the headline workload (x [1, 4096] . W[4096, 4096]^T at
+    4 bits), repeated until about `budget_s` seconds have passed."""
     import oracle
     from mlx_grouped_affine_gb300 import synth
     N, K = synth.DECODE_SHAPE
     w = synth.quant_weight(1, N, K, 4, 64)
     x = synth.x_bf16(1001, 1, K)
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     done, t0 = 0, time.perf_counter()
     while True:
         oracle.qmm(x, 1, w.packed, w.scales, w.biases, N, K, True, 64, 4, nthreads=threads)
