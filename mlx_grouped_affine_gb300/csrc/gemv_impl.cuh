@@ -69,7 +69,7 @@ struct GemvArgs {
 //   kFuseDual: blockIdx.z = 1 computes a second weight (scales2, biases2,
 //     through the second tensor map) on the same x into y2.
 //   kFuseSilu: x[m, k] = RN_bf16(silu(gate[m, k]) * up[m, k]) in fp32,
-//     formed by each block in shared memory for its K range.
+//     formed in shared memory by the warp that multiplies it, chunk by chunk.
 constexpr int kFuseNone = 0, kFuseDual = 1, kFuseSilu = 2;
 struct FuseArgs {
   const uint16_t *scales2, *biases2;
@@ -462,6 +462,20 @@ __device__ __forceinline__ void lds_words(const uint8_t *p, uint32_t *v) {
 // The weight copies and the scale/bias loads come before griddepcontrol.wait;
 // x, which the previous kernel may write, is read after it; 8 MMAs per chunk.
 
+// Two values of silu(g) * u, g / (1 + e^-g) * u in fp32, as one pair of E
+// (each rounded to nearest even).
+template <typename E>
+__device__ __forceinline__ uint32_t silu_mul2(uint32_t g2, uint32_t u2) {
+  float r[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float gf = E::to_f32((g2 >> (16 * h)) & 0xFFFFu);
+    const float uf = E::to_f32((u2 >> (16 * h)) & 0xFFFFu);
+    r[h] = __fdividef(gf, 1.0f + __expf(-gf)) * uf;
+  }
+  return E::pack2(r[0], r[1]);
+}
+
 struct TmaLayout {
   int kr;           // codes per block (multiple of 128)
   int box_bytes;    // shared bytes of one chunk box
@@ -592,33 +606,6 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
   // its own 32 x values per chunk (L2-resident: every block reads the same x),
   // natural pairs like the weights.
   griddep_wait();
-  if constexpr (FUSE == kFuseSilu) {
-    // x = silu(gate) * up for this block's K range, rounded once to bf16, into
-    // shared memory (rows of L.xpitch bytes); the lanes read it from there.
-    // gate and up may be written by the previous kernel: after the wait.
-    const int per_row = ncodes >> 3;  // 8 values per step
-    for (int i = threadIdx.x; i < a.M * per_row; i += blockDim.x) {
-      const int m = i / per_row, q = i - m * per_row;
-      const int64_t gofs = static_cast<int64_t>(m) * a.K + k0 + 8 * q;
-      const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(fa.gate + gofs));
-      const uint4 uv = __ldg(reinterpret_cast<const uint4 *>(fa.up + gofs));
-      const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float r[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float gf = E::to_f32((gw[j] >> (16 * h)) & 0xFFFFu);
-          const float uf = E::to_f32((uw[j] >> (16 * h)) & 0xFFFFu);
-          r[h] = __fdividef(gf, 1.0f + __expf(-gf)) * uf;
-        }
-        o[j] = E::pack2(r[0], r[1]);
-      }
-      *reinterpret_cast<uint4 *>(smem + L.x_off + m * L.xpitch + 16 * q) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-    __syncthreads();
-  }
   bool ok = true;
   // One pass computes mrows <= 8 * NT rows of x, from xc, into yc.
   auto pass = [&](const uint16_t *xc, void *yc, int mrows) {
@@ -644,6 +631,23 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
         }
       }
     };
+    // silu fusion: before a warp reads chunk c's x, its 32 lanes form that
+    // chunk's x = RN_bf16(silu(gate) * up) (fp32) in shared memory, 4 values
+    // a lane per row; the chunks are the warp's own, so a warp barrier is all
+    // the ordering it needs.
+    auto stage_silu = [&](int c) {
+      if constexpr (FUSE == kFuseSilu) {
+        for (int m = 0; m < ac.M; ++m) {
+          const int kk = (c << 7) + 4 * lane;
+          const int64_t off = static_cast<int64_t>(m) * a.K + k0 + kk;
+          const uint2 gv = __ldg(reinterpret_cast<const uint2 *>(fa.gate + off));
+          const uint2 uv = __ldg(reinterpret_cast<const uint2 *>(fa.up + off));
+          *reinterpret_cast<uint2 *>(smem + L.x_off + m * L.xpitch + kk * 2) =
+              make_uint2(silu_mul2<E>(gv.x, uv.x), silu_mul2<E>(gv.y, uv.y));
+        }
+        __syncwarp();
+      }
+    };
     uint32_t xv[NT][16];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -665,6 +669,7 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
       const int c = warp + j * kW;
       if (!ok || c >= nchunks) break;
       const uint16_t *cur = sv[j];
+      stage_silu(c);
       load_x(c, xv);
       uint32_t spins = 0;
       while (!mbar_try_wait(&bars[c], 0)) {
@@ -854,7 +859,7 @@ cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, const Batches &b, cudaStre
   L.box_bytes = box_bytes;
   const int nch = L.kr / 128;
   // x is read from global memory by each lane, or (silu) from the rows the
-  // block forms in shared memory.
+  // warps form in shared memory.
   L.x_off = nch * box_bytes;
   L.xpitch = FUSE == kFuseSilu ? L.kr * 2 + 16 : 0;
   L.red_off = L.x_off + a.M * L.xpitch;
