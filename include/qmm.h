@@ -21,10 +21,12 @@
  *     frees caller memory, as spark_runtime's `MlxInt8Weight` leaves buffers
  *     to their owner).  Every pointer must be 16-byte aligned.  bf16 values
  *     are passed as their 16-bit patterns (uint16_t).
- *   - The only memory the library takes is the split-K workspace of
- *     qmm_quantized_matmul (see there): stream-ordered, from the current
- *     device's default memory pool, returned on the same stream by the same
- *     call.  Every other path allocates nothing.
+ *   - The only memory the library takes is stream-ordered scratch, from the
+ *     current device's default memory pool, returned on the same stream by
+ *     the same call: the split-K workspace of qmm_quantized_matmul (and of its
+ *     fp32 form in qmm_quantized_matmul_typed) and the plan of
+ *     qmm_gather_qmm's tensor-core form (see there).  Every other path
+ *     allocates nothing.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream) and run on the current CUDA device.  Results follow
  *     stream order.
@@ -171,7 +173,13 @@ qmm_status qmm_quantized_matmul(const uint16_t *x, int64_t M, const uint32_t *w,
  * promise is false the results are wrong (nothing is read out of bounds).
  * Same tolerance as qmm_quantized_matmul.  The kernels are the decode ones
  * (M is walked in 8- or 16-row passes), launched without programmatic
- * dependent launch: the indices may come from the previous kernel.
+ * dependent launch: the indices may come from the previous kernel.  With
+ * sorted indices as above, transpose = 1 and 32 or more batches per weight
+ * batch on average (prefill-sized runs), the call instead runs a small
+ * planning kernel (each weight batch's run of rows, cut into 256-row tiles)
+ * and the tensor-core GEMM over those tiles; it then takes a stream-ordered
+ * allocation of 4 * (3 * tiles + 1) bytes for the plan, as the split-K
+ * workspace of qmm_quantized_matmul does.
  */
 qmm_status qmm_gather_qmm(const uint16_t *x, int64_t x_batches, int64_t M, const uint32_t *w,
                           const uint16_t *scales, const uint16_t *biases, int64_t w_batches,
