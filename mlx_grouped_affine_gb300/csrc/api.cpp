@@ -90,6 +90,124 @@ qmm_status check_weight(const char *op, const uint32_t *w, const uint16_t *scale
   return QMM_OK;
 }
 
+// ------------------------------------------------ shared implementations ----
+// The bf16 entry points are the typed ones with bf16 operands; `op` names the
+// entry point the caller used, for the last-error message.
+
+// dequantize (gather false) or rows (gather true: n rows at indices idx).
+qmm_status dequantize_impl(const char *op, const uint32_t *w, const void *scales,
+                           const void *biases, qmm_dtype sb_dtype, int64_t rows, int64_t cols,
+                           bool gather, const uint32_t *idx, int64_t n, int group_size, int bits,
+                           void *out, qmm_dtype out_dtype, qmm_stream_t stream) {
+  qmm_status st;
+  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
+  if (!known_dtype(sb_dtype))
+    return fail(QMM_ERR_UNSUPPORTED, "%s: unknown scale dtype %d", op, static_cast<int>(sb_dtype));
+  if ((st = check_out_dtype(op, out_dtype, sb_dtype)) != QMM_OK) return st;
+  const uint16_t *s16 = static_cast<const uint16_t *>(scales);
+  const uint16_t *b16 = static_cast<const uint16_t *>(biases);
+  if ((st = check_weight(op, w, s16, b16, rows, cols, group_size)) != QMM_OK) return st;
+  const int64_t out_rows = gather ? n : rows;
+  if (gather && n < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative index count %lld", op, (long long)n);
+  if (out_rows == 0) return QMM_OK;
+  if (gather && (!idx || !aligned16(idx)))
+    return fail(QMM_ERR_INVALID_ARG, "%s: indices must be a non-null 16-byte aligned pointer", op);
+  if (!out || !aligned16(out))
+    return fail(QMM_ERR_INVALID_ARG, "%s: output must be a non-null 16-byte aligned pointer", op);
+  qmm::PackedWeight pw{w, s16, b16, rows, cols, group_size, bits, static_cast<int>(sb_dtype)};
+  return cuda_status(qmm::launch_dequantize(pw, gather ? idx : nullptr, out_rows, out,
+                                            static_cast<int>(out_dtype),
+                                            reinterpret_cast<cudaStream_t>(stream)),
+                     op);
+}
+
+qmm_status quantize_impl(const char *op, const void *w, qmm_dtype w_dtype, int64_t rows,
+                         int64_t cols, int group_size, int bits, uint32_t *packed, void *scales,
+                         void *biases, qmm_stream_t stream) {
+  qmm_status st;
+  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
+  if (!known_dtype(w_dtype))
+    return fail(QMM_ERR_UNSUPPORTED, "%s: unknown weight dtype %d", op, static_cast<int>(w_dtype));
+  if (rows < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative row count %lld", op, (long long)rows);
+  if (cols <= 0 || cols % group_size != 0)
+    return fail(QMM_ERR_INVALID_ARG, "%s: cols (%lld) must be a positive multiple of group_size %d",
+                op, (long long)cols, group_size);
+  if (rows == 0) return QMM_OK;
+  if (!w || !aligned16(w) || !packed || !aligned16(packed) || !scales || !aligned16(scales) ||
+      !biases || !aligned16(biases))
+    return fail(QMM_ERR_INVALID_ARG, "%s: every pointer must be non-null and 16-byte aligned", op);
+  return cuda_status(qmm::launch_quantize(w, static_cast<int>(w_dtype), rows, cols, group_size,
+                                          bits, packed, scales, biases,
+                                          reinterpret_cast<cudaStream_t>(stream)),
+                     op);
+}
+
+// The checks of a quantized matmul, shared with the no-allocation entry
+// point.  On QMM_OK, *work is false for an empty product (nothing to launch).
+qmm_status check_matmul(const char *op, const void *x, qmm_dtype x_dtype, int64_t M,
+                        const uint32_t *w, const uint16_t *scales, const uint16_t *biases,
+                        qmm_dtype sb_dtype, int64_t N, int64_t K, int transpose, int group_size,
+                        int bits, const void *y, qmm_dtype y_dtype, bool *work) {
+  qmm_status st;
+  *work = false;
+  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
+  if (!known_dtype(x_dtype) || !known_dtype(sb_dtype))
+    return fail(QMM_ERR_UNSUPPORTED, "%s: unknown x or scale dtype (%d, %d)", op,
+                static_cast<int>(x_dtype), static_cast<int>(sb_dtype));
+  if ((st = check_out_dtype(op, y_dtype, promote(x_dtype, sb_dtype))) != QMM_OK) return st;
+  if (transpose != 0 && transpose != 1)
+    return fail(QMM_ERR_INVALID_ARG, "%s: transpose must be 0 or 1, got %d", op, transpose);
+  if (M < 0 || N < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative M or N", op);
+  if (K <= 0) return fail(QMM_ERR_INVALID_ARG, "%s: K must be positive, got %lld", op, (long long)K);
+  // Stored weight: [N, K] when transposed, [K, N] otherwise; the packed,
+  // grouped axis is the stored last one.
+  const int64_t rows = transpose ? N : K, cols = transpose ? K : N;
+  if (transpose || N > 0) {
+    if ((st = check_weight(op, w, scales, biases, rows, cols, group_size)) != QMM_OK) return st;
+  }
+  if (M == 0 || N == 0) return QMM_OK;
+  if (!x || !aligned16(x))
+    return fail(QMM_ERR_INVALID_ARG, "%s: x must be a non-null 16-byte aligned pointer", op);
+  if (!y || !aligned16(y))
+    return fail(QMM_ERR_INVALID_ARG, "%s: y must be a non-null 16-byte aligned pointer", op);
+  if (M > (int64_t(1) << 31) || K > (int64_t(1) << 31) || N > (int64_t(1) << 31))
+    return fail(QMM_ERR_INVALID_ARG, "%s: M, N and K must each be below 2^31", op);
+  if (promote(x_dtype, sb_dtype) == QMM_F32 && M > int64_t(65535) * 128)
+    return fail(QMM_ERR_INVALID_ARG, "%s: the fp32 path takes at most %lld rows of x", op,
+                (long long)(int64_t(65535) * 128));
+  *work = true;
+  return QMM_OK;
+}
+
+qmm_status matmul_impl(const char *op, const void *x, qmm_dtype x_dtype, int64_t M,
+                       const uint32_t *w, const void *scales, const void *biases,
+                       qmm_dtype sb_dtype, int64_t N, int64_t K, int transpose, int group_size,
+                       int bits, void *y, qmm_dtype y_dtype, qmm_stream_t stream) {
+  const uint16_t *s16 = static_cast<const uint16_t *>(scales);
+  const uint16_t *b16 = static_cast<const uint16_t *>(biases);
+  bool work = false;
+  const qmm_status st = check_matmul(op, x, x_dtype, M, w, s16, b16, sb_dtype, N, K, transpose,
+                                     group_size, bits, y, y_dtype, &work);
+  if (st != QMM_OK || !work) return st;
+  const int64_t rows = transpose ? N : K, cols = transpose ? K : N;
+  qmm::PackedWeight pw{w, s16, b16, rows, cols, group_size, bits, static_cast<int>(sb_dtype)};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const qmm_dtype d = promote(x_dtype, sb_dtype);
+  const bool y16 = y_dtype != QMM_F32;
+  const uint16_t *x16 = static_cast<const uint16_t *>(x);
+  cudaError_t e;
+  if (d == QMM_BF16)
+    e = M <= 16 ? qmm::launch_gemv(x16, M, pw, transpose != 0, y, y16, s)
+                : qmm::launch_gemm(x16, M, pw, transpose != 0, y, y16, s);
+  else if (d == QMM_F16)
+    e = M <= 16 ? qmm::launch_gemv_f16(x16, M, pw, transpose != 0, y, y16, s)
+                : qmm::launch_gemm_f16(x16, M, pw, transpose != 0, y, y16, s);
+  else
+    e = qmm::launch_mm_f32(x, static_cast<int>(x_dtype), M, pw, transpose != 0,
+                           static_cast<float *>(y), s);
+  return cuda_status(e, op);
+}
+
 }  // namespace
 
 namespace qmm {
@@ -114,72 +232,24 @@ unsigned qmm_set_launch_flags(unsigned flags) {
 qmm_status qmm_dequantize(const uint32_t *w, const uint16_t *scales, const uint16_t *biases,
                           int64_t rows, int64_t cols, int group_size, int bits, void *out,
                           qmm_dtype out_dtype, qmm_stream_t stream) {
-  const char *op = "qmm_dequantize";
-  qmm_status st;
-  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
-  if ((st = check_dtype(op, out_dtype)) != QMM_OK) return st;
-  if ((st = check_weight(op, w, scales, biases, rows, cols, group_size)) != QMM_OK) return st;
-  if (rows == 0) return QMM_OK;
-  if (!out || !aligned16(out))
-    return fail(QMM_ERR_INVALID_ARG, "%s: output must be a non-null 16-byte aligned pointer", op);
-  qmm::PackedWeight pw{w, scales, biases, rows, cols, group_size, bits};
-  return cuda_status(qmm::launch_dequantize(pw, nullptr, rows, out, static_cast<int>(out_dtype),
-                                            reinterpret_cast<cudaStream_t>(stream)),
-                     op);
+  return dequantize_impl("qmm_dequantize", w, scales, biases, QMM_BF16, rows, cols, false, nullptr,
+                         0, group_size, bits, out, out_dtype, stream);
 }
 
 qmm_status qmm_rows(const uint32_t *w, const uint16_t *scales, const uint16_t *biases,
                     int64_t table_rows, int64_t cols, const uint32_t *idx, int64_t n,
                     int group_size, int bits, void *out, qmm_dtype out_dtype,
                     qmm_stream_t stream) {
-  const char *op = "qmm_rows";
-  qmm_status st;
-  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
-  if ((st = check_dtype(op, out_dtype)) != QMM_OK) return st;
-  if ((st = check_weight(op, w, scales, biases, table_rows, cols, group_size)) != QMM_OK) return st;
-  if (n < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative index count %lld", op, (long long)n);
-  if (n == 0) return QMM_OK;
-  if (!idx || !aligned16(idx))
-    return fail(QMM_ERR_INVALID_ARG, "%s: indices must be a non-null 16-byte aligned pointer", op);
-  if (!out || !aligned16(out))
-    return fail(QMM_ERR_INVALID_ARG, "%s: output must be a non-null 16-byte aligned pointer", op);
-  qmm::PackedWeight pw{w, scales, biases, table_rows, cols, group_size, bits};
-  return cuda_status(qmm::launch_dequantize(pw, idx, n, out, static_cast<int>(out_dtype),
-                                            reinterpret_cast<cudaStream_t>(stream)),
-                     op);
+  return dequantize_impl("qmm_rows", w, scales, biases, QMM_BF16, table_rows, cols, true, idx, n,
+                         group_size, bits, out, out_dtype, stream);
 }
 
 qmm_status qmm_quantized_matmul(const uint16_t *x, int64_t M, const uint32_t *w,
                                 const uint16_t *scales, const uint16_t *biases, int64_t N,
                                 int64_t K, int transpose, int group_size, int bits, void *y,
                                 qmm_dtype y_dtype, qmm_stream_t stream) {
-  const char *op = "qmm_quantized_matmul";
-  qmm_status st;
-  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
-  if ((st = check_dtype(op, y_dtype)) != QMM_OK) return st;
-  if (transpose != 0 && transpose != 1)
-    return fail(QMM_ERR_INVALID_ARG, "%s: transpose must be 0 or 1, got %d", op, transpose);
-  if (M < 0 || N < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative M or N", op);
-  if (K <= 0) return fail(QMM_ERR_INVALID_ARG, "%s: K must be positive, got %lld", op, (long long)K);
-  // Stored weight: [N, K] when transposed, [K, N] otherwise; the packed,
-  // grouped axis is the stored last one.
-  const int64_t rows = transpose ? N : K, cols = transpose ? K : N;
-  if (transpose || N > 0) {
-    if ((st = check_weight(op, w, scales, biases, rows, cols, group_size)) != QMM_OK) return st;
-  }
-  if (M == 0 || N == 0) return QMM_OK;
-  if (!x || !aligned16(x))
-    return fail(QMM_ERR_INVALID_ARG, "%s: x must be a non-null 16-byte aligned pointer", op);
-  if (!y || !aligned16(y))
-    return fail(QMM_ERR_INVALID_ARG, "%s: y must be a non-null 16-byte aligned pointer", op);
-  if (M > (int64_t(1) << 31) || K > (int64_t(1) << 31) || N > (int64_t(1) << 31))
-    return fail(QMM_ERR_INVALID_ARG, "%s: M, N and K must each be below 2^31", op);
-  qmm::PackedWeight pw{w, scales, biases, rows, cols, group_size, bits};
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const bool bf16 = y_dtype == QMM_BF16;
-  cudaError_t e = M <= 16 ? qmm::launch_gemv(x, M, pw, transpose != 0, y, bf16, s)
-                          : qmm::launch_gemm(x, M, pw, transpose != 0, y, bf16, s);
-  return cuda_status(e, op);
+  return matmul_impl("qmm_quantized_matmul", x, QMM_BF16, M, w, scales, biases, QMM_BF16, N, K,
+                     transpose, group_size, bits, y, y_dtype, stream);
 }
 
 qmm_status qmm_gather_qmm(const uint16_t *x, int64_t x_batches, int64_t M, const uint32_t *w,
@@ -235,20 +305,8 @@ qmm_status qmm_gather_qmm(const uint16_t *x, int64_t x_batches, int64_t M, const
 qmm_status qmm_quantize(const uint16_t *w, int64_t rows, int64_t cols, int group_size, int bits,
                         uint32_t *packed, uint16_t *scales, uint16_t *biases,
                         qmm_stream_t stream) {
-  const char *op = "qmm_quantize";
-  qmm_status st;
-  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
-  if (rows < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative row count %lld", op, (long long)rows);
-  if (cols <= 0 || cols % group_size != 0)
-    return fail(QMM_ERR_INVALID_ARG, "%s: cols (%lld) must be a positive multiple of group_size %d",
-                op, (long long)cols, group_size);
-  if (rows == 0) return QMM_OK;
-  if (!w || !aligned16(w) || !packed || !aligned16(packed) || !scales || !aligned16(scales) ||
-      !biases || !aligned16(biases))
-    return fail(QMM_ERR_INVALID_ARG, "%s: every pointer must be non-null and 16-byte aligned", op);
-  return cuda_status(qmm::launch_quantize(w, qmm::kTypeBF16, rows, cols, group_size, bits, packed,
-                                          scales, biases, reinterpret_cast<cudaStream_t>(stream)),
-                     op);
+  return quantize_impl("qmm_quantize", w, QMM_BF16, rows, cols, group_size, bits, packed, scales,
+                       biases, stream);
 }
 
 // Checks shared by the fused decode GEMVs: a transposed weight [N, K] with K
@@ -324,24 +382,11 @@ qmm_status qmm_quantized_matmul_noalloc(const uint16_t *x, int64_t M, const uint
                                         int bits, void *y, qmm_dtype y_dtype,
                                         qmm_stream_t stream) {
   const char *op = "qmm_quantized_matmul_noalloc";
-  qmm_status st;
-  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
-  if ((st = check_dtype(op, y_dtype)) != QMM_OK) return st;
-  if (transpose != 0 && transpose != 1)
-    return fail(QMM_ERR_INVALID_ARG, "%s: transpose must be 0 or 1, got %d", op, transpose);
-  if (M < 0 || N < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative M or N", op);
-  if (K <= 0) return fail(QMM_ERR_INVALID_ARG, "%s: K must be positive, got %lld", op, (long long)K);
+  bool work = false;
+  const qmm_status st = check_matmul(op, x, QMM_BF16, M, w, scales, biases, QMM_BF16, N, K,
+                                     transpose, group_size, bits, y, y_dtype, &work);
+  if (st != QMM_OK || !work) return st;
   const int64_t rows = transpose ? N : K, cols = transpose ? K : N;
-  if (transpose || N > 0) {
-    if ((st = check_weight(op, w, scales, biases, rows, cols, group_size)) != QMM_OK) return st;
-  }
-  if (M == 0 || N == 0) return QMM_OK;
-  if (!x || !aligned16(x))
-    return fail(QMM_ERR_INVALID_ARG, "%s: x must be a non-null 16-byte aligned pointer", op);
-  if (!y || !aligned16(y))
-    return fail(QMM_ERR_INVALID_ARG, "%s: y must be a non-null 16-byte aligned pointer", op);
-  if (M > (int64_t(1) << 31) || K > (int64_t(1) << 31) || N > (int64_t(1) << 31))
-    return fail(QMM_ERR_INVALID_ARG, "%s: M, N and K must each be below 2^31", op);
   // Set-up on the first call on this device: the scratch's device address.
   float *scratch = qmm::static_scratch();
   if (!scratch)
@@ -375,69 +420,23 @@ qmm_status qmm_promote_types(qmm_dtype a, qmm_dtype b, qmm_dtype *out) {
 qmm_status qmm_dequantize_typed(const uint32_t *w, const void *scales, const void *biases,
                                 qmm_dtype sb_dtype, int64_t rows, int64_t cols, int group_size,
                                 int bits, void *out, qmm_dtype out_dtype, qmm_stream_t stream) {
-  const char *op = "qmm_dequantize_typed";
-  qmm_status st;
-  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
-  if (!known_dtype(sb_dtype))
-    return fail(QMM_ERR_UNSUPPORTED, "%s: unknown scale dtype %d", op, static_cast<int>(sb_dtype));
-  if ((st = check_out_dtype(op, out_dtype, sb_dtype)) != QMM_OK) return st;
-  const uint16_t *s16 = static_cast<const uint16_t *>(scales);
-  const uint16_t *b16 = static_cast<const uint16_t *>(biases);
-  if ((st = check_weight(op, w, s16, b16, rows, cols, group_size)) != QMM_OK) return st;
-  if (rows == 0) return QMM_OK;
-  if (!out || !aligned16(out))
-    return fail(QMM_ERR_INVALID_ARG, "%s: output must be a non-null 16-byte aligned pointer", op);
-  qmm::PackedWeight pw{w, s16, b16, rows, cols, group_size, bits, static_cast<int>(sb_dtype)};
-  return cuda_status(qmm::launch_dequantize(pw, nullptr, rows, out, static_cast<int>(out_dtype),
-                                            reinterpret_cast<cudaStream_t>(stream)),
-                     op);
+  return dequantize_impl("qmm_dequantize_typed", w, scales, biases, sb_dtype, rows, cols, false,
+                         nullptr, 0, group_size, bits, out, out_dtype, stream);
 }
 
 qmm_status qmm_rows_typed(const uint32_t *w, const void *scales, const void *biases,
                           qmm_dtype sb_dtype, int64_t table_rows, int64_t cols,
                           const uint32_t *idx, int64_t n, int group_size, int bits, void *out,
                           qmm_dtype out_dtype, qmm_stream_t stream) {
-  const char *op = "qmm_rows_typed";
-  qmm_status st;
-  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
-  if (!known_dtype(sb_dtype))
-    return fail(QMM_ERR_UNSUPPORTED, "%s: unknown scale dtype %d", op, static_cast<int>(sb_dtype));
-  if ((st = check_out_dtype(op, out_dtype, sb_dtype)) != QMM_OK) return st;
-  const uint16_t *s16 = static_cast<const uint16_t *>(scales);
-  const uint16_t *b16 = static_cast<const uint16_t *>(biases);
-  if ((st = check_weight(op, w, s16, b16, table_rows, cols, group_size)) != QMM_OK) return st;
-  if (n < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative index count %lld", op, (long long)n);
-  if (n == 0) return QMM_OK;
-  if (!idx || !aligned16(idx))
-    return fail(QMM_ERR_INVALID_ARG, "%s: indices must be a non-null 16-byte aligned pointer", op);
-  if (!out || !aligned16(out))
-    return fail(QMM_ERR_INVALID_ARG, "%s: output must be a non-null 16-byte aligned pointer", op);
-  qmm::PackedWeight pw{w, s16, b16, table_rows, cols, group_size, bits, static_cast<int>(sb_dtype)};
-  return cuda_status(qmm::launch_dequantize(pw, idx, n, out, static_cast<int>(out_dtype),
-                                            reinterpret_cast<cudaStream_t>(stream)),
-                     op);
+  return dequantize_impl("qmm_rows_typed", w, scales, biases, sb_dtype, table_rows, cols, true, idx,
+                         n, group_size, bits, out, out_dtype, stream);
 }
 
 qmm_status qmm_quantize_typed(const void *w, qmm_dtype w_dtype, int64_t rows, int64_t cols,
                               int group_size, int bits, uint32_t *packed, void *scales,
                               void *biases, qmm_stream_t stream) {
-  const char *op = "qmm_quantize_typed";
-  qmm_status st;
-  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
-  if (!known_dtype(w_dtype))
-    return fail(QMM_ERR_UNSUPPORTED, "%s: unknown weight dtype %d", op, static_cast<int>(w_dtype));
-  if (rows < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative row count %lld", op, (long long)rows);
-  if (cols <= 0 || cols % group_size != 0)
-    return fail(QMM_ERR_INVALID_ARG, "%s: cols (%lld) must be a positive multiple of group_size %d",
-                op, (long long)cols, group_size);
-  if (rows == 0) return QMM_OK;
-  if (!w || !aligned16(w) || !packed || !aligned16(packed) || !scales || !aligned16(scales) ||
-      !biases || !aligned16(biases))
-    return fail(QMM_ERR_INVALID_ARG, "%s: every pointer must be non-null and 16-byte aligned", op);
-  return cuda_status(qmm::launch_quantize(w, static_cast<int>(w_dtype), rows, cols, group_size,
-                                          bits, packed, scales, biases,
-                                          reinterpret_cast<cudaStream_t>(stream)),
-                     op);
+  return quantize_impl("qmm_quantize_typed", w, w_dtype, rows, cols, group_size, bits, packed,
+                       scales, biases, stream);
 }
 
 qmm_status qmm_quantized_matmul_typed(const void *x, qmm_dtype x_dtype, int64_t M,
@@ -445,49 +444,8 @@ qmm_status qmm_quantized_matmul_typed(const void *x, qmm_dtype x_dtype, int64_t 
                                       qmm_dtype sb_dtype, int64_t N, int64_t K, int transpose,
                                       int group_size, int bits, void *y, qmm_dtype y_dtype,
                                       qmm_stream_t stream) {
-  const char *op = "qmm_quantized_matmul_typed";
-  qmm_status st;
-  if ((st = check_params(op, group_size, bits)) != QMM_OK) return st;
-  if (!known_dtype(x_dtype) || !known_dtype(sb_dtype))
-    return fail(QMM_ERR_UNSUPPORTED, "%s: unknown x or scale dtype (%d, %d)", op,
-                static_cast<int>(x_dtype), static_cast<int>(sb_dtype));
-  const qmm_dtype d = promote(x_dtype, sb_dtype);
-  if ((st = check_out_dtype(op, y_dtype, d)) != QMM_OK) return st;
-  if (transpose != 0 && transpose != 1)
-    return fail(QMM_ERR_INVALID_ARG, "%s: transpose must be 0 or 1, got %d", op, transpose);
-  if (M < 0 || N < 0) return fail(QMM_ERR_INVALID_ARG, "%s: negative M or N", op);
-  if (K <= 0) return fail(QMM_ERR_INVALID_ARG, "%s: K must be positive, got %lld", op, (long long)K);
-  const int64_t rows = transpose ? N : K, cols = transpose ? K : N;
-  const uint16_t *s16 = static_cast<const uint16_t *>(scales);
-  const uint16_t *b16 = static_cast<const uint16_t *>(biases);
-  if (transpose || N > 0) {
-    if ((st = check_weight(op, w, s16, b16, rows, cols, group_size)) != QMM_OK) return st;
-  }
-  if (M == 0 || N == 0) return QMM_OK;
-  if (!x || !aligned16(x))
-    return fail(QMM_ERR_INVALID_ARG, "%s: x must be a non-null 16-byte aligned pointer", op);
-  if (!y || !aligned16(y))
-    return fail(QMM_ERR_INVALID_ARG, "%s: y must be a non-null 16-byte aligned pointer", op);
-  if (M > (int64_t(1) << 31) || K > (int64_t(1) << 31) || N > (int64_t(1) << 31))
-    return fail(QMM_ERR_INVALID_ARG, "%s: M, N and K must each be below 2^31", op);
-  if (d == QMM_F32 && M > int64_t(65535) * 128)
-    return fail(QMM_ERR_INVALID_ARG, "%s: the fp32 path takes at most %lld rows of x", op,
-                (long long)(int64_t(65535) * 128));
-  qmm::PackedWeight pw{w, s16, b16, rows, cols, group_size, bits, static_cast<int>(sb_dtype)};
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const bool y16 = y_dtype != QMM_F32;
-  const uint16_t *x16 = static_cast<const uint16_t *>(x);
-  cudaError_t e;
-  if (d == QMM_BF16)
-    e = M <= 16 ? qmm::launch_gemv(x16, M, pw, transpose != 0, y, y16, s)
-                : qmm::launch_gemm(x16, M, pw, transpose != 0, y, y16, s);
-  else if (d == QMM_F16)
-    e = M <= 16 ? qmm::launch_gemv_f16(x16, M, pw, transpose != 0, y, y16, s)
-                : qmm::launch_gemm_f16(x16, M, pw, transpose != 0, y, y16, s);
-  else
-    e = qmm::launch_mm_f32(x, static_cast<int>(x_dtype), M, pw, transpose != 0,
-                           static_cast<float *>(y), s);
-  return cuda_status(e, op);
+  return matmul_impl("qmm_quantized_matmul_typed", x, x_dtype, M, w, scales, biases, sb_dtype, N,
+                     K, transpose, group_size, bits, y, y_dtype, stream);
 }
 
 qmm_status qmm_get_device_error(qmm_stream_t stream) {

@@ -177,3 +177,23 @@ def test_typed_calls_check_dtypes_before_launching():
     assert L.qmm_quantize_typed(A, 7, 4, 64, 32, 4, A, A, A, S) == U
     assert L.qmm_quantize_typed(A, qmm.QMM_F32, 0, 64, 32, 4, A, A, A, S) == qmm.QMM_OK
     assert L.qmm_quantize_typed(A, qmm.QMM_F32, 4, 48, 32, 4, A, A, A, S) == BAD
+
+
+def test_rows_checks_its_index_count_before_its_pointer():
+    assert rows(n=-3, idx=0) == BAD and "negative index count" in qmm.qmm_last_error()
+    assert rows(n=-3) == BAD
+    L = qmm.lib()
+    assert L.qmm_rows_typed(A, A, A, qmm.QMM_F16, 10, 64, 0, -1, 64, 4, A, qmm.QMM_F16, S) == BAD
+    assert "negative index count" in qmm.qmm_last_error()
+
+
+def test_each_entry_point_names_itself_in_its_errors():
+    L = qmm.lib()
+    assert deq(G=48) == BAD and qmm.qmm_last_error().startswith("qmm_dequantize:")
+    assert mm(G=48) == BAD and qmm.qmm_last_error().startswith("qmm_quantized_matmul:")
+    assert rows(G=48) == BAD and qmm.qmm_last_error().startswith("qmm_rows:")
+    assert L.qmm_quantized_matmul_noalloc(A, 1, A, A, A, 64, 64, 1, 48, 4, A, qmm.QMM_BF16, S) == BAD
+    assert qmm.qmm_last_error().startswith("qmm_quantized_matmul_noalloc:")
+    assert mm_typed(G=48) == BAD and qmm.qmm_last_error().startswith("qmm_quantized_matmul_typed:")
+    assert L.qmm_quantize(A, 4, 64, 48, 4, A, A, A, S) == BAD
+    assert qmm.qmm_last_error().startswith("qmm_quantize:")
