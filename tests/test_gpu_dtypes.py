@@ -261,3 +261,20 @@ def test_matmul_f32_split_k_repeats_bit_for_bit_and_long_k(M, transpose):
     ref, absy = oracle.qmm(x, M, w.packed, w.scales, w.biases, N, K, transpose, gs, bits,
                            x_dtype="f32", sb_dtype="f32")
     check_mm(a, ref, absy, "f32", "f32", K, "f32 long K M=%d T=%s" % (M, transpose))
+
+
+@pytest.mark.parametrize("x_dt,sb_dt", (("f16", "f16"), ("f32", "f32"), ("bf16", "f16")))
+@pytest.mark.parametrize("M", (1, 5, 16, 24))
+def test_matmul_typed_k_not_a_multiple_of_128(x_dt, sb_dt, M):
+    """W stored [N, K] with K = 320 (a multiple of the group, not of 128): the
+    decode kernels' plain-load form (no TMA boxes) in fp16, the fp32 GEMV form,
+    and the tensor-core GEMM at M = 24."""
+    N, K, gs, bits = 136, 320, 32, 5
+    w = synth.quant_weight_typed(990 + M, N, K, bits, gs, sb_dt)
+    x = synth.x_typed(991 + M, M, K, x_dt)
+    d = promoted(x_dt, sb_dt)
+    ref, absy = oracle.qmm(x, M, w.packed, w.scales, w.biases, N, K, True, gs, bits,
+                           x_dtype=x_dt, sb_dtype=sb_dt)
+    for y_dt in sorted({"f32", d}):
+        got = run_mm(x, x_dt, M, w, N, K, True, y_dt)
+        check_mm(got, ref, absy, d, y_dt, K, "K=320 %s x %s M=%d y=%s" % (x_dt, sb_dt, M, y_dt))
