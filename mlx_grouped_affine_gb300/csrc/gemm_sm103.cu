@@ -908,7 +908,10 @@ cudaError_t launch_gemm_grouped(const uint16_t *x, int64_t batches, const Packed
   a.sb_bstride = w.rows * (w.cols / w.group);
   void *p = nullptr;
   cudaError_t e = cudaMallocAsync(&p, sizeof(int) * (1 + 3 * static_cast<size_t>(a.m_tiles)), stream);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess) {  // no plan buffer: the caller takes the decode kernels instead
+    cudaGetLastError();
+    return cudaErrorNotSupported;
+  }
   int *plan = static_cast<int *>(p);
   const size_t plan_smem = 2 * sizeof(int) * static_cast<size_t>(w_batches);
   group_plan_kernel<<<1, kPlanThreads, plan_smem, stream>>>(

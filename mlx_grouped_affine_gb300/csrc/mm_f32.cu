@@ -394,10 +394,13 @@ cudaError_t launch_gemv_cfg(const MmArgs &a, cudaStream_t stream) {
 template <int BITS>
 cudaError_t launch_bits(const MmArgs &a, bool transpose, cudaStream_t stream) {
   if (a.M <= 16 && transpose) {
-    if (a.M == 1) return launch_gemv_cfg<BITS, 1>(a, stream);
-    if (a.M <= 4) return launch_gemv_cfg<BITS, 4>(a, stream);
-    if (a.M <= 8) return launch_gemv_cfg<BITS, 8>(a, stream);
-    return launch_gemv_cfg<BITS, 16>(a, stream);
+    const cudaError_t e = a.M == 1   ? launch_gemv_cfg<BITS, 1>(a, stream)
+                          : a.M <= 4 ? launch_gemv_cfg<BITS, 4>(a, stream)
+                          : a.M <= 8 ? launch_gemv_cfg<BITS, 8>(a, stream)
+                                     : launch_gemv_cfg<BITS, 16>(a, stream);
+    // Without the slices' workspace the tiled form runs K unsplit.
+    if (e != cudaErrorMemoryAllocation) return e;
+    return launch_cfg<BITS, 16, 128, 6, true>(a, stream);
   }
   if (a.M <= 16) return launch_cfg<BITS, 16, 128, 6, false>(a, stream);
   return transpose ? launch_cfg<BITS, 128, 128, 1, true>(a, stream)
