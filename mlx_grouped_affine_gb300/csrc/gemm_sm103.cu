@@ -6,15 +6,18 @@
 // 256-row x 64-code tile of W is dequantized straight into shared memory,
 // where the tensor cores read it.
 //
+// The element type E of x and of the dequantized weight is bf16, or fp16 for
+// fp16 x, scales and biases (kind::f16 takes either, the same for A and B).
 // One persistent block per SM walks output tiles of 256 x-rows by 256
 // weight-rows.  Each dequantized W tile feeds two 128-row MMAs (the two x
 // halves), which halves the dequantization work per tensor-core flop
 // compared with a 128-row tile.  Its warps specialise:
-//   warp 0      TMA: x tiles [256 x 64] bf16 into a 128-byte-swizzled ring
+//   warp 0      TMA: x tiles [256 x 64] of E into a 128-byte-swizzled ring
 //   warp 1      allocates tensor memory and issues tcgen05.mma (one lane):
 //               D[2 x 128 x 256] fp32 in TMEM (all 512 columns)
 //   warps 2-5   epilogue: tcgen05.ld of the accumulators, convert, store y
-//   warps 6-21  dequantize: packed W -> bf16 (one rounding per weight,
+//               (32-byte stores where the rows allow), or fp32 split-K partials
+//   warps 6-21  dequantize: packed W -> E (one rounding per weight,
 //               RN(scale * code + bias)), 32 codes a thread per stage, written
 //               in the same 128-byte swizzle the MMA descriptor expects, then
 //               fence.proxy.async and arrive; the packed codes of the next two
@@ -23,8 +26,12 @@
 // out sets the device error word, makes every role stop, and the block still
 // waits for its own copies and MMAs and frees its tensor memory.
 //
+// Units are (output tile, K range) pairs: split-K when the tiles are too few
+// for the SMs, and in grouped mode (gather_qmm over sorted expert runs) the
+// row tiles come from a plan made on the device (see launch_gemm_grouped).
+//
 // Shared-memory tiles are K-major with the 128-byte swizzle: row r of a tile
-// is 128 bytes (64 bf16) at r*128, and its 16-byte chunk c sits at chunk
+// is 128 bytes (64 16-bit values) at r*128, and its 16-byte chunk c sits at chunk
 // position c ^ (r % 8).  The UMMA descriptor gives stride 1024 bytes between
 // 8-row groups; a 16-wide K step inside the 64-wide atom advances the start
 // address by 32 bytes.
