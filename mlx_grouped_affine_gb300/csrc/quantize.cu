@@ -34,8 +34,11 @@ constexpr int kThreads = 256;
 // take the correctly rounded division.
 __device__ __forceinline__ float rint_quotient(float d, float s, float r) {
   const float q = __fmul_rn(d, r);
-  const float f = q - floorf(q);  // exact: |q| is far below 2^23
-  if (fabsf(f - 0.5f) > fabsf(q) * 0x1p-20f + 0x1p-40f) return rintf(q);
+  const float n = rintf(q);
+  // q - n is exact (|q| is far below 2^23 and n is its nearest integer); its
+  // distance from +-1/2 is q's distance from the half-integer between n and
+  // its neighbour on q's side.
+  if (0.5f - fabsf(q - n) > fabsf(q) * 0x1p-20f + 0x1p-40f) return n;
   return rintf(__fdiv_rn(d, s));
 }
 
