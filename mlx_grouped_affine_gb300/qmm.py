@@ -164,12 +164,15 @@ def qmm_promote_types(a, b):
 
 def qmm_dequantize_typed(w, scales, biases, sb_dtype, rows, cols, group_size, bits, out,
                          out_dtype, stream=None):
+    """qmm_dequantize with scales and biases of sb_dtype (QMM_BF16, QMM_F16 or
+    QMM_F32); out_dtype is QMM_F32 or sb_dtype."""
     _check(lib().qmm_dequantize_typed(_ptr(w), _ptr(scales), _ptr(biases), sb_dtype, rows, cols,
                                       group_size, bits, _ptr(out), out_dtype, _stream(stream)))
 
 
 def qmm_rows_typed(w, scales, biases, sb_dtype, table_rows, cols, idx, n, group_size, bits, out,
                    out_dtype, stream=None):
+    """qmm_rows with scales and biases of sb_dtype; out_dtype QMM_F32 or sb_dtype."""
     _check(lib().qmm_rows_typed(_ptr(w), _ptr(scales), _ptr(biases), sb_dtype, table_rows, cols,
                                 _ptr(idx), n, group_size, bits, _ptr(out), out_dtype,
                                 _stream(stream)))
@@ -177,12 +180,16 @@ def qmm_rows_typed(w, scales, biases, sb_dtype, table_rows, cols, idx, n, group_
 
 def qmm_quantize_typed(w, w_dtype, rows, cols, group_size, bits, packed, scales, biases,
                        stream=None):
+    """qmm_quantize of a weight of w_dtype; scales and biases are written in w_dtype."""
     _check(lib().qmm_quantize_typed(_ptr(w), w_dtype, rows, cols, group_size, bits, _ptr(packed),
                                     _ptr(scales), _ptr(biases), _stream(stream)))
 
 
 def qmm_quantized_matmul_typed(x, x_dtype, M, w, scales, biases, sb_dtype, N, K, transpose,
                                group_size, bits, y, y_dtype, stream=None):
+    """qmm_quantized_matmul computed in qmm_promote_types(x_dtype, sb_dtype):
+    bf16 and fp16 on the tensor cores, fp32 on the CUDA cores; y_dtype is
+    QMM_F32 or that type."""
     _check(lib().qmm_quantized_matmul_typed(_ptr(x), x_dtype, M, _ptr(w), _ptr(scales),
                                             _ptr(biases), sb_dtype, N, K, int(transpose),
                                             group_size, bits, _ptr(y), y_dtype, _stream(stream)))
