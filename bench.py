@@ -69,6 +69,10 @@ def gemv_bytes(M, N, K, bits, group):
 # ------------------------------------------------------------------ clocks ---
 
 class ClockSampler:
+    """Samples SM clocks, power and throttle reasons with a read-only
+    nvidia-smi query every 100 ms while the `with` block runs.  Entering waits
+    (up to 5 s) for the first sample, so that even a short timed region is
+    covered by the samples taken during its warm-up and itself."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -76,27 +80,51 @@ class ClockSampler:
     def __init__(self, device):
         self.device = device
         self.proc = None
+        self.samples = []
+
+    def _target(self):
+        """nvidia-smi's name for this process's device: its UUID when torch
+        reports one (device indices differ when CUDA_VISIBLE_DEVICES is set)."""
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(self.device).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            return str(self.device)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8 and parts[0].replace(".", "").isdigit():
+                self.samples.append(parts)
 
     def __enter__(self):
+        import threading
+        self.samples = []
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.device), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                ["nvidia-smi", "-i", self._target(), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.samples and self.proc.poll() is None and time.time() - t0 < 5.0:
+            time.sleep(0.02)
         return self
 
     def __exit__(self, *exc):
-        self.samples = []
         if self.proc is None:
             return
         self.proc.terminate()
-        out, _ = self.proc.communicate(timeout=10)
-        for line in out.strip().splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 8:
-                self.samples.append(parts)
+        try:
+            self.proc.wait(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
 
     def summary(self):
         if not self.samples:
@@ -186,30 +214,33 @@ def dequant_rows_detail(torch, qmm, synth, peaks, steps, warmup):
     N, K = 14336, 4096
     for bits in (4, 8):
         w = synth.quant_weight(40 + bits, N, K, bits, 64)
+        # Rotating weights and outputs whose bytes together exceed 3x L2.
+        R = max(2, -(-3 * L2_BYTES // (w.nbytes + 2 * N * K)))
         copies = [(dev(np.roll(w.packed, r, 0)), dev(np.roll(w.scales, r, 0)),
-                   dev(np.roll(w.biases, r, 0))) for r in range(2)]
-        o = torch.empty((2, N, K), dtype=torch.int16, device="cuda")
+                   dev(np.roll(w.biases, r, 0))) for r in range(R)]
+        o = torch.empty((R, N, K), dtype=torch.int16, device="cuda")
         def fn():
-            for r in range(2):
+            for r in range(R):
                 pw, ps, pb = copies[r]
                 qmm.qmm_dequantize(pw, ps, pb, N, K, 64, bits, o[r], qmm.QMM_BF16)
-        t = time_graph(torch, graph_of(torch, fn), steps, warmup) / 2
+        t = time_graph(torch, graph_of(torch, fn), steps, warmup) / R
         nbytes = w.nbytes + 2 * N * K
         out["dequantize_b%d_%dx%d_bf16" % (bits, N, K)] = {
             "us": round(t * 1e3, 2), "GB/s": round(nbytes / (t * 1e-3) / 1e9, 1),
             "frac_hbm": round(nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
         del copies, o
     # quantize: bf16 [N, K] read, packed codes + bf16 scales and biases written
-    wsrc = [dev(synth.x_bf16(45 + r, N, K)) for r in range(2)]
+    R = max(2, -(-3 * L2_BYTES // (2 * N * K + N * K + 4 * N * (K // 64))))
+    wsrc = [dev(synth.x_bf16(45 + r, N, K)) for r in range(R)]
     for bits in (4, 8):
-        p = torch.empty((2, N, K * bits // 32), dtype=torch.int32, device="cuda")
-        sc = torch.empty((2, N, K // 64), dtype=torch.int16, device="cuda")
+        p = torch.empty((R, N, K * bits // 32), dtype=torch.int32, device="cuda")
+        sc = torch.empty((R, N, K // 64), dtype=torch.int16, device="cuda")
         bi = torch.empty_like(sc)
 
         def fn():
-            for r in range(2):
+            for r in range(R):
                 qmm.qmm_quantize(wsrc[r], N, K, 64, bits, p[r], sc[r], bi[r])
-        t = time_graph(torch, graph_of(torch, fn), steps, warmup) / 2
+        t = time_graph(torch, graph_of(torch, fn), steps, warmup) / R
         nbytes = 2 * N * K + N * K * bits // 8 + 4 * N * (K // 64)
         out["quantize_b%d_%dx%d_bf16" % (bits, N, K)] = {
             "us": round(t * 1e3, 2), "GB/s": round(nbytes / (t * 1e-3) / 1e9, 1),
@@ -267,7 +298,8 @@ def sweep_detail(torch, qmm, synth, peaks, warmup):
     for (N, K) in synth.SWEEP_SHAPES:
         for bits in (4, 8):
             w = synth.quant_weight(90 + bits, N, K, bits, 64)
-            R = 2
+            # Rotate weights and outputs whose bytes together exceed 3x L2.
+            R = max(2, -(-3 * L2_BYTES // (w.nbytes + 2 * N * K)))
             copies = [(dev(np.roll(w.packed, r, 0)), dev(np.roll(w.scales, r, 0)),
                        dev(np.roll(w.biases, r, 0))) for r in range(R)]
             o = torch.empty((R, N, K), dtype=torch.int16, device="cuda")
@@ -499,8 +531,17 @@ def run_gpu(args):
     head = Case(torch, qmm, synth, 1, N, K, 4, 64, seed=1 + rank)
     head.capture()
     with ClockSampler(local) as clk:
+        # Keep the GPU under this load for half a second before the timed
+        # region (extra warm-up), so the clock samples describe it.
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < 0.5:
+            for _ in range(50):
+                head.graph.replay()
+            torch.cuda.synchronize()
         ms = time_graph(torch, head.graph, args.steps, args.warmup, barrier)
     clocks = clk.summary()
+    clocks["window"] = "0.5 s of the step's replays before the timed region, and the timed region"
+
     ms = max_over_ranks(ms, dist, device="cuda")
     launch_ms = ms / head.R
     per_launch = head.bytes_per_launch()
@@ -538,6 +579,7 @@ def run_gpu(args):
 
     detail = {}
     if rank == 0:
+        detail.update(reference_case_detail(torch, qmm, synth, peaks, args.warmup))
         flags = qmm.qmm_set_launch_flags(0)
         c = Case(torch, qmm, synth, 1, N, K, 4, 64, seed=2)
         c.capture()
@@ -576,6 +618,10 @@ def run_gpu(args):
         detail.update(fused_detail(torch, qmm, synth, peaks, args.warmup))
         detail.update(dtype_detail(torch, qmm, synth, peaks, args.warmup))
 
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(budget_s=args.cpu_seconds)
+        one = cpu_baseline(budget_s=min(5.0, args.cpu_seconds), threads=1)
+        detail["cpu_oracle_1thread"] = {"GB/s": one["value"], "sample": one["sample"]}
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -595,13 +641,59 @@ def run_gpu(args):
         "detail": detail,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
-        one = cpu_baseline(budget_s=min(5.0, args.cpu_seconds), threads=1)
-        detail["cpu_oracle_1thread"] = {"GB/s": one["value"], "sample": one["sample"]}
+        out["cpu_baseline"] = cpu
+    # The headline lines again, last, so that they survive a tail of the line.
+    out["headline"] = headline(detail, out)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
     return out if rank == 0 else None
+
+
+def headline(detail, out):
+    """A compact summary of the lines that carry the metric: decode (GB/s and
+    fraction of HBM), the M = 2048 prefill (TFLOP/s and fraction of bf16
+    peak), odd widths, rows and dequantize."""
+    h = {"decode_b4_M1_4096x4096": {"GB/s": out["value"], "frac_hbm": out["roofline"]["frac"]}}
+    for k, v in detail.items():
+        if k.startswith("prefill_b4_M2048"):
+            h[k] = {"us": v.get("us"), "TFLOP/s": v.get("TFLOP/s"), "frac_bf16": v.get("frac_bf16")}
+        elif k.startswith(("decode_b", "odd_", "rows_", "dequantize_", "reference_case")):
+            h[k] = {kk: v[kk] for kk in ("us", "frac_hbm") if kk in v}
+    h["clocks_sm_mhz"] = out["clocks"].get("sm_mhz")
+    return h
+
+
+def reference_case_detail(torch, qmm, synth, peaks, warmup):
+    """The small reference case: x [1, 512] . W[256, 512]^T at 4 bits, group
+    64, fp32 out, and the fp32 dequantize of W.  Both are latency-bound (76 KB
+    and 0.6 MB); the line reports time per launch in a CUDA graph of 64
+    launches (inputs L2-resident: the workload is smaller than L2) and the
+    algorithmic bytes over that time."""
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(
+        {np.dtype(np.uint32): np.int32, np.dtype(np.uint16): np.int16}[a.dtype])).cuda()
+    w = synth.pr1_weight(0)
+    pw, ps, pb = dev(w.packed), dev(w.scales), dev(w.biases)
+    x = dev(synth.x_bf16(0, 1, 512))
+    y = torch.empty((1, 256), dtype=torch.float32, device="cuda")
+    o = torch.empty((256, 512), dtype=torch.float32, device="cuda")
+    out = {}
+    n = 64
+
+    def mm():
+        for _ in range(n):
+            qmm.qmm_quantized_matmul(x, 1, pw, ps, pb, 256, 512, 1, 64, 4, y, qmm.QMM_F32)
+
+    def dq():
+        for _ in range(n):
+            qmm.qmm_dequantize(pw, ps, pb, 256, 512, 64, 4, o, qmm.QMM_F32)
+    for name, fn, nbytes in (("reference_case_qmm_1x512_256x512_b4_f32", mm,
+                              w.nbytes + 2 * 512 + 4 * 256),
+                             ("reference_case_dequantize_256x512_b4_f32", dq, w.nbytes + 4 * 256 * 512)):
+        t = time_graph(torch, graph_of(torch, fn), 50, warmup) / n
+        out[name] = {"us": round(t * 1e3, 3), "GB/s": round(nbytes / (t * 1e-3) / 1e9, 1),
+                     "frac_hbm": round(nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+    return out
 
 
 # ------------------------------------------------------------------- CPU ----

@@ -243,14 +243,16 @@ qmm_status qmm_gemv_silu_gate(const uint16_t *gate, const uint16_t *up, int64_t 
  * call may appear.  (The pages have no counterpart: MLX allocates its
  * outputs and scratch through its own allocator.)
  *
- * Same arguments, checks, kernels and results as qmm_quantized_matmul.  The
- * only difference: the split-K partials (M > 16 with few output tiles) go to
- * a fixed 24 MiB scratch array inside the library instead of a stream-ordered
- * allocation, so the call allocates and frees nothing.  Every GPU that loads
- * the library holds that array until the process exits.
- *   - A call whose partials would need more than 24 MiB (splits * M * N * 4
- *     bytes) returns QMM_ERR_INVALID_ARG, says how much it needs, and runs
- *     nothing; qmm_quantized_matmul has no such limit.
+ * Same arguments, checks and kernels as qmm_quantized_matmul, and results
+ * within the same tolerance.  The only difference: the split-K partials
+ * (M > 16 with few output tiles) go to a fixed 24 MiB scratch array inside
+ * the library instead of a stream-ordered allocation, so the call allocates
+ * and frees nothing.  Every GPU that loads the library holds that array until
+ * the process exits.
+ *   - When the usual split would need more than 24 MiB of partials
+ *     (splits * M * N * 4 bytes), K is split fewer ways, as many as fit, or
+ *     not at all; the sums then run in another order than
+ *     qmm_quantized_matmul's (same tolerance, not the same bits).
  *   - The first call on each device looks up the array's device address
  *     (set-up, once per device, with that device current); make that first
  *     call before any stream capture.
@@ -302,6 +304,24 @@ qmm_status qmm_rows(const uint32_t *w, const uint16_t *scales,
  */
 #define QMM_LAUNCH_PDL 1u
 unsigned qmm_set_launch_flags(unsigned flags);
+
+/*
+ * qmm_set_wait_limit -- after how many unsuccessful polls of one of its own
+ * barriers a kernel gives up (the pages have no counterpart: it bounds the
+ * waits of this library's kernels on their own copies and stages).  Applies
+ * to the calls this host thread makes from now on; returns the previous
+ * setting.  0 restores the default (2^24 polls, each suspended for at most a
+ * few hundred nanoseconds: seconds in all); 1 gives up at the first poll that
+ * finds the barrier incomplete.
+ *
+ * A wait that runs out makes the kernel stop early: it records
+ * QMM_ERR_TIMEOUT in the device error word (qmm_get_device_error), waits
+ * for the copies it has in flight, frees what it holds and returns; the
+ * outputs of that call are then undefined (the split-K matmul writes NaN).
+ * A small limit makes waits run out on purpose, which is how the timeout
+ * path is tested; nothing faults or hangs.
+ */
+uint32_t qmm_set_wait_limit(uint32_t polls);
 
 /* The message for the last non-OK status returned on this host thread
  * (empty string if none).  The pointer stays valid until the next call. */

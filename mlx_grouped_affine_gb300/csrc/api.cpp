@@ -18,6 +18,7 @@ namespace {
 
 thread_local char g_last_error[512] = "";
 thread_local unsigned g_launch_flags = 0;
+thread_local uint32_t g_wait_limit = 0;  // 0: the default
 
 qmm_status fail(qmm_status st, const char *fmt, ...) {
   va_list ap;
@@ -212,11 +213,18 @@ qmm_status matmul_impl(const char *op, const void *x, qmm_dtype x_dtype, int64_t
 
 namespace qmm {
 unsigned launch_flags() { return g_launch_flags; }
+uint32_t wait_limit() { return g_wait_limit ? g_wait_limit : kDefaultWaitLimit; }
 }  // namespace qmm
 
 extern "C" {
 
 const char *qmm_last_error(void) { return g_last_error; }
+
+uint32_t qmm_set_wait_limit(uint32_t polls) {
+  const uint32_t prev = g_wait_limit;
+  g_wait_limit = polls;
+  return prev;
+}
 
 unsigned qmm_set_launch_flags(unsigned flags) {
   const unsigned prev = g_launch_flags;

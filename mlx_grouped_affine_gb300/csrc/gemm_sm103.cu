@@ -93,6 +93,7 @@ struct GemmArgs {
   // from the plan on the device.
   const int *plan = nullptr;
   int64_t w_bstride = 0, sb_bstride = 0;
+  uint32_t spin_limit = kDefaultWaitLimit;  // polls of a bounded wait before it gives up
 };
 
 // The rows [row0, row_end) of x and y one row tile covers, and its weight batch.
@@ -128,14 +129,14 @@ __device__ __forceinline__ Unit unit_of(const GemmArgs &a, int u, int nk) {
 // Warp-uniform result: false if this wait ran out (the error word is set) or
 // another role already gave up.
 __device__ __noinline__ bool wait_warp(uint64_t *b, uint32_t parity, volatile int *abort,
-                                       unsigned *err) {
+                                       unsigned *err, uint32_t limit) {
   uint32_t spins = 0;
   while (true) {
     const bool done = mbar_try_wait(b, parity);
     if (__all_sync(0xffffffffu, done)) return true;
-    if ((++spins & 255u) == 0) {
+    if ((++spins & 255u) == 0 || spins >= limit) {
       int stop = *abort;
-      if (!stop && spins > kSpinLimit) {
+      if (!stop && spins >= limit) {
         stop = 1;
         *abort = 1;
         atomicOr(err, kErrTimeoutBit);
@@ -358,7 +359,7 @@ __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int
     if (unit >= num_units) return false;
     const ItemLoad<BITS> cur = buf;
     prefetch(buf);
-    if (!wait_warp(&bars->empty_b[s], ph ^ 1u, abort, a.err)) return false;
+    if (!wait_warp(&bars->empty_b[s], ph ^ 1u, abort, a.err, a.spin_limit)) return false;
     const uint32_t base = smem_u32(sB + s * B_BYTES);
     const uint32_t hs = cur.sb & 0xFFFFu, hb = cur.sb >> 16;
     const uint32_t b2 = hb * 0x00010001u;
@@ -418,7 +419,7 @@ __device__ void tma_role(const CUtensorMap *tmap, const GemmArgs &a, uint8_t *sA
     const Unit un = unit_of(a, u, nk);
     const int m0 = row_tile(a, un.tile % a.m_tiles).row0;
     for (int kb = un.kb0; kb < un.kb1; ++kb) {
-      if (!wait_warp(&bars->empty_a[s], ph ^ 1u, abort, a.err)) { ok = false; break; }
+      if (!wait_warp(&bars->empty_a[s], ph ^ 1u, abort, a.err, a.spin_limit)) { ok = false; break; }
       if (lane == 0) {
         mbar_expect_tx(&bars->full_a[s], A_BYTES);
         tma_load_2d(smem_u32(sA + s * A_BYTES), tmap, kb * BK, m0, &bars->full_a[s]);
@@ -454,14 +455,14 @@ __device__ void mma_role(const GemmArgs &a, uint8_t *sA, uint8_t *sB, Barriers *
   for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x, ++it) {
     const Unit un = unit_of(a, u, nk);
     // The epilogue must have drained the accumulators of the previous unit.
-    if (!wait_warp(&bars->tmem_empty, (it & 1) ^ 1u, abort, a.err)) break;
+    if (!wait_warp(&bars->tmem_empty, (it & 1) ^ 1u, abort, a.err, a.spin_limit)) break;
     tc_fence_after();
     // The second 128-row half only when this tile has x rows there.
     const RowTile rt = row_tile(a, un.tile % a.m_tiles);
     const bool two = rt.row0 + UM < rt.row_end;
     for (int kb = un.kb0; kb < un.kb1; ++kb) {
-      if (!wait_warp(&bars->full_a[sa], pha, abort, a.err) ||
-          !wait_warp(&bars->full_b[sb], phb, abort, a.err)) {
+      if (!wait_warp(&bars->full_a[sa], pha, abort, a.err, a.spin_limit) ||
+          !wait_warp(&bars->full_b[sb], phb, abort, a.err, a.spin_limit)) {
         ok = false;
         break;
       }
@@ -509,7 +510,7 @@ __device__ void epilogue_role(const GemmArgs &a, Barriers *bars, uint32_t tmem) 
   const bool ws32 = a.N % 8 == 0 && (reinterpret_cast<uintptr_t>(a.ws) & 31u) == 0;
   int it = 0;
   for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++it) {
-    if (!wait_warp(&bars->tmem_full, it & 1, abort, a.err)) return;
+    if (!wait_warp(&bars->tmem_full, it & 1, abort, a.err, a.spin_limit)) return;
     tc_fence_after();
     const int tile = u / a.splits, split = u - tile * a.splits;
     const int n0 = (tile / a.m_tiles) * BN;
@@ -651,8 +652,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, GemmArgs a) {
 // with 16-byte loads when the slices are 16-byte aligned.
 template <typename E, bool OUT_BF16>
 __global__ void __launch_bounds__(256)
-splitk_finalize(const float *__restrict__ ws, int splits, int64_t mn, void *__restrict__ y) {
+splitk_finalize(const float *__restrict__ ws, int splits, int64_t mn, void *__restrict__ y,
+                const unsigned *err) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  // A bounded wait of the GEMM ran out (here or in an earlier call whose
+  // error has not been read): its partials are incomplete, so y is NaN
+  // rather than a plausible wrong sum.
+  if (*reinterpret_cast<const volatile unsigned *>(err) & kErrTimeoutBit) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < mn; i += stride) {
+      if (OUT_BF16) static_cast<uint16_t *>(y)[i] = E::kF16 ? 0x7E00u : 0x7FC0u;
+      else static_cast<float *>(y)[i] = __int_as_float(0x7FC00000);
+    }
+    return;
+  }
   if (mn % 4 == 0) {
     for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4; i < mn;
          i += stride * 4) {
@@ -720,7 +732,7 @@ cudaError_t launch_t(const uint16_t *x, const GemmArgs &a, cudaStream_t stream) 
   int64_t blocks = (mn / 4 + 255) / 256;
   if (blocks > 4 * sm_count()) blocks = 4 * sm_count();
   if (blocks < 1) blocks = 1;
-  splitk_finalize<E, OUT_BF16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.ws, a.splits, mn, a.y);
+  splitk_finalize<E, OUT_BF16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.ws, a.splits, mn, a.y, a.err);
   return cudaGetLastError();
 }
 
@@ -779,6 +791,7 @@ cudaError_t gemm_entry(const uint16_t *x, int64_t M, const PackedWeight &w, bool
   a.m_tiles = (a.M + BM - 1) / BM;
   a.n_tiles = (a.N + BN - 1) / BN;
   a.err = device_error_word();
+  a.spin_limit = wait_limit();
   if (!a.err) return cudaErrorInvalidSymbol;
   a.splits = choose_splits(a.m_tiles * a.n_tiles, (a.K + BK - 1) / BK, sm_count());
   a.ws = nullptr;
@@ -910,6 +923,7 @@ cudaError_t launch_gemm_grouped(const uint16_t *x, int64_t batches, const Packed
   a.splits = 1;
   a.ws = nullptr;
   a.err = device_error_word();
+  a.spin_limit = wait_limit();
   if (!a.err) return cudaErrorInvalidSymbol;
   a.w_bstride = w.rows * ((w.cols * w.bits) / 32);
   a.sb_bstride = w.rows * (w.cols / w.group);
@@ -978,11 +992,19 @@ cudaError_t launch_gemm_static_scratch(const uint16_t *x, int64_t M, const Packe
   a.m_tiles = (a.M + BM - 1) / BM;
   a.n_tiles = (a.N + BN - 1) / BN;
   a.err = device_error_word();
+  a.spin_limit = wait_limit();
   if (!a.err) return cudaErrorInvalidSymbol;
   // Same split as launch_gemm; x rows TMA cannot address take the decode
   // kernel below and need no partials.
   const bool tma_rows = (static_cast<int64_t>(a.K) * 2) % 16 == 0;
   a.splits = tma_rows ? choose_splits(a.m_tiles * a.n_tiles, (a.K + BK - 1) / BK, sm_count()) : 1;
+  // Fewer splits when the partials of the usual split do not fit the array
+  // (none when not even two do): the same kernels, a shorter split.
+  const size_t slice = static_cast<size_t>(a.M) * a.N * sizeof(float);
+  if (a.splits > 1 && splitk_bytes(a) > static_scratch_bytes()) {
+    const size_t fit = static_scratch_bytes() / slice;
+    a.splits = fit >= 2 ? static_cast<int>(fit) : 1;
+  }
   *needed = a.splits > 1 ? splitk_bytes(a) : 0;
   if (*needed > static_scratch_bytes()) return cudaErrorInvalidValue;
   a.ws = a.splits > 1 ? scratch : nullptr;

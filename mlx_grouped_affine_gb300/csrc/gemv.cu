@@ -101,6 +101,7 @@ GemvArgs transposed_args(const uint16_t *x, int64_t M, const PackedWeight &w, vo
   a.group_shift = w.group == 32 ? 5 : w.group == 64 ? 6 : 7;
   a.parts = 1;
   a.resid = nullptr;
+  a.spin_limit = wait_limit();
   return a;
 }
 
@@ -146,6 +147,7 @@ cudaError_t launch_gather(const uint16_t *x, int64_t x_batches, int64_t M, const
   a.group_shift = w.group == 32 ? 5 : w.group == 64 ? 6 : 7;
   a.parts = 1;
   a.resid = nullptr;
+  a.spin_limit = wait_limit();
   Batches b;
   b.g.lhs = lhs;
   b.g.rhs = rhs;

@@ -29,6 +29,8 @@
 //   D 16x8:  d0,d1 row g, cols 2t, 2t+1; d2,d3 row g+8, cols 2t, 2t+1
 // The contraction index may be permuted freely as long as A and B agree.
 #pragma once
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -62,6 +64,7 @@ struct GemvArgs {
   int group_shift;
   int parts;  // K parts = cluster size * warps per block
   const uint16_t *resid;  // bf16 [M, N] added to y before it is stored, or null
+  uint32_t spin_limit = kDefaultWaitLimit;  // polls of a bounded wait
 };
 
 // Fused decode GEMVs (spark_runtime weights/mlx_int8.rs, `gemv_gate_up`,
@@ -673,7 +676,7 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
       load_x(c, xv);
       uint32_t spins = 0;
       while (!mbar_try_wait(&bars[c], 0)) {
-        if (++spins > (1u << 24)) {
+        if (++spins >= a.spin_limit) {
           if (lane == 0) atomicOr(err, kErrTimeoutBit);
           ok = false;
           break;
@@ -748,6 +751,16 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
     }
   } else {
     pass(xbase, ybase, rows);
+  }
+  if (!ok) {
+    // A wait ran out: before the block exits, wait (bounded) for the copies
+    // still in flight into its shared memory.
+    for (int j = 0; j < kTmaMaxChunksPerWarp; ++j) {
+      const int c = warp + j * kW;
+      if (c >= nchunks) break;
+      for (uint32_t s = 0; s < kDefaultWaitLimit; ++s)
+        if (mbar_try_wait(&bars[c], 0)) break;
+    }
   }
 }
 
@@ -911,23 +924,14 @@ cudaError_t launch_n(const GemvArgs &a0, const Batches &b, cudaStream_t stream) 
   });
 }
 
-// The plain decode GEMV in element type E: the TMA kernel for a transposed W
-// with K a multiple of 128 (when its layout fits), else the plain-load
-// kernels.  y_16 stores y in E, else fp32.
+// The decode GEMV in element type E with the plain-load kernels: W stored
+// [K, N], or a transposed W the decode kernel (decode.cu) does not take.
+// y_16 stores y in E, else fp32.
 template <typename E, int BITS>
 cudaError_t launch_bits(const GemvArgs &a, bool transpose, bool y_16, bool pdl,
                         cudaStream_t stream) {
+  (void)pdl;
   const Batches one;
-  if (transpose && a.K % 128 == 0) {
-    cudaError_t e;
-    if (a.M <= 8)
-      e = y_16 ? launch_t_tma<E, BITS, 1, true, false>(a, pdl, one, stream)
-               : launch_t_tma<E, BITS, 1, false, false>(a, pdl, one, stream);
-    else
-      e = y_16 ? launch_t_tma<E, BITS, 2, true, false>(a, pdl, one, stream)
-               : launch_t_tma<E, BITS, 2, false, false>(a, pdl, one, stream);
-    if (e != cudaErrorNotSupported) return e;
-  }
   if (transpose) {
     if (a.M <= 8)
       return y_16 ? launch_t<E, BITS, 1, true, false>(a, one, stream)
@@ -956,7 +960,13 @@ cudaError_t gemv_entry(const uint16_t *x, int64_t M, const PackedWeight &w, bool
   a.group_shift = w.group == 32 ? 5 : w.group == 64 ? 6 : 7;
   a.parts = 1;
   a.resid = nullptr;
+  a.spin_limit = wait_limit();
   const bool pdl = (launch_flags() & kLaunchPdl) != 0;
+  if (transpose && a.K % 128 == 0) {
+    // The decode kernel (decode.cu); the kernels below take what it cannot.
+    const cudaError_t e = launch_decode(x, M, w, y, y_16, E::kF16, pdl, stream);
+    if (e != cudaErrorNotSupported) return e;
+  }
   switch (w.bits) {
     case 1: return launch_bits<E, 1>(a, transpose, y_16, pdl, stream);
     case 2: return launch_bits<E, 2>(a, transpose, y_16, pdl, stream);

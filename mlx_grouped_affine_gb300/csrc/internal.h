@@ -15,6 +15,10 @@ constexpr unsigned kErrTimeoutBit = 2u;  // a bounded wait inside a kernel ran o
 // Launch options of the calling host thread (qmm_set_launch_flags).
 constexpr unsigned kLaunchPdl = 1u;
 unsigned launch_flags();
+// Polls a bounded wait of the calling host thread's kernels makes before it
+// gives up (qmm_set_wait_limit; default kDefaultWaitLimit).
+constexpr uint32_t kDefaultWaitLimit = 1u << 24;
+uint32_t wait_limit();
 
 // Element types, numbered as the C ABI's qmm_dtype.
 constexpr int kTypeF32 = 0, kTypeBF16 = 1, kTypeF16 = 2;
@@ -76,6 +80,13 @@ cudaError_t launch_dequantize(const PackedWeight &w, const uint32_t *idx,
 cudaError_t launch_gemv(const uint16_t *x, int64_t M, const PackedWeight &w,
                         bool transpose, void *y, bool y_bf16,
                         cudaStream_t stream);
+
+// decode.cu: the decode kernel for a transposed W ([N, K]) with K a multiple
+// of 128 and 1 <= M <= 16, x / scales / biases bf16 (or fp16 when f16), y
+// of that type when y_16 else fp32; pdl: programmatic dependent launch.
+// cudaErrorNotSupported (nothing launched) when the shape does not suit it.
+cudaError_t launch_decode(const uint16_t *x, int64_t M, const PackedWeight &w, void *y, bool y_16,
+                          bool f16, bool pdl, cudaStream_t stream);
 
 // gemv_f16.cu: the same for fp16 x, scales and biases (y fp16 if y_f16).
 cudaError_t launch_gemv_f16(const uint16_t *x, int64_t M, const PackedWeight &w,

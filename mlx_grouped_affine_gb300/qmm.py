@@ -16,7 +16,7 @@ STATUS_NAMES = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED",
 QMM_LAUNCH_PDL = 1
 EXPORTS = ("qmm_quantize", "qmm_dequantize", "qmm_quantized_matmul", "qmm_quantized_matmul_noalloc",
            "qmm_gather_qmm", "qmm_gemv_gate_up", "qmm_gemv_silu_gate", "qmm_rows",
-           "qmm_last_error", "qmm_get_device_error", "qmm_set_launch_flags",
+           "qmm_last_error", "qmm_get_device_error", "qmm_set_launch_flags", "qmm_set_wait_limit",
            "qmm_promote_types", "qmm_dequantize_typed", "qmm_rows_typed", "qmm_quantize_typed",
            "qmm_quantized_matmul_typed")
 
@@ -57,6 +57,8 @@ def lib():
             getattr(L, f).restype = I
         L.qmm_set_launch_flags.argtypes = [ctypes.c_uint]
         L.qmm_set_launch_flags.restype = ctypes.c_uint
+        L.qmm_set_wait_limit.argtypes = [ctypes.c_uint32]
+        L.qmm_set_wait_limit.restype = ctypes.c_uint32
         L.qmm_last_error.argtypes = []
         L.qmm_last_error.restype = ctypes.c_char_p
         _lib = L
@@ -153,6 +155,12 @@ def qmm_get_device_error(stream=None):
 def qmm_set_launch_flags(flags):
     """Set this host thread's launch flags (QMM_LAUNCH_PDL); returns the previous ones."""
     return int(lib().qmm_set_launch_flags(flags))
+
+
+def qmm_set_wait_limit(polls):
+    """Polls a bounded wait in this host thread's kernels makes before it
+    gives up (0: the default); returns the previous limit."""
+    return int(lib().qmm_set_wait_limit(polls))
 
 
 def qmm_promote_types(a, b):

@@ -135,6 +135,18 @@ def test_launch_flags_are_per_thread_and_checked():
     assert qmm.qmm_set_launch_flags(0) == qmm.QMM_LAUNCH_PDL   # the unknown bit was dropped
 
 
+def test_wait_limit_is_per_thread_and_restorable():
+    import threading
+    assert qmm.qmm_set_wait_limit(5) == 0                # 0: the default until set
+    seen = []
+    t = threading.Thread(target=lambda: seen.append(qmm.qmm_set_wait_limit(7)))
+    t.start()
+    t.join()
+    assert seen == [0]                                   # other thread has its own
+    assert qmm.qmm_set_wait_limit(0) == 5
+    assert qmm.qmm_set_wait_limit(0) == 0
+
+
 # -- typed calls (dtypes) ----------------------------------------------------------
 
 def test_promote_types_matches_the_oracle():
