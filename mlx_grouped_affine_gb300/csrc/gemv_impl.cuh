@@ -924,14 +924,23 @@ cudaError_t launch_n(const GemvArgs &a0, const Batches &b, cudaStream_t stream) 
   });
 }
 
-// The decode GEMV in element type E with the plain-load kernels: W stored
-// [K, N], or a transposed W the decode kernel (decode.cu) does not take.
-// y_16 stores y in E, else fp32.
+// The plain decode GEMV in element type E: the TMA kernel for a transposed W
+// with K a multiple of 128 (when its layout fits), else the plain-load
+// kernels.  y_16 stores y in E, else fp32.
 template <typename E, int BITS>
 cudaError_t launch_bits(const GemvArgs &a, bool transpose, bool y_16, bool pdl,
                         cudaStream_t stream) {
-  (void)pdl;
   const Batches one;
+  if (transpose && a.K % 128 == 0) {
+    cudaError_t e;
+    if (a.M <= 8)
+      e = y_16 ? launch_t_tma<E, BITS, 1, true, false>(a, pdl, one, stream)
+               : launch_t_tma<E, BITS, 1, false, false>(a, pdl, one, stream);
+    else
+      e = y_16 ? launch_t_tma<E, BITS, 2, true, false>(a, pdl, one, stream)
+               : launch_t_tma<E, BITS, 2, false, false>(a, pdl, one, stream);
+    if (e != cudaErrorNotSupported) return e;
+  }
   if (transpose) {
     if (a.M <= 8)
       return y_16 ? launch_t<E, BITS, 1, true, false>(a, one, stream)
@@ -962,11 +971,6 @@ cudaError_t gemv_entry(const uint16_t *x, int64_t M, const PackedWeight &w, bool
   a.resid = nullptr;
   a.spin_limit = wait_limit();
   const bool pdl = (launch_flags() & kLaunchPdl) != 0;
-  if (transpose && a.K % 128 == 0) {
-    // The decode kernel (decode.cu); the kernels below take what it cannot.
-    const cudaError_t e = launch_decode(x, M, w, y, y_16, E::kF16, pdl, stream);
-    if (e != cudaErrorNotSupported) return e;
-  }
   switch (w.bits) {
     case 1: return launch_bits<E, 1>(a, transpose, y_16, pdl, stream);
     case 2: return launch_bits<E, 2>(a, transpose, y_16, pdl, stream);

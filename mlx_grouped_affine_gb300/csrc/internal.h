@@ -81,13 +81,6 @@ cudaError_t launch_gemv(const uint16_t *x, int64_t M, const PackedWeight &w,
                         bool transpose, void *y, bool y_bf16,
                         cudaStream_t stream);
 
-// decode.cu: the decode kernel for a transposed W ([N, K]) with K a multiple
-// of 128 and 1 <= M <= 16, x / scales / biases bf16 (or fp16 when f16), y
-// of that type when y_16 else fp32; pdl: programmatic dependent launch.
-// cudaErrorNotSupported (nothing launched) when the shape does not suit it.
-cudaError_t launch_decode(const uint16_t *x, int64_t M, const PackedWeight &w, void *y, bool y_16,
-                          bool f16, bool pdl, cudaStream_t stream);
-
 // gemv_f16.cu: the same for fp16 x, scales and biases (y fp16 if y_f16).
 cudaError_t launch_gemv_f16(const uint16_t *x, int64_t M, const PackedWeight &w,
                             bool transpose, void *y, bool y_f16, cudaStream_t stream);

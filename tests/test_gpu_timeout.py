@@ -35,7 +35,7 @@ def matmul(x, M, w, N, K, y_dtype):
 def test_gemm_wait_runs_out_then_next_call_is_correct(M, N, K):
     w = synth.quant_weight(800 + M, N, K, 4, 64)
     x = synth.x_bf16(801 + M, M, K)
-    assert qmm.qmm_get_device_error() == qmm.QMM_OK
+    qmm.qmm_get_device_error()  # read and clear what earlier calls left (an index test's bit)
     prev = qmm.qmm_set_wait_limit(1)
     try:
         y = matmul(x, M, w, N, K, qmm.QMM_F32)
@@ -63,6 +63,7 @@ def test_decode_wait_limit_then_next_call_is_correct():
     N, K = 4096, 4096
     w = synth.quant_weight(810, N, K, 4, 64)
     x = synth.x_bf16(811, 1, K)
+    qmm.qmm_get_device_error()
     prev = qmm.qmm_set_wait_limit(1)
     try:
         for _ in range(8):
