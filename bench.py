@@ -770,6 +770,8 @@ PROFILE_CASES = {
     "decode_b8": (1, 4096, 4096, 8, 64, True),
     "prefill": (2048, 14336, 4096, 4, 64, True),
     "splitk_m128": (128, 4096, 4096, 4, 64, True),
+    "splitk_m128_k14336": (128, 4096, 14336, 4, 64, True),
+    "prefill_nt": (2048, 14336, 4096, 4, 64, False),
 }
 OTHER_PROFILES = ("gather_sorted", "silu_gate", "quantize", "dequantize", "rows", "f16_prefill",
                   "f16_decode", "f32_decode", "f32_decode16", "f32_prefill", "gather_prefill")

@@ -245,41 +245,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint32_t (&v)[
 
 // Dequant side: 32 consecutive codes of one stored row (`bits` words) with
 // their group's scale and bias (s | b << 16).  32 codes never straddle a
-// group (group_size >= 32) and start on a word boundary.
+// group (group_size >= 32) and start on a word boundary.  `live` is false
+// past the block's last stage.
 template <int BITS>
 struct ItemLoad {
   uint32_t v[BITS];
   uint32_t sb;
+  bool live;
 };
-
-// The 32 codes from column `col` (a multiple of 32) of stored row `row`
-// (stored [N, K] when TRANS, else [K, N]; codes and groups run along the
-// stored columns).  Words past the end of the row read as zero.
-template <int BITS, bool TRANS>
-__device__ __forceinline__ void load_item(const GemmArgs &a, int row, int col, int expert,
-                                          ItemLoad<BITS> &it) {
-  const int rows = TRANS ? a.N : a.K, cols = TRANS ? a.K : a.N;
-#pragma unroll
-  for (int i = 0; i < BITS; ++i) it.v[i] = 0u;
-  it.sb = 0u;
-  if (row < rows && col < cols) {
-    const int64_t wpr = (static_cast<int64_t>(cols) * BITS) >> 5;
-    const int64_t w0 = static_cast<int64_t>(row) * wpr + (col >> 5) * BITS;
-    const uint32_t *rp = a.w + expert * a.w_bstride + w0;
-    constexpr int kAlign = BITS % 4 == 0 ? 4 : BITS % 2 == 0 ? 2 : 1;  // words
-    if ((col >> 5) * BITS + BITS <= wpr && (w0 & (kAlign - 1)) == 0) {
-      load_words<BITS>(rp, it.v);
-    } else {
-      const int64_t left = wpr - (col >> 5) * BITS;
-#pragma unroll
-      for (int i = 0; i < BITS; ++i)
-        if (i < left) it.v[i] = __ldg(rp + i);
-    }
-    const int64_t g = expert * a.sb_bstride + static_cast<int64_t>(row) * (cols >> a.group_shift) +
-                      (col >> a.group_shift);
-    it.sb = __ldg(a.scales + g) | (static_cast<uint32_t>(__ldg(a.biases + g)) << 16);
-  }
-}
 
 // The item a dequant thread owns in a stage, and the shared-memory byte
 // offsets of its four 16-byte chunks (8 dequantized weights each).
@@ -313,6 +286,89 @@ __device__ __forceinline__ void item_place(int dt, int tile_n0, int kb, int &row
   }
 }
 
+// A dequant thread's item across the stages of its block: the unit and
+// k-block it loads next, with the pointers of its codes and of its row's (or
+// column's) scales and biases.  Moving to the next k-block is a pointer step;
+// the unit's geometry is worked out once, when the thread moves to it.
+template <int BITS, bool TRANS>
+struct ItemCursor {
+  const uint32_t *w;       // codes of the item at k-block kb
+  const uint16_t *s, *b;   // TRANS: the row's scales / biases; else the item's, at kb
+  int unit, kb, kb1;
+  int kpos;                // TRANS: first code of the item at kb; else its k row
+  bool in;                 // the item's weight row (TRANS) / column (else) exists
+  bool vec;                // the codes allow vector loads
+};
+
+template <int BITS, bool TRANS>
+__device__ __forceinline__ void cursor_unit(const GemmArgs &a, int nk, int dt,
+                                            ItemCursor<BITS, TRANS> &c) {
+  const Unit un = unit_of(a, c.unit, nk);
+  c.kb = un.kb0;
+  c.kb1 = un.kb1;
+  const int n0 = (un.tile / a.m_tiles) * BN;
+  const int expert = a.plan ? row_tile(a, un.tile % a.m_tiles).expert : 0;
+  const uint32_t *wb = a.w + expert * a.w_bstride;
+  const uint16_t *sb = a.scales + expert * a.sb_bstride, *bb = a.biases + expert * a.sb_bstride;
+  if (TRANS) {
+    const int row = n0 + (dt >> 1), h = dt & 1;
+    const int64_t wpr = (static_cast<int64_t>(a.K) * BITS) >> 5;
+    const int64_t gpr = a.K >> a.group_shift;
+    c.in = row < a.N;
+    c.kpos = c.kb * BK + 32 * h;
+    c.w = wb + row * wpr + (c.kpos >> 5) * BITS;
+    c.s = sb + row * gpr;
+    c.b = bb + row * gpr;
+  } else {
+    const int kr = (dt >> 6) * 8 + (dt & 7), col = n0 + 32 * ((dt >> 3) & 7);
+    const int64_t wpr = (static_cast<int64_t>(a.N) * BITS) >> 5;
+    const int64_t gpr = a.N >> a.group_shift;
+    c.in = col < a.N;
+    c.kpos = c.kb * BK + kr;
+    c.w = wb + c.kpos * wpr + (col >> 5) * BITS;
+    c.s = sb + c.kpos * gpr + (col >> a.group_shift);
+    c.b = bb + c.kpos * gpr + (col >> a.group_shift);
+  }
+  constexpr int kAlign = BITS % 4 == 0 ? 16 : BITS % 2 == 0 ? 8 : 4;  // bytes
+  c.vec = (reinterpret_cast<uintptr_t>(c.w) & (kAlign - 1)) == 0;
+}
+
+// Load the item at the cursor's k-block into `it` and step the cursor.
+// Items outside W (rows or columns past its edge, codes past K) read as zero.
+template <int BITS, bool TRANS>
+__device__ __forceinline__ void cursor_load(const GemmArgs &a, int nk, int dt, int num_units,
+                                            ItemCursor<BITS, TRANS> &c, ItemLoad<BITS> &it) {
+#pragma unroll
+  for (int i = 0; i < BITS; ++i) it.v[i] = 0u;
+  it.sb = 0u;
+  it.live = c.unit < num_units;
+  if (!it.live) return;
+  if (c.in && c.kpos < a.K) {
+    if (c.vec) {
+      load_words<BITS>(c.w, it.v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < BITS; ++i) it.v[i] = __ldg(c.w + i);
+    }
+    const int g = TRANS ? (c.kpos >> a.group_shift) : 0;
+    it.sb = __ldg(c.s + g) | (static_cast<uint32_t>(__ldg(c.b + g)) << 16);
+  }
+  if (++c.kb == c.kb1) {
+    c.unit += gridDim.x;
+    if (c.unit < num_units) cursor_unit<BITS, TRANS>(a, nk, dt, c);
+  } else if (TRANS) {
+    c.kpos += BK;
+    c.w += 2 * BITS;
+  } else {
+    const int64_t wpr = (static_cast<int64_t>(a.N) * BITS) >> 5;
+    const int64_t gpr = a.N >> a.group_shift;
+    c.kpos += BK;
+    c.w += BK * wpr;
+    c.s += BK * gpr;
+    c.b += BK * gpr;
+  }
+}
+
 template <typename E, int BITS, bool TRANS>
 __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int nk) {
   const int dt = threadIdx.x - 32 * (2 + kEpiWarps);  // 0 .. 32 * kDeqWarps - 1
@@ -320,33 +376,12 @@ __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int
   volatile int *abort = &bars->abort;
   // Stages are consumed in order (unit, kb); the codes of the next kLoadAhead
   // stages are always in flight in register buffers while one is dequantized.
-  // The unit being dequantized and the unit being loaded, each with its
-  // k-block; a unit's range is worked out once, when a thread moves to it.
-  int unit = blockIdx.x;
-  Unit cu = unit_of(a, unit < num_units ? unit : 0, nk);
-  int kb = cu.kb0;
-  int punit = unit, pkb = kb;
-  Unit pu = cu;
-  auto advance = [&](int &u, Unit &un, int &k) {
-    if (++k == un.kb1) {
-      u += gridDim.x;
-      if (u < num_units) {
-        un = unit_of(a, u, nk);
-        k = un.kb0;
-      }
-    }
-  };
-  auto prefetch = [&](ItemLoad<BITS> &buf) {
-    if (punit >= num_units) return;
-    int row, col;
-    uint32_t off[4];
-    item_place<TRANS>(dt, (pu.tile / a.m_tiles) * BN, pkb, row, col, off);
-    load_item<BITS, TRANS>(a, row, col, a.plan ? row_tile(a, pu.tile % a.m_tiles).expert : 0, buf);
-    advance(punit, pu, pkb);
-  };
+  ItemCursor<BITS, TRANS> c;
+  c.unit = blockIdx.x;
+  if (c.unit < num_units) cursor_unit<BITS, TRANS>(a, nk, dt, c);
   ItemLoad<BITS> buf[kLoadAhead];
 #pragma unroll
-  for (int i = 0; i < kLoadAhead; ++i) prefetch(buf[i]);
+  for (int i = 0; i < kLoadAhead; ++i) cursor_load<BITS, TRANS>(a, nk, dt, num_units, c, buf[i]);
   int s = 0;
   uint32_t ph = 0;
   uint32_t off[4];
@@ -356,9 +391,9 @@ __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int
   }
   // One stage out of `buf`, which is then refilled; false when done or stopped.
   auto step = [&](ItemLoad<BITS> &buf) -> bool {
-    if (unit >= num_units) return false;
     const ItemLoad<BITS> cur = buf;
-    prefetch(buf);
+    if (!cur.live) return false;
+    cursor_load<BITS, TRANS>(a, nk, dt, num_units, c, buf);
     if (!wait_warp(&bars->empty_b[s], ph ^ 1u, abort, a.err, a.spin_limit)) return false;
     const uint32_t base = smem_u32(sB + s * B_BYTES);
     const uint32_t hs = cur.sb & 0xFFFFu, hb = cur.sb >> 16;
@@ -393,7 +428,6 @@ __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int
     __syncwarp();
     if ((dt & 31) == 0) mbar_arrive(&bars->full_b[s]);
     if (++s == SB) { s = 0; ph ^= 1u; }
-    advance(unit, cu, kb);
     return true;
   };
   for (bool more = true; more;) {
