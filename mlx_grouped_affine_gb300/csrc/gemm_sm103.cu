@@ -51,11 +51,11 @@ constexpr int BM = 2 * UM; // x rows per tile: two MMAs share each dequantized W
 constexpr int BN = 256;   // weight rows per tile (MMA N)
 constexpr int BK = 64;    // codes per stage: one 128-byte swizzle atom of bf16
 // Separate rings for the x tiles and the dequantized W tiles.  Measured on
-// the 2048 x 14336 x 4096 case: the MMA waits mostly on W (the dequant warps
-// can only start a stage once the MMAs have freed its slot), so W gets the
-// deeper ring.
+// the 2048 x 14336 x 4096 and 128 x 4096 x 14336 cases: two or three W
+// stages run as fast as four (the dequant warps, not the ring, set the
+// pace), and the shared memory left to L1 serves their loads.
 constexpr int SA = 2;  // x stages
-constexpr int SB = 4;  // W stages
+constexpr int SB = 3;  // W stages
 constexpr int kEpiWarps = 4;
 constexpr int kDeqWarps = 16;  // one 32-code item of a stage per thread
 constexpr int kLoadAhead = 2;  // stages of packed codes in flight per dequant thread
