@@ -60,7 +60,26 @@ constexpr int kEpiWarps = 4;
 constexpr int kDeqWarps = 16;  // one 32-code item of a stage per thread
 constexpr int kLoadAhead = 2;  // stages of packed codes in flight per dequant thread
 static_assert(32 * kDeqWarps == BN * BK / 32, "one item per dequant thread");
-constexpr int kThreads = 32 * (2 + kEpiWarps + kDeqWarps);
+// TMA-fed dequant (W stored [N, K] at an even width whose rows and groups
+// TMA can address): warp 2 + kEpiWarps + kDeqWarps stages each k-block's
+// packed codes [BN rows x 64 codes] and, every kSbWin groups, a window of
+// the tile rows' scales and biases in shared memory; the dequant warps read
+// their items there instead of from global memory (per-thread global loads
+// of 16-32 bytes from 16 rows a warp cost L1 a wavefront per row).
+constexpr int kSbWin = 8;                               // groups per scale/bias window
+constexpr int SS = 2;                                   // scale/bias window slots
+constexpr uint32_t SB_WIN_BYTES = 2 * BN * kSbWin * 2;  // scales [BN][8], then biases
+constexpr int kMaxPStages = 4;
+template <int BITS>
+__host__ __device__ constexpr uint32_t p_bytes() { return BN * 8 * BITS; }  // one k-block of codes
+template <int BITS>
+__host__ __device__ constexpr int p_stages() {
+  return 49152 / p_bytes<BITS>() < kMaxPStages ? 49152 / p_bytes<BITS>() : kMaxPStages;
+}
+template <bool WTMA>
+__host__ __device__ constexpr int gemm_threads() {
+  return 32 * (2 + kEpiWarps + kDeqWarps + (WTMA ? 1 : 0));
+}
 constexpr uint32_t A_BYTES = BM * BK * 2;
 constexpr uint32_t A_HALF = UM * BK * 2;
 constexpr uint32_t B_BYTES = BN * BK * 2;
@@ -69,12 +88,19 @@ constexpr uint32_t kSpinLimit = 1u << 24;
 
 struct Barriers {
   uint64_t full_a[SA], empty_a[SA], full_b[SB], empty_b[SB];
+  uint64_t full_p[kMaxPStages], empty_p[kMaxPStages], full_s[SS], empty_s[SS];
   uint64_t tmem_full, tmem_empty, mma_done;
   uint32_t tmem_base;
   int abort;
 };
 
-constexpr size_t kSmemBytes = SA * A_BYTES + SB * B_BYTES + sizeof(Barriers) + 1024;
+// Shared memory: x ring, dequantized W ring, [packed code ring, scale/bias
+// windows,] barriers; + 1024 for aligning the base.
+template <int BITS, bool WTMA>
+constexpr size_t smem_bytes() {
+  return SA * A_BYTES + SB * B_BYTES +
+         (WTMA ? p_stages<BITS>() * p_bytes<BITS>() + SS * SB_WIN_BYTES : 0) + sizeof(Barriers) + 1024;
+}
 
 struct GemmArgs {
   const uint32_t *w;
@@ -93,6 +119,7 @@ struct GemmArgs {
   // from the plan on the device.
   const int *plan = nullptr;
   int64_t w_bstride = 0, sb_bstride = 0;
+  int w_batches = 1;  // weight batches the arrays hold (host side: tensor map extents)
   uint32_t spin_limit = kDefaultWaitLimit;  // polls of a bounded wait before it gives up
 };
 
@@ -286,6 +313,39 @@ __device__ __forceinline__ void item_place(int dt, int tile_n0, int kb, int &row
   }
 }
 
+// One item's 32 codes (v, `bits` words) dequantized with scale bits hs and
+// bias bits hb into the four 16-byte chunks of the W tile at base + off[j].
+// The fast form is bf16's (fp16 has no room for its multipliers); a warp
+// takes it when every lane's scale allows it.
+template <typename E, int BITS>
+__device__ __forceinline__ void dequant_store(const uint32_t (&v)[BITS], uint32_t hs, uint32_t hb,
+                                              uint32_t base, const uint32_t (&off)[4]) {
+  const uint32_t b2 = hb * 0x00010001u;
+  bool fast = false;
+  if constexpr (!E::kF16) fast = __all_sync(0xffffffffu, fast_scale(hs));
+  if (fast) {
+    uint32_t m[fast_slots<BITS>()];
+    fast_muls<BITS>(hs, m);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = pair_fast<BITS>(v, 4 * j + i, m, b2);
+      st_shared_v4(base + off[j], o);
+    }
+  } else {
+    const uint32_t s2 = hs * 0x00010001u;
+    const float sf = E::to_f32(hs), bf = E::to_f32(hb);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = pair_exact<BITS, E>(v, 4 * j + i, s2, b2, sf, bf);
+      st_shared_v4(base + off[j], o);
+    }
+  }
+}
+
 // A dequant thread's item across the stages of its block: the unit and
 // k-block it loads next, with the pointers of its codes and of its row's (or
 // column's) scales and biases.  Moving to the next k-block is a pointer step;
@@ -396,32 +456,7 @@ __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int
     cursor_load<BITS, TRANS>(a, nk, dt, num_units, c, buf);
     if (!wait_warp(&bars->empty_b[s], ph ^ 1u, abort, a.err, a.spin_limit)) return false;
     const uint32_t base = smem_u32(sB + s * B_BYTES);
-    const uint32_t hs = cur.sb & 0xFFFFu, hb = cur.sb >> 16;
-    const uint32_t b2 = hb * 0x00010001u;
-    // The fast form is bf16's (fp16 has no room for its multipliers).
-    bool fast = false;
-    if constexpr (!E::kF16) fast = __all_sync(0xffffffffu, fast_scale(hs));
-    if (fast) {
-      uint32_t m[fast_slots<BITS>()];
-      fast_muls<BITS>(hs, m);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = pair_fast<BITS>(cur.v, 4 * j + i, m, b2);
-        st_shared_v4(base + off[j], v);
-      }
-    } else {
-      const uint32_t s2 = hs * 0x00010001u;
-      const float sf = E::to_f32(hs), bf = E::to_f32(hb);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = pair_exact<BITS, E>(cur.v, 4 * j + i, s2, b2, sf, bf);
-        st_shared_v4(base + off[j], v);
-      }
-    }
+    dequant_store<E, BITS>(cur.v, cur.sb & 0xFFFFu, cur.sb >> 16, base, off);
     // Each thread makes its stores visible to the tensor cores, then one
     // arrival per warp.
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -434,6 +469,152 @@ __device__ void dequant_role(const GemmArgs &a, uint8_t *sB, Barriers *bars, int
 #pragma unroll
     for (int i = 0; i < kLoadAhead; ++i)
       if (more) more = step(buf[i]);
+  }
+}
+
+// TMA-fed dequant, producer (one warp, lane 0 issues): for every k-block of
+// the block's units, the packed codes of the tile's BN rows (a [BN x 2*bits]
+// word box) into the next code slot, and at each new window of kSbWin groups
+// the rows' scales and biases ([BN x 8] boxes) into the next window slot.
+// Weight batch e's row n is row e*N + n of the maps.
+template <int BITS>
+__device__ void w_tma_role(const CUtensorMap *wmap, const CUtensorMap *smap,
+                           const CUtensorMap *bmap, const GemmArgs &a, uint8_t *sP, uint8_t *sS,
+                           Barriers *bars, int nk) {
+  constexpr int SP = p_stages<BITS>();
+  const int lane = threadIdx.x & 31;
+  const int num_units = a.m_tiles * a.n_tiles * a.splits;
+  volatile int *abort = &bars->abort;
+  int ps = 0, ss = 0;
+  uint32_t pph = 0, sph = 0;
+  // Parity of the last load issued into each slot, for the drain after a stop.
+  int pend_p[SP], pend_s[SS];
+#pragma unroll
+  for (int i = 0; i < SP; ++i) pend_p[i] = -1;
+#pragma unroll
+  for (int i = 0; i < SS; ++i) pend_s[i] = -1;
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+    const Unit un = unit_of(a, u, nk);
+    const int expert = a.plan ? row_tile(a, un.tile % a.m_tiles).expert : 0;
+    const int row0 = expert * a.N + (un.tile / a.m_tiles) * BN;
+    int win = -1;
+    for (int kb = un.kb0; kb < un.kb1; ++kb) {
+      const int w = (kb * BK) >> (a.group_shift + 3);
+      if (w != win) {
+        if (!wait_warp(&bars->empty_s[ss], sph ^ 1u, abort, a.err, a.spin_limit)) { ok = false; break; }
+        if (lane == 0) {
+          const uint32_t dst = smem_u32(sS + ss * SB_WIN_BYTES);
+          mbar_expect_tx(&bars->full_s[ss], SB_WIN_BYTES);
+          tma_load_2d(dst, smap, w * kSbWin, row0, &bars->full_s[ss]);
+          tma_load_2d(dst + SB_WIN_BYTES / 2, bmap, w * kSbWin, row0, &bars->full_s[ss]);
+        }
+        __syncwarp();
+        pend_s[ss] = static_cast<int>(sph);
+        win = w;
+        if (++ss == SS) { ss = 0; sph ^= 1u; }
+      }
+      if (!wait_warp(&bars->empty_p[ps], pph ^ 1u, abort, a.err, a.spin_limit)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_expect_tx(&bars->full_p[ps], p_bytes<BITS>());
+        tma_load_2d(smem_u32(sP + ps * p_bytes<BITS>()), wmap, kb * 2 * BITS, row0, &bars->full_p[ps]);
+      }
+      __syncwarp();
+      pend_p[ps] = static_cast<int>(pph);
+      if (++ps == SP) { ps = 0; pph ^= 1u; }
+    }
+  }
+  if (!ok) {
+    // Stopped early: wait (bounded) for the copies still in flight.
+#pragma unroll
+    for (int i = 0; i < SP; ++i) {
+      if (pend_p[i] < 0) continue;
+      for (uint32_t spin = 0; spin < kSpinLimit; ++spin)
+        if (__all_sync(0xffffffffu, mbar_try_wait(&bars->full_p[i], pend_p[i]))) break;
+    }
+#pragma unroll
+    for (int i = 0; i < SS; ++i) {
+      if (pend_s[i] < 0) continue;
+      for (uint32_t spin = 0; spin < kSpinLimit; ++spin)
+        if (__all_sync(0xffffffffu, mbar_try_wait(&bars->full_s[i], pend_s[i]))) break;
+    }
+  }
+}
+
+// TMA-fed dequant, consumers: the same items as dequant_role (thread (r, h)
+// takes codes [32h, 32h+32) of tile row r), read from the staged codes and
+// scale/bias window; a code slot is released as soon as its words are in
+// registers, a window when the unit moves past it.  Rows and codes outside W
+// arrive as zeros (codes 0, scale and bias 0: weight 0).
+template <typename E, int BITS>
+__device__ void dequant_role_tma(const GemmArgs &a, uint8_t *sB, const uint8_t *sP,
+                                 const uint8_t *sS, Barriers *bars, int nk) {
+  constexpr int SP = p_stages<BITS>();
+  const int dt = threadIdx.x - 32 * (2 + kEpiWarps);  // 0 .. 32 * kDeqWarps - 1
+  const int lane = dt & 31, r = dt >> 1, h = dt & 1;
+  const int num_units = a.m_tiles * a.n_tiles * a.splits;
+  volatile int *abort = &bars->abort;
+  uint32_t off[4];
+  {
+    int row, col;
+    item_place<true>(dt, 0, 0, row, col, off);
+  }
+  // This thread's words inside a code slot and its row inside a window.
+  const uint32_t p_off = r * (8 * BITS) + h * (4 * BITS);
+  const uint32_t s_off = r * (2 * kSbWin);
+  int ps = 0, ss = 0, s = 0;
+  uint32_t pph = 0, sph = 0, ph = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+    const Unit un = unit_of(a, u, nk);
+    int win = -1, cur = 0;
+    for (int kb = un.kb0; kb < un.kb1; ++kb) {
+      const int w = (kb * BK) >> (a.group_shift + 3);
+      if (w != win) {
+        if (win >= 0) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->empty_s[cur]);
+        }
+        if (!wait_warp(&bars->full_s[ss], sph, abort, a.err, a.spin_limit)) { ok = false; break; }
+        cur = ss;
+        win = w;
+        if (++ss == SS) { ss = 0; sph ^= 1u; }
+      }
+      if (!wait_warp(&bars->full_p[ps], pph, abort, a.err, a.spin_limit)) { ok = false; break; }
+      uint32_t v[BITS];
+      const uint32_t pa = smem_u32(sP + ps * p_bytes<BITS>()) + p_off;
+      if constexpr (BITS % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < BITS / 4; ++i)
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(v[4 * i]), "=r"(v[4 * i + 1]), "=r"(v[4 * i + 2]), "=r"(v[4 * i + 3])
+                       : "r"(pa + 16 * i));
+      } else {
+#pragma unroll
+        for (int i = 0; i < BITS / 2; ++i)
+          asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v[2 * i]), "=r"(v[2 * i + 1]) : "r"(pa + 8 * i));
+      }
+      const int g = ((kb * BK + 32 * h) >> a.group_shift) & (kSbWin - 1);
+      const uint32_t sa = smem_u32(sS + cur * SB_WIN_BYTES) + s_off + 2 * g;
+      uint32_t hs, hb;
+      asm volatile("ld.shared.u16 %0, [%1];" : "=r"(hs) : "r"(sa));
+      asm volatile("ld.shared.u16 %0, [%1];" : "=r"(hb) : "r"(sa + SB_WIN_BYTES / 2));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->empty_p[ps]);
+      if (++ps == SP) { ps = 0; pph ^= 1u; }
+      if (!wait_warp(&bars->empty_b[s], ph ^ 1u, abort, a.err, a.spin_limit)) { ok = false; break; }
+      dequant_store<E, BITS>(v, hs, hb, smem_u32(sB + s * B_BYTES), off);
+      // Each thread makes its stores visible to the tensor cores, then one
+      // arrival per warp.
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->full_b[s]);
+      if (++s == SB) { s = 0; ph ^= 1u; }
+    }
+    if (ok && win >= 0) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->empty_s[cur]);
+    }
   }
 }
 
@@ -626,9 +807,13 @@ __device__ void epilogue_role(const GemmArgs &a, Barriers *bars, uint32_t tmem) 
   }
 }
 
-template <typename E, int BITS, bool OUT_BF16, bool TRANS>
-__global__ void __launch_bounds__(kThreads, 1)
-gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, GemmArgs a) {
+// WTMA: the TMA-fed dequant (maps of the packed codes, scales and biases in
+// tmap_w / tmap_s / tmap_b); otherwise those three maps are unused.
+template <typename E, int BITS, bool OUT_BF16, bool TRANS, bool WTMA>
+__global__ void __launch_bounds__(gemm_threads<WTMA>(), 1)
+gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+            const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_b,
+            GemmArgs a) {
   // Grouped mode: the row tiles in use, as the plan kernel counted them.
   if (a.plan) a.m_tiles = __ldg(a.plan);
   extern __shared__ uint8_t smem_raw[];
@@ -636,7 +821,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, GemmArgs a) {
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + SA * A_BYTES;
-  Barriers *bars = reinterpret_cast<Barriers *>(sB + SB * B_BYTES);
+  uint8_t *sP = sB + SB * B_BYTES;
+  uint8_t *sS = sP + (WTMA ? p_stages<BITS>() * p_bytes<BITS>() : 0);
+  Barriers *bars = reinterpret_cast<Barriers *>(sS + (WTMA ? SS * SB_WIN_BYTES : 0));
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
@@ -648,12 +835,25 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, GemmArgs a) {
       mbar_init(&bars->full_b[i], kDeqWarps);
       mbar_init(&bars->empty_b[i], 1);
     }
+    for (int i = 0; i < kMaxPStages; ++i) {
+      mbar_init(&bars->full_p[i], 1);
+      mbar_init(&bars->empty_p[i], kDeqWarps);
+    }
+    for (int i = 0; i < SS; ++i) {
+      mbar_init(&bars->full_s[i], 1);
+      mbar_init(&bars->empty_s[i], kDeqWarps);
+    }
     mbar_init(&bars->tmem_full, 1);
     mbar_init(&bars->tmem_empty, 32 * kEpiWarps);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_x) : "memory");
+    if (WTMA) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_w) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_s) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_b) : "memory");
+    }
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -670,7 +870,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, GemmArgs a) {
   if (warp == 0) tma_role(&tmap_x, a, sA, bars, nk);
   else if (warp == 1) mma_role<E, TRANS>(a, sA, sB, bars, nk, tmem);
   else if (warp < 2 + kEpiWarps) epilogue_role<E, OUT_BF16>(a, bars, tmem);
-  else dequant_role<E, BITS, TRANS>(a, sB, bars, nk);
+  else if (warp < 2 + kEpiWarps + kDeqWarps) {
+    if constexpr (WTMA) dequant_role_tma<E, BITS>(a, sB, sP, sS, bars, nk);
+    else dequant_role<E, BITS, TRANS>(a, sB, bars, nk);
+  } else if constexpr (WTMA) {
+    w_tma_role<BITS>(&tmap_w, &tmap_s, &tmap_b, a, sP, sS, bars, nk);
+  }
 
   tc_fence_before();
   __syncthreads();
@@ -754,13 +959,43 @@ cudaError_t launch_t(const uint16_t *x, const GemmArgs &a, cudaStream_t stream) 
                                  static_cast<uint64_t>(a.K) * 2, BK, BM,
                                  CU_TENSOR_MAP_SWIZZLE_128B);
   if (me != cudaSuccess) return me;
-  auto kern = gemm_kernel<E, BITS, OUT_BF16, TRANS>;
-  const cudaError_t ae = ensure_smem_limit<gemm_kernel<E, BITS, OUT_BF16, TRANS>>(kSmemBytes);
-  if (ae != cudaSuccess) return ae;
   const int units = a.m_tiles * a.n_tiles * a.splits;
   const int grid = units < sm_count() ? units : sm_count();
-  kern<<<grid, kThreads, kSmemBytes, stream>>>(map, a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = cudaErrorNotSupported;
+  // The TMA-fed dequant where TMA can address W's rows, its k-blocks' words
+  // and its scale/bias windows (16-byte boxes and strides).
+  if constexpr (TRANS && BITS % 2 == 0) {
+    const uint64_t rows = static_cast<uint64_t>(a.N) * a.w_batches;
+    const int64_t groups = a.K >> a.group_shift;
+    if ((static_cast<int64_t>(a.K) * BITS) % 128 == 0 && groups % kSbWin == 0 &&
+        rows < (uint64_t(1) << 31) && (reinterpret_cast<uintptr_t>(a.w) & 15u) == 0 &&
+        (reinterpret_cast<uintptr_t>(a.scales) & 15u) == 0 &&
+        (reinterpret_cast<uintptr_t>(a.biases) & 15u) == 0) {
+      CUtensorMap wm, sm, bm;
+      const uint64_t wpr = static_cast<uint64_t>(a.K) * BITS / 32;
+      if (encode_map_2d(&wm, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.w, wpr, rows, wpr * 4, 2 * BITS, BN,
+                        CU_TENSOR_MAP_SWIZZLE_NONE) == cudaSuccess &&
+          encode_map_2d(&sm, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, groups, rows, groups * 2,
+                        kSbWin, BN, CU_TENSOR_MAP_SWIZZLE_NONE) == cudaSuccess &&
+          encode_map_2d(&bm, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.biases, groups, rows, groups * 2,
+                        kSbWin, BN, CU_TENSOR_MAP_SWIZZLE_NONE) == cudaSuccess) {
+        constexpr size_t smem = smem_bytes<BITS, true>();
+        const cudaError_t ae = ensure_smem_limit<gemm_kernel<E, BITS, OUT_BF16, TRANS, true>>(smem);
+        if (ae != cudaSuccess) return ae;
+        gemm_kernel<E, BITS, OUT_BF16, TRANS, true><<<grid, gemm_threads<true>(), smem, stream>>>(
+            map, wm, sm, bm, a);
+        e = cudaGetLastError();
+      }
+    }
+  }
+  if (e == cudaErrorNotSupported) {
+    constexpr size_t smem = smem_bytes<BITS, false>();
+    const cudaError_t ae = ensure_smem_limit<gemm_kernel<E, BITS, OUT_BF16, TRANS, false>>(smem);
+    if (ae != cudaSuccess) return ae;
+    gemm_kernel<E, BITS, OUT_BF16, TRANS, false><<<grid, gemm_threads<false>(), smem, stream>>>(
+        map, map, map, map, a);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess || a.splits == 1) return e;
   const int64_t mn = static_cast<int64_t>(a.M) * a.N;
   int64_t blocks = (mn / 4 + 255) / 256;
@@ -961,6 +1196,7 @@ cudaError_t launch_gemm_grouped(const uint16_t *x, int64_t batches, const Packed
   if (!a.err) return cudaErrorInvalidSymbol;
   a.w_bstride = w.rows * ((w.cols * w.bits) / 32);
   a.sb_bstride = w.rows * (w.cols / w.group);
+  a.w_batches = static_cast<int>(w_batches);
   void *p = nullptr;
   cudaError_t e = cudaMallocAsync(&p, sizeof(int) * (1 + 3 * static_cast<size_t>(a.m_tiles)), stream);
   if (e != cudaSuccess) {  // no plan buffer: the caller takes the decode kernels instead
