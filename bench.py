@@ -413,12 +413,25 @@ def fused_detail(torch, qmm, synth, peaks, warmup):
     def fused_silu():
         for r in range(R):
             qmm.qmm_gemv_silu_gate(gate, up, 1, *ws[r], N, K, 64, 4, resid, y[r], qmm.QMM_BF16)
-    t = time_graph(torch, graph_of(torch, fused_silu), 200, warmup) / R
-    out["gemv_silu_gate_resid_%dx%d_b4_M1" % (N, K)] = {
-        "us": round(t * 1e3, 2), "GB/s": round(nbytes / (t * 1e-3) / 1e9, 1),
-        "frac_hbm": round(nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
+    # The calls it replaces: x = RN_bf16(silu(gate) * up) and y + resid as
+    # PyTorch elementwise kernels around the plain GEMV (bf16 in and out).
+    gb, ub = gate.view(torch.bfloat16), up.view(torch.bfloat16)
+    rb = resid.view(torch.bfloat16)
+    xs = torch.empty((1, K), dtype=torch.bfloat16, device="cuda")
+    yt = torch.empty((R, 1, N), dtype=torch.int16, device="cuda")
+
+    def unfused_silu():
+        for r in range(R):
+            torch.mul(torch.nn.functional.silu(gb.float()), ub.float(), out=xs)
+            qmm.qmm_quantized_matmul(xs.view(torch.int16), 1, *ws[r], N, K, 1, 64, 4, yt[r], qmm.QMM_BF16)
+            y[r].view(torch.bfloat16).copy_(yt[r].view(torch.bfloat16) + rb)
+    for name, fn in (("gemv_silu_gate_resid_%dx%d_b4_M1" % (N, K), fused_silu),
+                     ("gemv_silu_gate_resid_unfused_%dx%d_b4_M1" % (N, K), unfused_silu)):
+        t = time_graph(torch, graph_of(torch, fn), 200, warmup) / R
+        out[name] = {"us": round(t * 1e3, 2), "GB/s": round(nbytes / (t * 1e-3) / 1e9, 1),
+                     "frac_hbm": round(nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
     qmm.qmm_set_launch_flags(flags)
-    del ws, y
+    del ws, y, yt
     torch.cuda.empty_cache()
     return out
 
