@@ -62,6 +62,11 @@ cudaError_t launch_fused_bits(const GemvArgs &a, int fuse, const FuseArgs &f, co
   if (fuse == kFuseDual) {
     Batches two;
     two.count = 2;
+    // Both weights' row tiles together more than two 16-warp blocks an SM hold:
+    // 8-warp blocks, as for the plain decode GEMV.
+    if (BITS < 6 && a.M <= 8 && 2 * ((a.N + 15) / 16) > 2 * sm_count())
+      return y_bf16 ? launch_t_tma<ElemBF16, BITS, 1, true, false, kFuseDual, 8>(a, pdl, two, stream, f, w2)
+                    : launch_t_tma<ElemBF16, BITS, 1, false, false, kFuseDual, 8>(a, pdl, two, stream, f, w2);
     if (a.M <= 8)
       return y_bf16 ? launch_t_tma<ElemBF16, BITS, 1, true, false, kFuseDual>(a, pdl, two, stream, f, w2)
                     : launch_t_tma<ElemBF16, BITS, 1, false, false, kFuseDual>(a, pdl, two, stream, f, w2);

@@ -497,8 +497,10 @@ constexpr int kTmaMaxChunksPerWarp = 4;
 // (A minimum of 0 blocks leaves the register budget to the compiler, as with
 // no minimum given; the gather and fused instantiations are held to two
 // blocks per SM.)
-template <typename E, int BITS, int NT, bool OUT_BF16, bool GATHER, int FUSE>
-__global__ void __launch_bounds__(32 * tma_warps<NT>(), GATHER || FUSE ? 2 : 0)
+// W: warps per block (the default for NT, or 8 for one n8 tile: blocks of
+// 16K registers, four an SM, for weights with many row tiles).
+template <typename E, int BITS, int NT, bool OUT_BF16, bool GATHER, int FUSE, int W = tma_warps<NT>()>
+__global__ void __launch_bounds__(32 * W, W < tma_warps<NT>() ? 4 : (GATHER || FUSE ? 2 : 0))
 gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayout L,
                   unsigned *err, GatherArgs ga, const __grid_constant__ CUtensorMap wmap2,
                   FuseArgs fa) {
@@ -597,7 +599,7 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
   // Scales and biases of every chunk this warp will compute, before the
   // wait: they are weights too, and their HBM latency then overlaps the
   // previous kernel instead of the chunk loop.
-  constexpr int kW = tma_warps<NT>();
+  constexpr int kW = W;
   uint16_t sv[kTmaMaxChunksPerWarp][4];
 #pragma unroll
   for (int j = 0; j < kTmaMaxChunksPerWarp; ++j) {
@@ -736,7 +738,7 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) flat[nt * 4 + i] = acc[0][nt][i] + acc[1][nt][i];
-    reduce_and_store<E, NT * 4>(flat, red, tma_warps<NT>(), static_cast<int>(csize), ac, OUT_BF16,
+    reduce_and_store<E, NT * 4>(flat, red, W, static_cast<int>(csize), ac, OUT_BF16,
                              [&](int ln, int i, int &m, int &n) {
                                const int gg = ln >> 2, tt = ln & 3, nt = i >> 2, e = i & 3;
                                n = n0 + gg + 8 * (e >> 1);
@@ -849,7 +851,8 @@ cudaError_t launch_t(const GemvArgs &a0, const Batches &b, cudaStream_t stream) 
   });
 }
 
-template <typename E, int BITS, int NT, bool OUT_BF16, bool GATHER, int FUSE = kFuseNone>
+template <typename E, int BITS, int NT, bool OUT_BF16, bool GATHER, int FUSE = kFuseNone,
+          int W = tma_warps<NT>()>
 cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, const Batches &b, cudaStream_t stream,
                          const FuseArgs &f = FuseArgs{}, const uint32_t *w2 = nullptr) {
   const int64_t tiles = (a.N + 15) / 16;
@@ -857,12 +860,12 @@ cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, const Batches &b, cudaStre
   auto kr_of = [&](int c) { return ((a.K / c + 127) / 128) * 128; };
   auto smem_of = [&](int c) {
     const int kr = kr_of(c);
-    return (kr / 128) * (box_bytes + 8) + tma_warps<NT>() * NT * 4 * 32 * 4 + 2048;
+    return (kr / 128) * (box_bytes + 8) + W * NT * 4 * 32 * 4 + 2048;
   };
   // Split K over a cluster only when the weight has too few 16-row tiles to
   // give every SM work, or one block's share would not fit.
   int C = 1;
-  const int max_kr = 128 * kTmaMaxChunksPerWarp * tma_warps<NT>();
+  const int max_kr = 128 * kTmaMaxChunksPerWarp * W;
   while (C < 8 && kr_of(2 * C) >= 128 &&
          (tiles * C < 240 || smem_of(C) > 100 * 1024 || kr_of(C) > max_kr))
     C *= 2;
@@ -876,7 +879,7 @@ cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, const Batches &b, cudaStre
   L.x_off = nch * box_bytes;
   L.xpitch = FUSE == kFuseSilu ? L.kr * 2 + 16 : 0;
   L.red_off = L.x_off + a.M * L.xpitch;
-  L.bar_off = L.red_off + tma_warps<NT>() * NT * 4 * 32 * 4;
+  L.bar_off = L.red_off + W * NT * 4 * 32 * 4;
   const size_t smem = L.bar_off + 8 * (nch + 1) + 1024;  // + slack for the 1024-byte base
   if (smem > 220 * 1024) return cudaErrorNotSupported;
   // The tensor map spans every weight batch: batch e's row n is row e*N + n.
@@ -897,13 +900,13 @@ cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, const Batches &b, cudaStre
   }
   unsigned *err = device_error_word();
   if (!err) return cudaErrorInvalidSymbol;
-  auto kern = gemv_t_tma_kernel<E, BITS, NT, OUT_BF16, GATHER, FUSE>;
+  auto kern = gemv_t_tma_kernel<E, BITS, NT, OUT_BF16, GATHER, FUSE, W>;
   if (smem > 48 * 1024) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
   return over_z(b, [&](const GatherArgs &g, unsigned nz) {
-    return launch_ex(kern, dim3(static_cast<unsigned>(tiles), C, nz), dim3(32 * tma_warps<NT>()),
+    return launch_ex(kern, dim3(static_cast<unsigned>(tiles), C, nz), dim3(32 * W),
                      smem, C, pdl, stream, wmap, a, L, err, g, wmap2, f);
   });
 }
@@ -931,26 +934,17 @@ template <typename E, int BITS>
 cudaError_t launch_bits(const GemvArgs &a, bool transpose, bool y_16, bool pdl,
                         cudaStream_t stream) {
   const Batches one;
-  // More 16-row tiles than two one-tile blocks an SM hold at once, at 1 to 3
-  // bits: the persistent streaming kernel (measured on [11008, 4096], M = 1:
-  // 12-13 % faster at 1 and 2 bits, 4 % at 3; no faster at 4 bits).
-  if constexpr (!E::kF16 && BITS <= 3) {
-    if (transpose && a.M <= 8 && a.K % 128 == 0 && (a.N + 15) / 16 > 2 * sm_count()) {
-      PackedWeight pw;
-      pw.w = a.w;
-      pw.scales = a.scales;
-      pw.biases = a.biases;
-      pw.rows = a.N;
-      pw.cols = a.K;
-      pw.group = 1 << a.group_shift;
-      pw.bits = BITS;
-      const cudaError_t e = launch_gemv_stream(a.x, a.M, pw, a.y, y_16, pdl, stream);
-      if (e != cudaErrorNotSupported) return e;
-    }
-  }
   if (transpose && a.K % 128 == 0) {
     cudaError_t e;
-    if (a.M <= 8)
+    // More row tiles than two 16-warp blocks an SM hold: 8-warp blocks (four an
+    // SM), so that twice the tiles stream at once (measured at M = 1: [14336,
+    // 4096] 4-bit 13.1 -> 10.8 us, [11008, 4096] 3-bit 12.9 -> 11.6 us).  6 and
+    // 8 bits keep 16 warps (6-bit 14.0 -> 14.6 us, 8-bit [14336, 4096] 15.2 ->
+    // 18.4 us), as do one-wave shapes ([4096, 4096] 4.24 us against 4.83).
+    if (BITS < 6 && a.M <= 8 && (a.N + 15) / 16 > 2 * sm_count())
+      e = y_16 ? launch_t_tma<E, BITS, 1, true, false, kFuseNone, 8>(a, pdl, one, stream)
+               : launch_t_tma<E, BITS, 1, false, false, kFuseNone, 8>(a, pdl, one, stream);
+    else if (a.M <= 8)
       e = y_16 ? launch_t_tma<E, BITS, 1, true, false>(a, pdl, one, stream)
                : launch_t_tma<E, BITS, 1, false, false>(a, pdl, one, stream);
     else

@@ -81,14 +81,6 @@ cudaError_t launch_gemv(const uint16_t *x, int64_t M, const PackedWeight &w,
                         bool transpose, void *y, bool y_bf16,
                         cudaStream_t stream);
 
-// gemv_stream.cu: transposed decode for weights with many 16-row tiles
-// (persistent blocks, whole tiles streamed by TMA): bf16, 1 to 3 bits,
-// M <= 8, K a multiple of 128 and at most 4096, K/G a multiple of 8 and at
-// most 256, 16-byte aligned arrays.  cudaErrorNotSupported (nothing
-// launched) for any other case.
-cudaError_t launch_gemv_stream(const uint16_t *x, int64_t M, const PackedWeight &w, void *y,
-                               bool y_bf16, bool pdl, cudaStream_t stream);
-
 // gemv_f16.cu: the same for fp16 x, scales and biases (y fp16 if y_f16).
 cudaError_t launch_gemv_f16(const uint16_t *x, int64_t M, const PackedWeight &w,
                             bool transpose, void *y, bool y_f16, cudaStream_t stream);

@@ -30,6 +30,22 @@ def test_gate_up(bits, M):
         assert_within_tolerance(y, ref, absy, "gate_up %s bits=%d M=%d" % (what, bits, M))
 
 
+@pytest.mark.parametrize("bits", (3, 4, 8))
+@pytest.mark.parametrize("M", (1, 8))
+def test_gate_up_many_row_tiles(bits, M):
+    # 2 x 157 row tiles, more than two 16-warp blocks an SM: the 8-warp form
+    # below 6 bits.
+    N, K, gs = 2500, 1024, 64
+    wg = synth.quant_weight(70 + bits, N, K, bits, gs)
+    wu = synth.quant_weight(71 + bits, N, K, bits, gs)
+    x = synth.x_bf16(72 + M, M, K)
+    yg, yu = empty_out((M, N), qmm.QMM_BF16), empty_out((M, N), qmm.QMM_BF16)
+    qmm.qmm_gemv_gate_up(dev(x), M, *weight(wg), *weight(wu), N, K, gs, bits, yg, yu, qmm.QMM_BF16)
+    for y, w in ((yg, wg), (yu, wu)):
+        ref, absy = oracle.qmm(x, M, w.packed, w.scales, w.biases, N, K, True, gs, bits)
+        assert_within_tolerance(y, ref, absy, "gate_up many tiles b%d M%d" % (bits, M))
+
+
 @pytest.mark.parametrize("bits", ALL_BITS)
 @pytest.mark.parametrize("M", (1, 3, 8))
 @pytest.mark.parametrize("with_resid", (False, True))

@@ -98,22 +98,22 @@ def test_odd_widths_full_size(bits, gs):
     check(x, 1, w, N, K, True, what="odd b%d g%d" % (bits, gs))
 
 
-# Weights with more 16-row tiles than two one-tile blocks per SM cover (N >
-# 2 * 16 * 152) at 1 to 3 bits take the persistent streaming kernel: several
-# tiles per block, a ragged last tile, M up to 8, both output types, both
-# dequantization forms (scales up to 0.2 leave the fast form's range).
-@pytest.mark.parametrize("bits", (1, 2, 3))
+# Weights with more 16-row tiles than two 16-warp blocks per SM cover (N >
+# 2 * 16 * 152) take 8-warp blocks: a ragged last tile, M up to 8, both output
+# types, both dequantization forms (scales up to 0.2 leave the fast form's
+# range); 6 and 8 bits keep 16-warp blocks.
+@pytest.mark.parametrize("bits", (1, 2, 3, 4, 6, 8))
 @pytest.mark.parametrize("M,gs,K,y_dtype,scale_hi", [
     (1, 32, 4096, qmm.QMM_BF16, 0.02),
     (5, 64, 4096, qmm.QMM_F32, 0.02),
     (8, 128, 2048, qmm.QMM_BF16, 0.2),
     (3, 64, 1024, qmm.QMM_F32, 0.2),
 ])
-def test_many_tiles_streaming(bits, M, gs, K, y_dtype, scale_hi):
+def test_many_row_tiles(bits, M, gs, K, y_dtype, scale_hi):
     N = 5003
     w = synth.quant_weight(300 + bits + M, N, K, bits, gs, scale_hi=scale_hi)
     x = synth.x_bf16(301 + M, M, K)
-    check(x, M, w, N, K, True, y_dtype, what="stream b%d M%d g%d K%d" % (bits, M, gs, K))
+    check(x, M, w, N, K, True, y_dtype, what="many tiles b%d M%d g%d K%d" % (bits, M, gs, K))
 
 
 @pytest.mark.parametrize("shape", synth.SWEEP_SHAPES)
