@@ -666,13 +666,16 @@ def run_gpu(args):
 def headline(detail, out):
     """A compact summary of the lines that carry the metric: decode (GB/s and
     fraction of HBM), the M = 2048 prefill (TFLOP/s and fraction of bf16
-    peak), odd widths, rows and dequantize."""
+    peak), odd widths, rows, dequantize, the fused GEMVs against their unfused
+    calls and the 4-bit M = 128 lines."""
     h = {"decode_b4_M1_4096x4096": {"GB/s": out["value"], "frac_hbm": out["roofline"]["frac"]}}
     for k, v in detail.items():
         if k.startswith("prefill_b4_M2048"):
             h[k] = {"us": v.get("us"), "TFLOP/s": v.get("TFLOP/s"), "frac_bf16": v.get("frac_bf16")}
-        elif k.startswith(("decode_b", "odd_", "rows_", "dequantize_", "reference_case")):
+        elif k.startswith(("decode_b", "odd_", "rows_", "dequantize_", "reference_case", "gemv_")):
             h[k] = {kk: v[kk] for kk in ("us", "frac_hbm") if kk in v}
+        elif k.startswith("sweep_b4_") and k.endswith("_M128"):
+            h[k] = {kk: v[kk] for kk in ("us", "frac_bf16") if kk in v}
     h["clocks_sm_mhz"] = out["clocks"].get("sm_mhz")
     return h
 
