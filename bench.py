@@ -789,6 +789,7 @@ PROFILE_CASES = {
     "splitk_m128_k14336": (128, 4096, 14336, 4, 64, True),
     "prefill_nt": (2048, 14336, 4096, 4, 64, False),
     "decode_b2_many_tiles": (1, 11008, 4096, 2, 32, True),
+    "decode_many_tiles": (1, 14336, 4096, 4, 64, True),
 }
 OTHER_PROFILES = ("gather_sorted", "silu_gate", "quantize", "dequantize", "rows", "f16_prefill",
                   "f16_decode", "f32_decode", "f32_decode16", "f32_prefill", "gather_prefill")
