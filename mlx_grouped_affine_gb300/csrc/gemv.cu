@@ -20,8 +20,15 @@ cudaError_t launch_gather_bits(const GemvArgs &a0, const Batches &b0, bool trans
       Batches bs = b0;
       bs.g.sorted = 1;
       bs.count = b0.g.w_batches + 1;
-      e = y_bf16 ? launch_t_tma<ElemBF16, BITS, 1, true, true>(a0, false, bs, stream)
-                 : launch_t_tma<ElemBF16, BITS, 1, false, true>(a0, false, bs, stream);
+      if (BITS < 6 && ((a0.N + 15) / 16) * bs.count > 2 * sm_count())
+        e = y_bf16 ? launch_t_tma<ElemBF16, BITS, 1, true, true, kFuseNone, 8>(a0, false, bs, stream)
+                   : launch_t_tma<ElemBF16, BITS, 1, false, true, kFuseNone, 8>(a0, false, bs, stream);
+      else
+        e = y_bf16 ? launch_t_tma<ElemBF16, BITS, 1, true, true>(a0, false, bs, stream)
+                   : launch_t_tma<ElemBF16, BITS, 1, false, true>(a0, false, bs, stream);
+    } else if (a0.M <= 8 && BITS < 6 && ((a0.N + 15) / 16) * b0.count > 2 * sm_count()) {
+      e = y_bf16 ? launch_t_tma<ElemBF16, BITS, 1, true, true, kFuseNone, 8>(a0, false, b0, stream)
+                 : launch_t_tma<ElemBF16, BITS, 1, false, true, kFuseNone, 8>(a0, false, b0, stream);
     } else if (a0.M <= 8) {
       e = y_bf16 ? launch_t_tma<ElemBF16, BITS, 1, true, true>(a0, false, b0, stream)
                  : launch_t_tma<ElemBF16, BITS, 1, false, true>(a0, false, b0, stream);

@@ -100,6 +100,23 @@ def test_sorted_runs(bits, y_dtype):
           what="sorted runs bits=%d" % bits)
 
 
+@pytest.mark.parametrize("bits", (3, 4, 5))
+@pytest.mark.parametrize("sorted_", (False, True))
+@pytest.mark.parametrize("y_dtype", (qmm.QMM_F32, qmm.QMM_BF16))
+def test_many_row_tiles(bits, sorted_, y_dtype):
+    # 8 experts of 1000 rows (63 row tiles, the last ragged) and 24 slots:
+    # more blocks than two a multiprocessor, so the decode runs 8-warp blocks.
+    E, N, K, gs = 8, 1000, 512, 64
+    packed, s, b = experts(800 + bits, E, N, K, bits, gs)
+    rhs = np.random.default_rng(bits).integers(0, E, 24).astype(np.uint32)
+    if sorted_:
+        rhs = np.sort(rhs)
+    B = len(rhs)
+    x = synth.x_bf16(801, B, K)
+    check(x, B, 1, packed, s, b, E, N, K, None, rhs, B, 1, gs, bits, sorted_=sorted_,
+          y_dtype=y_dtype, what="many row tiles bits=%d sorted=%d" % (bits, sorted_))
+
+
 @pytest.mark.parametrize("sorted_", (False, True))
 def test_index_past_the_weights_gives_zeros_and_is_reported(sorted_):
     E, N, K, bits, gs = 3, 64, 256, 4, 64
