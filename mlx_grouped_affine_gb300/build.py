@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(HERE, "libqmm.so")
-SOURCES = ("api.cpp", "tensormap.cpp", "dequant.cu", "gemv.cu", "gemv_f16.cu",
+SOURCES = ("api.cpp", "tensormap.cpp", "dequant.cu", "gemv.cu", "gemv_gather.cu", "gemv_f16.cu",
            "gemm_sm103.cu", "quantize.cu", "mm_f32.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

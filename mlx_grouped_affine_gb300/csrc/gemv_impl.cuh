@@ -1,6 +1,7 @@
 // Decode path of quantized_matmul (M <= 16): kernels and launchers,
-// templated on the 16-bit element type; included by gemv.cu (bf16) and
-// gemv_f16.cu (fp16), which compile in parallel.
+// templated on the 16-bit element type; included by gemv.cu (bf16 plain and
+// fused), gemv_gather.cu (bf16 gather_qmm) and gemv_f16.cu (fp16), which
+// compile in parallel.
 //
 // y = x . dequant(W)^T (transpose) or x . dequant(W) (nuvec_core
 // quantized.rs, `quantized_matmul`; spark_runtime weights/mlx_int8.rs,
@@ -36,6 +37,15 @@
 
 namespace qmm {
 namespace {
+
+// Eight words from p (32-byte aligned, read-only for the kernel's lifetime)
+// with one 256-bit load.
+__device__ __forceinline__ void ldg_v8(const void *p, uint32_t *v) {
+  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                 "=r"(v[6]), "=r"(v[7])
+               : "l"(p));
+}
 
 // d += A B on the tensor pipe, A and B of E (bf16 or fp16), fp32 accumulate.
 template <typename E>
@@ -486,6 +496,7 @@ struct TmaLayout {
   int xpitch;       // their pitch, bytes
   int red_off;      // offset of the reduction buffer
   int bar_off;      // offset of the chunk mbarriers
+  int x32;          // x starts on a 32-byte boundary: 256-bit x loads
 };
 
 // Warps per block: 16 for one n8 tile of x rows; 8 for two (twice the
@@ -499,7 +510,8 @@ constexpr int kTmaMaxChunksPerWarp = 4;
 // blocks per SM.)
 // W: warps per block (the default for NT, or 8 for one n8 tile: blocks of
 // 16K registers, four an SM, for weights with many row tiles).
-template <typename E, int BITS, int NT, bool OUT_BF16, bool GATHER, int FUSE, int W = tma_warps<NT>()>
+template <typename E, int BITS, int NT, bool OUT_BF16, bool GATHER, int FUSE, int W = tma_warps<NT>(),
+          bool X32 = false>
 __global__ void __launch_bounds__(32 * W, W < tma_warps<NT>() ? 4 : (GATHER || FUSE ? 2 : 0))
 gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayout L,
                   unsigned *err, GatherArgs ga, const __grid_constant__ CUtensorMap wmap2,
@@ -619,22 +631,39 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
     ac.y = yc;
     ac.M = mrows;
     // Lanes whose x row is beyond M keep zero fragments throughout.
-    auto load_x = [&](int c, uint32_t (&xv)[NT][16]) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int m = g + 8 * nt;
-        if (m < ac.M) {
+    auto load_x_nt = [&](int c, int nt, uint32_t (&xt)[16]) {
+      const int m = g + 8 * nt;
+      if (m < ac.M) {
+        if constexpr (FUSE == kFuseSilu) {
           const uint4 *xp =
-              FUSE == kFuseSilu
-                  ? reinterpret_cast<const uint4 *>(smem + L.x_off + m * L.xpitch + ((c << 7) + 32 * t) * 2)
-                  : reinterpret_cast<const uint4 *>(ac.x + static_cast<int64_t>(m) * a.K + k0 + (c << 7) + 32 * t);
+              reinterpret_cast<const uint4 *>(smem + L.x_off + m * L.xpitch + ((c << 7) + 32 * t) * 2);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const uint4 u = FUSE == kFuseSilu ? xp[i] : __ldg(xp + i);
-            xv[nt][4 * i] = u.x; xv[nt][4 * i + 1] = u.y; xv[nt][4 * i + 2] = u.z; xv[nt][4 * i + 3] = u.w;
+            const uint4 u = xp[i];
+            xt[4 * i] = u.x; xt[4 * i + 1] = u.y; xt[4 * i + 2] = u.z; xt[4 * i + 3] = u.w;
+          }
+        } else if ((NT == 1 && X32) || (NT == 2 && L.x32)) {
+          // Two 32-byte loads: each fills whole sectors, half the requests
+          // of 16-byte loads (at M > 8 the x reads set the L1's pace).  One
+          // n8 tile takes them only by its template flag: the branch alone
+          // costs 1 % at M = 1.
+          const uint16_t *xp = ac.x + static_cast<int64_t>(m) * a.K + k0 + (c << 7) + 32 * t;
+          ldg_v8(xp, &xt[0]);
+          ldg_v8(xp + 16, &xt[8]);
+        } else {
+          const uint4 *xp =
+              reinterpret_cast<const uint4 *>(ac.x + static_cast<int64_t>(m) * a.K + k0 + (c << 7) + 32 * t);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 u = __ldg(xp + i);
+            xt[4 * i] = u.x; xt[4 * i + 1] = u.y; xt[4 * i + 2] = u.z; xt[4 * i + 3] = u.w;
           }
         }
       }
+    };
+    auto load_x = [&](int c, uint32_t (&xv)[NT][16]) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) load_x_nt(c, nt, xv[nt]);
     };
     // silu fusion: before a warp reads chunk c's x, its 32 lanes form that
     // chunk's x = RN_bf16(silu(gate) * up) (fp32) in shared memory, 4 values
@@ -669,13 +698,24 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
         for (int i = 0; i < 4; ++i) acc[h][nt][i] = 0.0f;
 
     constexpr int kRowBytes = 16 * BITS;  // one row of a chunk box
+    // Two n8 tiles of x (M > 8): the next chunk's x is loaded while this one
+    // computes -- a tile's registers are reloaded as soon as its MMAs have
+    // read them, so the chunk's pairs are dequantized up front.  The MMAs
+    // then run tile by tile; each accumulator sees the same steps in the
+    // same order as below.  (Not for 8-bit gathers, which would spill.)
+    constexpr bool kPrefetchX = NT == 2 && FUSE != kFuseSilu && !(GATHER && BITS == 8);
+    if constexpr (kPrefetchX) {
+      if (warp < nchunks) load_x(warp, xv);
+    }
 #pragma unroll
     for (int j = 0; j < kTmaMaxChunksPerWarp; ++j) {
       const int c = warp + j * kW;
       if (!ok || c >= nchunks) break;
       const uint16_t *cur = sv[j];
-      stage_silu(c);
-      load_x(c, xv);
+      if constexpr (!kPrefetchX) {
+        stage_silu(c);
+        load_x(c, xv);
+      }
       uint32_t spins = 0;
       while (!mbar_try_wait(&bars[c], 0)) {
         if (++spins >= a.spin_limit) {
@@ -704,7 +744,38 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
       // The fast form is bf16's (fp16 has no room for its multipliers).
       bool fast = false;
       if constexpr (!E::kF16) fast = __all_sync(0xffffffffu, fast_scale(cur[0]) && fast_scale(cur[2]));
-      if (fast) {
+      if constexpr (kPrefetchX) {
+        uint32_t p0[16], p1[16];
+        if (fast) {
+          uint32_t m0[fast_slots<BITS>()], m1[fast_slots<BITS>()];
+          fast_muls<BITS>(cur[0], m0);
+          fast_muls<BITS>(cur[2], m1);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            p0[q] = pair_fast<BITS>(v0, q, m0, b0);
+            p1[q] = pair_fast<BITS>(v1, q, m1, b1);
+          }
+        } else {
+          const uint32_t s0 = bcast2(cur[0]), s1 = bcast2(cur[2]);
+          const float fs0 = E::to_f32(cur[0]), fb0 = E::to_f32(cur[1]);
+          const float fs1 = E::to_f32(cur[2]), fb1 = E::to_f32(cur[3]);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            p0[q] = pair_exact<BITS, E>(v0, q, s0, b0, fs0, fb0);
+            p1[q] = pair_exact<BITS, E>(v1, q, s1, b1, fs1, fb1);
+          }
+        }
+        const int cn = c + kW;
+        const bool more = j + 1 < kTmaMaxChunksPerWarp && cn < nchunks;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+            mma_16816<E>(acc[r & 1][nt], p0[2 * r], p1[2 * r], p0[2 * r + 1], p1[2 * r + 1],
+                         xv[nt][2 * r], xv[nt][2 * r + 1]);
+          if (more) load_x_nt(cn, nt, xv[nt]);
+        }
+      } else if (fast) {
         uint32_t m0[fast_slots<BITS>()], m1[fast_slots<BITS>()];
         fast_muls<BITS>(cur[0], m0);
         fast_muls<BITS>(cur[2], m1);
@@ -851,8 +922,11 @@ cudaError_t launch_t(const GemvArgs &a0, const Batches &b, cudaStream_t stream) 
   });
 }
 
+// Whether x starts on a 32-byte boundary (the decode's 32-byte x loads).
+inline bool x_aligned32(const void *x) { return (reinterpret_cast<uintptr_t>(x) & 31u) == 0; }
+
 template <typename E, int BITS, int NT, bool OUT_BF16, bool GATHER, int FUSE = kFuseNone,
-          int W = tma_warps<NT>()>
+          int W = tma_warps<NT>(), bool X32 = false>
 cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, const Batches &b, cudaStream_t stream,
                          const FuseArgs &f = FuseArgs{}, const uint32_t *w2 = nullptr) {
   const int64_t tiles = (a.N + 15) / 16;
@@ -880,6 +954,10 @@ cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, const Batches &b, cudaStre
   L.xpitch = FUSE == kFuseSilu ? L.kr * 2 + 16 : 0;
   L.red_off = L.x_off + a.M * L.xpitch;
   L.bar_off = L.red_off + W * NT * 4 * 32 * 4;
+  // Row and batch offsets of x are multiples of K (a multiple of 128), so the
+  // base decides the alignment of every lane's 32 values.
+  L.x32 = x_aligned32(a.x);
+  if (X32 && !L.x32) return cudaErrorInvalidValue;
   const size_t smem = L.bar_off + 8 * (nch + 1) + 1024;  // + slack for the 1024-byte base
   if (smem > 220 * 1024) return cudaErrorNotSupported;
   // The tensor map spans every weight batch: batch e's row n is row e*N + n.
@@ -900,7 +978,7 @@ cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, const Batches &b, cudaStre
   }
   unsigned *err = device_error_word();
   if (!err) return cudaErrorInvalidSymbol;
-  auto kern = gemv_t_tma_kernel<E, BITS, NT, OUT_BF16, GATHER, FUSE, W>;
+  auto kern = gemv_t_tma_kernel<E, BITS, NT, OUT_BF16, GATHER, FUSE, W, X32>;
   if (smem > 48 * 1024) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -941,13 +1019,28 @@ cudaError_t launch_bits(const GemvArgs &a, bool transpose, bool y_16, bool pdl,
     // 4096] 4-bit 13.1 -> 10.8 us, [11008, 4096] 3-bit 12.9 -> 11.6 us).  6 and
     // 8 bits keep 16 warps (6-bit 14.0 -> 14.6 us, 8-bit [14336, 4096] 15.2 ->
     // 18.4 us), as do one-wave shapes ([4096, 4096] 4.24 us against 4.83).
-    if (BITS < 6 && a.M <= 8 && (a.N + 15) / 16 > 2 * sm_count())
-      e = y_16 ? launch_t_tma<E, BITS, 1, true, false, kFuseNone, 8>(a, pdl, one, stream)
-               : launch_t_tma<E, BITS, 1, false, false, kFuseNone, 8>(a, pdl, one, stream);
-    else if (a.M <= 8)
-      e = y_16 ? launch_t_tma<E, BITS, 1, true, false>(a, pdl, one, stream)
-               : launch_t_tma<E, BITS, 1, false, false>(a, pdl, one, stream);
-    else
+    // At 2 <= M <= 8, 32-byte x loads when x allows them (M = 8 [4096, 4096]
+    // 4-bit 5.22 -> 4.61 us).
+    const bool wide = a.M > 1 && x_aligned32(a.x);
+    bool many = false;
+    if constexpr (BITS < 6) many = a.M <= 8 && (a.N + 15) / 16 > 2 * sm_count();
+    if (many) {
+      if constexpr (BITS < 6) {
+        if (wide)
+          e = y_16 ? launch_t_tma<E, BITS, 1, true, false, kFuseNone, 8, true>(a, pdl, one, stream)
+                   : launch_t_tma<E, BITS, 1, false, false, kFuseNone, 8, true>(a, pdl, one, stream);
+        else
+          e = y_16 ? launch_t_tma<E, BITS, 1, true, false, kFuseNone, 8>(a, pdl, one, stream)
+                   : launch_t_tma<E, BITS, 1, false, false, kFuseNone, 8>(a, pdl, one, stream);
+      }
+    } else if (a.M <= 8) {
+      if (wide)
+        e = y_16 ? launch_t_tma<E, BITS, 1, true, false, kFuseNone, tma_warps<1>(), true>(a, pdl, one, stream)
+                 : launch_t_tma<E, BITS, 1, false, false, kFuseNone, tma_warps<1>(), true>(a, pdl, one, stream);
+      else
+        e = y_16 ? launch_t_tma<E, BITS, 1, true, false>(a, pdl, one, stream)
+                 : launch_t_tma<E, BITS, 1, false, false>(a, pdl, one, stream);
+    } else
       e = y_16 ? launch_t_tma<E, BITS, 2, true, false>(a, pdl, one, stream)
                : launch_t_tma<E, BITS, 2, false, false>(a, pdl, one, stream);
     if (e != cudaErrorNotSupported) return e;

@@ -185,3 +185,27 @@ def test_chained_launches_with_programmatic_dependent_launch(bits):
         x_in = ys[i].cpu().numpy().view(np.uint16)
         ref, absy = oracle.qmm(x_in, 1, w.packed, w.scales, w.biases, N, K, True, 64, bits)
         assert_within_tolerance(ys[i + 1], ref, absy, "link %d" % i)
+
+
+@pytest.mark.parametrize("M", (1, 4, 16))
+@pytest.mark.parametrize("bits", (4, 8))
+def test_x_on_a_16_byte_boundary(bits, M):
+    # x 16- but not 32-byte aligned takes 16-byte loads instead of 32-byte
+    # ones (M > 1); the results are the same bits as from an aligned x.
+    N, K = 512, 1024
+    w = synth.quant_weight(900 + bits, N, K, bits, 64)
+    x = synth.x_bf16(901 + M, M, K)
+    pw, ps, pb = weight(w)
+    buf = torch.zeros(M * K + 16, dtype=torch.int16, device="cuda")
+    xs = []
+    for off in (0, 8):  # elements: 0 and 16 bytes past a 512-byte aligned base
+        assert (buf.data_ptr() + 2 * off) % 32 == (16 if off else 0)
+        buf[off:off + M * K] = dev(x).reshape(-1)
+        y = empty_out((M, N), qmm.QMM_F32)
+        qmm.qmm_quantized_matmul(buf[off:off + M * K], M, pw, ps, pb, N, K, 1, 64, bits, y,
+                                 qmm.QMM_F32)
+        torch.cuda.synchronize()
+        xs.append(y.cpu().numpy())
+    assert np.array_equal(xs[0].view(np.uint32), xs[1].view(np.uint32))
+    ref, absy = oracle.qmm(x, M, w.packed, w.scales, w.biases, N, K, True, 64, bits)
+    assert_within_tolerance(torch.from_numpy(xs[1]), ref, absy, "16-byte x bits=%d M=%d" % (bits, M))
