@@ -792,7 +792,8 @@ PROFILE_CASES = {
     "decode_many_tiles": (1, 14336, 4096, 4, 64, True),
 }
 OTHER_PROFILES = ("gather_sorted", "silu_gate", "quantize", "dequantize", "rows", "f16_prefill",
-                  "f16_decode", "f32_decode", "f32_decode16", "f32_prefill", "gather_prefill")
+                  "f16_decode", "f32_decode", "f32_decode16", "f32_prefill", "gather_prefill",
+                  "odd_widths")
 
 
 def run_other_profile(case, launches):
@@ -865,6 +866,20 @@ def run_other_profile(case, launches):
         y = torch.empty((M, N), dtype=torch.float32 if d == "f32" else torch.int16, device="cuda")
         for i in range(launches):
             qmm.qmm_quantized_matmul_typed(x, Q, M, *ws[i % R], Q, N, K, 1, 64, 4, y, Q)
+    elif case == "odd_widths":
+        # The odd-width decode lines at M = 1, each width `launches` times in
+        # turn over two weight copies (> L2 together at every width).
+        N, K = synth.ODD_SHAPE
+        x = dev(synth.x_bf16(61, 1, K))
+        y = torch.empty((1, N), dtype=torch.int16, device="cuda")
+        for bits in synth.ODD_BITS:
+            for g in synth.ODD_GROUPS:
+                w = synth.quant_weight(60 + bits + g, N, K, bits, g)
+                R = max(2, -(-int(1.5 * L2_BYTES) // w.nbytes))
+                ws = [tuple(dev(np.roll(a, r, 0)) for a in (w.packed, w.scales, w.biases)) for r in range(R)]
+                for i in range(launches):
+                    qmm.qmm_quantized_matmul(x, 1, *ws[i % R], N, K, 1, g, bits, y, qmm.QMM_BF16)
+                del ws
     elif case == "rows":
         T, C = synth.ROWS_TABLE
         w = synth.quant_weight(2, T, C, 4, 64)
