@@ -492,7 +492,7 @@ __device__ __forceinline__ uint32_t silu_mul2(uint32_t g2, uint32_t u2) {
 struct TmaLayout {
   int kr;           // codes per block (multiple of 128)
   int box_bytes;    // shared bytes of one chunk box
-  int x_off;        // offset of the staged x rows
+  int x_off;        // offset of the x rows formed in shared memory (silu fusion)
   int xpitch;       // their pitch, bytes
   int red_off;      // offset of the reduction buffer
   int bar_off;      // offset of the chunk mbarriers
@@ -509,7 +509,9 @@ constexpr int kTmaMaxChunksPerWarp = 4;
 // no minimum given; the gather and fused instantiations are held to two
 // blocks per SM.)
 // W: warps per block (the default for NT, or 8 for one n8 tile: blocks of
-// 16K registers, four an SM, for weights with many row tiles).
+// 16K registers, four an SM, for weights with many row tiles).  X32: one n8
+// tile reads x with 32-byte loads (the launcher takes it at 2 <= M <= 8 when
+// x is 32-byte aligned; two tiles decide at run time from L.x32).
 template <typename E, int BITS, int NT, bool OUT_BF16, bool GATHER, int FUSE, int W = tma_warps<NT>(),
           bool X32 = false>
 __global__ void __launch_bounds__(32 * W, W < tma_warps<NT>() ? 4 : (GATHER || FUSE ? 2 : 0))
@@ -579,7 +581,7 @@ gemv_t_tma_kernel(const __grid_constant__ CUtensorMap wmap, GemvArgs a, TmaLayou
   }
 
   if (warp == 0) {
-    for (int c = lane; c <= nchunks; c += 32) mbar_init(&bars[c], 1);  // chunks, then x
+    for (int c = lane; c < nchunks; c += 32) mbar_init(&bars[c], 1);  // one per chunk
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -958,7 +960,7 @@ cudaError_t launch_t_tma(const GemvArgs &a, bool pdl, const Batches &b, cudaStre
   // base decides the alignment of every lane's 32 values.
   L.x32 = x_aligned32(a.x);
   if (X32 && !L.x32) return cudaErrorInvalidValue;
-  const size_t smem = L.bar_off + 8 * (nch + 1) + 1024;  // + slack for the 1024-byte base
+  const size_t smem = L.bar_off + 8 * nch + 1024;  // + slack for the 1024-byte base
   if (smem > 220 * 1024) return cudaErrorNotSupported;
   // The tensor map spans every weight batch: batch e's row n is row e*N + n.
   const uint64_t map_rows = static_cast<uint64_t>(a.N) * (GATHER ? b.g.w_batches : 1);
