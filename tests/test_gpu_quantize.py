@@ -52,6 +52,22 @@ def test_quantize_constant_and_mixed_groups(bits):
     check(w, rows, cols, gs, bits, "constant/mixed bits=%d" % bits)
 
 
+@pytest.mark.parametrize("bits", (2, 4, 8))
+def test_quantize_signed_zero_minimum(bits):
+    # Groups whose minimum is zero with both signs present: the minimum is
+    # compared in the group's order, so the stored bias keeps the sign of the
+    # first zero, and every code follows from it.  Row 0: -0 before +0; row 1:
+    # +0 before -0; row 2: all zeros of mixed sign (a constant group).
+    rows, cols, gs = 3, 128, 64
+    w = synth.x_bf16(97 + bits, rows, cols) & np.uint16(0x7FFF)  # |x|: non-negative
+    w[0, 3], w[0, 9] = 0x8000, 0x0000
+    w[0, 64 + 1], w[0, 64 + 2] = 0x8000, 0x0000
+    w[1, 5], w[1, 6] = 0x0000, 0x8000
+    w[1, 64 + 0], w[1, 64 + 40] = 0x0000, 0x8000
+    w[2, :] = np.where(np.arange(cols) % 3 == 0, 0x8000, 0x0000).astype(np.uint16)
+    check(w, rows, cols, gs, bits, "signed zeros bits=%d" % bits)
+
+
 def test_quantize_full_size_weight():
     rows, cols = 4096, 4096
     w = synth.x_bf16(95, rows, cols)
