@@ -32,13 +32,14 @@ constexpr int kThreads = 256;
 // both round to the same integer; those few elements, and every element of a
 // group whose reciprocal is not finite (the comparison is false for NaN),
 // take the correctly rounded division.
+// Codes stay below 2^9, so for |q| < 512 the margin |q| 2^-20 is below 2^-11
+// and a fixed one serves: q - n is exact (n is q's nearest integer), and
+// |q - n| < 1/2 - 2^-11 keeps q more than 2^-11 from the half-integer between
+// n and its neighbour on q's side.
 __device__ __forceinline__ float rint_quotient(float d, float s, float r) {
   const float q = __fmul_rn(d, r);
   const float n = rintf(q);
-  // q - n is exact (|q| is far below 2^23 and n is its nearest integer); its
-  // distance from +-1/2 is q's distance from the half-integer between n and
-  // its neighbour on q's side.
-  if (0.5f - fabsf(q - n) > fabsf(q) * 0x1p-20f + 0x1p-40f) return n;
+  if (fabsf(q - n) < 0.5f - 0x1p-11f && fabsf(q) < 512.0f) return n;
   return rintf(__fdiv_rn(d, s));
 }
 
@@ -91,8 +92,13 @@ quantize_kernel(const void *__restrict__ w, uint32_t total, uint32_t groups_per_
     const uint32_t r = gid / groups_per_row, j = gid - r * groups_per_row;
     const void *src = static_cast<const char *>(w) +
                       (static_cast<int64_t>(r) * cols + static_cast<int64_t>(j) * G) * ESZ;
-    // Minimum and maximum, compared in the group's order.
-    float lo = 0.0f, hi = 0.0f;
+    // Minimum and maximum as compared in the group's order (a value replaces
+    // the running one only when strictly smaller / larger): the first element
+    // that attains each.  fminf / fmaxf skip NaNs the same way, except a NaN
+    // first element, which the ordered comparison keeps; and they may return
+    // either zero when both signs occur, so a zero extremum is taken again as
+    // the first zero of the group.
+    float lo = 0.0f, hi = 0.0f, first = 0.0f;
 #pragma unroll
     for (int q = 0; q < G / 8; ++q) {
       float v[8];
@@ -100,12 +106,28 @@ quantize_kernel(const void *__restrict__ w, uint32_t total, uint32_t groups_per_
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         if (q == 0 && e == 0) {
-          lo = hi = v[0];
+          lo = hi = first = v[0];
         } else {
-          if (v[e] < lo) lo = v[e];
-          if (v[e] > hi) hi = v[e];
+          lo = fminf(lo, v[e]);
+          hi = fmaxf(hi, v[e]);
         }
       }
+    }
+    if (first != first) {
+      lo = hi = first;
+    } else if (lo == 0.0f || hi == 0.0f) {
+      float z = 0.0f;
+      for (int q = 0; q < G / 8; ++q) {
+        float v[8];
+        load8<WT>(src, q, v);
+        bool found = false;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (!found && v[e] == 0.0f) { z = v[e]; found = true; }
+        if (found) break;
+      }
+      if (lo == 0.0f) lo = z;
+      if (hi == 0.0f) hi = z;
     }
     const int64_t o = static_cast<int64_t>(r) * groups_per_row + j;
     const float s = store_value<WT>(scales, o, __fdiv_rn(__fsub_rn(hi, lo), static_cast<float>(TOP)));
