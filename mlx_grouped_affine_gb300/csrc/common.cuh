@@ -165,6 +165,20 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t *v, int j) {
   return __funnelshift_r(v[word], v[word + 1], sh) & mask;
 }
 
+// Codes j and j+1 (j even) of a little-endian bit stream held in words v[],
+// as code j in bits [0, BITS) and code j+1 in bits [16, 16 + BITS), the rest
+// zero: one (funnel) shift brings the pair's 2*BITS bits to the bottom, a
+// copy shifted by 16 - BITS carries the second code into the high half, and
+// one select-and-mask keeps each half's code.
+template <int BITS>
+__device__ __forceinline__ uint32_t pair_at(const uint32_t *v, int j) {
+  const int bit = j * BITS, word = bit >> 5, sh = bit & 31;
+  const uint32_t y = sh + 2 * BITS <= 32 ? v[word] >> sh : __funnelshift_r(v[word], v[word + 1], sh);
+  constexpr uint32_t lo = (1u << BITS) - 1u, hi = lo << 16;
+  // low half from y, high half from the shifted copy, then the two code fields
+  return ((y & lo) | ((y << (16 - BITS)) & hi));
+}
+
 // Dequantize the 2*NP codes held in v[] (bit stream, LSB first) to NP
 // natural pairs of E (code 2i in the low half, 2i+1 in the high half), each
 // RN(s*c + b).  s2, b2 are (s, s) and (b, b) as E pairs; sf, bf the same in
@@ -210,7 +224,7 @@ __device__ __forceinline__ void dequant_pairs(const uint32_t *v, uint32_t s2, ui
   } else {
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
-      const uint32_t p = code_at<BITS>(v, 2 * i) | (code_at<BITS>(v, 2 * i + 1) << 16) | E::kMagic2;
+      const uint32_t p = pair_at<BITS>(v, 2 * i) | E::kMagic2;
       out[i] = E::fma2(E::sub2(p, E::kMagic2), s2, b2);
     }
   }
@@ -281,7 +295,7 @@ __device__ __forceinline__ uint32_t pair_fast(const uint32_t *v, int p,
     const uint32_t t = prmt(v[p >> 4], 0u, 0x4040u | j | (j << 8)) & (0x00020001u << (2 * k));
     return bf16x2_fma(t, m[k], b2);
   } else {
-    const uint32_t t = code_at<BITS>(v, 2 * p) | (code_at<BITS>(v, 2 * p + 1) << 16);
+    const uint32_t t = pair_at<BITS>(v, 2 * p);
     return bf16x2_fma(t, m[0], b2);
   }
 }
@@ -306,7 +320,7 @@ __device__ __forceinline__ uint32_t pair_exact(const uint32_t *v, int p, uint32_
     const uint32_t q = and_or(prmt(w, w >> 4, 0x0400u | j | (j << 8)), 0x000F000Fu, E::kMagic2);
     return E::fma2(E::sub2(q, E::kMagic2), s2, b2);
   } else {
-    const uint32_t q = code_at<BITS>(v, 2 * p) | (code_at<BITS>(v, 2 * p + 1) << 16) | E::kMagic2;
+    const uint32_t q = pair_at<BITS>(v, 2 * p) | E::kMagic2;
     return E::fma2(E::sub2(q, E::kMagic2), s2, b2);
   }
 }
